@@ -1,0 +1,405 @@
+// api.cpp -- the C ABI of libll.so (declared in include/ll.h): argument and
+// shape checks, library memory, the RoPE table, schedule upload, launches and
+// status handling.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ll_internal.h"
+
+using ll::Instr;
+using ll::KParams;
+
+struct ll_handle {
+    ll_config cfg{};
+    int device = 0;
+    int nsm = 0;
+    int splits = 1;
+    int smem_bytes = 0;
+    cudaStream_t stream = nullptr;
+    uint8_t *dmem = nullptr;
+    size_t dmem_bytes = 0;
+    KParams kp{};
+    ll::ChainBufs cb{};
+    std::vector<ll::LayerW> host_layers;
+    std::vector<std::vector<Instr>> lists;
+    Instr *d_instrs = nullptr;
+    int max_instr = 0;
+    uint32_t epoch = 0;
+    int32_t *pinned = nullptr;  // [0] next token, [1] status
+    std::string err;
+};
+
+namespace {
+
+thread_local std::string g_init_error;
+
+int fail(ll_handle *h, int code, const std::string &msg) {
+    if (h) h->err = msg;
+    return code;
+}
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+int upload_schedule(ll_handle *h) {
+    std::vector<Instr> flat(size_t(h->nsm) * h->max_instr);
+    std::vector<int32_t> counts(h->nsm);
+    for (int sm = 0; sm < h->nsm; sm++) {
+        counts[sm] = static_cast<int32_t>(h->lists[sm].size());
+        std::copy(h->lists[sm].begin(), h->lists[sm].end(), flat.begin() + size_t(sm) * h->max_instr);
+    }
+    if (cudaMemcpy(h->d_instrs, flat.data(), flat.size() * sizeof(Instr), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(const_cast<int32_t *>(h->kp.n_instr), counts.data(), counts.size() * sizeof(int32_t),
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+        return fail(h, LL_ERR_CUDA, "schedule upload failed");
+    return LL_OK;
+}
+
+void build_lists(ll_handle *h) {
+    const ll_config &c = h->cfg;
+    ll::build_schedule(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim, c.inter,
+                       c.vocab, c.n_kv_heads, h->nsm, h->splits, h->lists);
+}
+
+// Clear counters and the status word after a failed step so the next starts clean.
+int reset_device_state(ll_handle *h) {
+    const size_t nctr = size_t(ll::CtrLayout::count(h->cfg.n_layers, h->cfg.n_kv_heads)) * ll::CTR_STRIDE;
+    if (cudaMemsetAsync(h->kp.ctr, 0, nctr * sizeof(uint32_t), h->stream) != cudaSuccess ||
+        cudaMemsetAsync(h->kp.status, 0, sizeof(int32_t), h->stream) != cudaSuccess ||
+        cudaStreamSynchronize(h->stream) != cudaSuccess)
+        return LL_ERR_CUDA;
+    h->epoch = 0;
+    return LL_OK;
+}
+
+int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, float *logits,
+            int32_t *next_token_dev) {
+    if (pos < 0 || pos >= h->cfg.max_seq)
+        return fail(h, LL_ERR_ARG, "pos " + std::to_string(pos) + " outside [0, max_seq)");
+    if (logits && !aligned16(logits)) return fail(h, LL_ERR_ARG, "logits buffer not 16-byte aligned");
+    KParams p = h->kp;
+    p.token = token;
+    p.token_dev = token_dev;
+    p.pos = pos;
+    p.logits = logits;
+    p.next_token_dev = next_token_dev;
+    p.epoch = ++h->epoch;
+    int rc;
+    if (h->cfg.backend == LL_BACKEND_CHAIN) rc = ll::launch_chain_step(p, h->cb, h->stream);
+    else rc = ll::launch_megakernel(p, h->stream, h->smem_bytes);
+    if (rc != LL_OK) {
+        cudaError_t e = cudaGetLastError();
+        return fail(h, rc, std::string("kernel launch failed: ") + cudaGetErrorString(e));
+    }
+    return LL_OK;
+}
+
+const char *status_text(int s) {
+    switch (s) {
+        case LL_ERR_ARG: return "token out of range";
+        case LL_ERR_DEP_TIMEOUT: return "a device-side wait ran past its time limit";
+        default: return "device error";
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ll_init_error(void) { return g_init_error.c_str(); }
+
+int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16_t *v_cache, void *stream,
+            ll_handle **out) {
+    g_init_error.clear();
+    auto bad = [&](int code, const std::string &msg) {
+        g_init_error = msg;
+        return code;
+    };
+    if (!out) return bad(LL_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (!cfg || !w) return bad(LL_ERR_ARG, "cfg or weights is NULL");
+    const ll_config c = *cfg;
+    // ---- shape checks
+    if (c.n_layers < 1 || c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.inter <= 0 ||
+        c.vocab <= 0 || c.max_seq <= 0)
+        return bad(LL_ERR_SHAPE, "every size must be positive");
+    if (c.head_dim != 64 && c.head_dim != 128) return bad(LL_ERR_SHAPE, "head_dim must be 64 or 128");
+    if (c.n_q_heads % c.n_kv_heads != 0 || c.n_q_heads / c.n_kv_heads > ll::MAX_GQA)
+        return bad(LL_ERR_SHAPE, "n_q_heads must be a multiple (at most 8x) of n_kv_heads");
+    if (c.backend != LL_BACKEND_MEGAKERNEL && c.backend != LL_BACKEND_CHAIN)
+        return bad(LL_ERR_ARG, "unknown backend");
+    if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad(LL_ERR_ARG, "rms_eps/rope_theta invalid");
+    ll::MvShape mh{}, mq{}, mi{};
+    if (!ll::mv_shape(c.hidden, mh) || !ll::mv_shape(c.n_q_heads * c.head_dim, mq) || !ll::mv_shape(c.inter, mi))
+        return bad(LL_ERR_SHAPE, "hidden, n_q_heads*head_dim and inter must be multiples of 256, at most 16384");
+    // ---- pointer checks
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return bad(LL_ERR_ARG, "KV caches must be 16-byte aligned");
+    if (!aligned16(w->embed) || !aligned16(w->final_norm)) return bad(LL_ERR_ARG, "embed/final_norm not 16-byte aligned");
+    if (!c.tied && !aligned16(w->lm_head)) return bad(LL_ERR_ARG, "lm_head not 16-byte aligned");
+    const uint16_t *const *lp[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->wg, w->wu, w->wd};
+    for (auto a : lp)
+        if (!a) return bad(LL_ERR_ARG, "a per-layer pointer array is NULL");
+    std::vector<ll::LayerW> layers(c.n_layers);
+    for (int l = 0; l < c.n_layers; l++) {
+        ll::LayerW &L = layers[l];
+        L = {w->attn_norm[l], w->wq[l], w->wk[l], w->wv[l], w->wo[l], w->mlp_norm[l], w->wg[l], w->wu[l], w->wd[l]};
+        const uint16_t *all[9] = {L.attn_norm, L.wq, L.wk, L.wv, L.wo, L.mlp_norm, L.wg, L.wu, L.wd};
+        for (auto a : all)
+            if (!aligned16(a)) return bad(LL_ERR_ARG, "layer " + std::to_string(l) + " weight not 16-byte aligned");
+    }
+    // ---- device checks
+    int dev = 0;
+    cudaDeviceProp prop{};
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return bad(LL_ERR_CUDA, "no CUDA device");
+    if (prop.major != 10 || prop.minor != 3)
+        return bad(LL_ERR_DEVICE, "device is sm_" + std::to_string(prop.major) + std::to_string(prop.minor) +
+                                      ", this library is built for sm_103a");
+    if (!prop.cooperativeLaunch) return bad(LL_ERR_DEVICE, "device lacks cooperative launch");
+
+    ll_handle *h = new ll_handle();
+    h->cfg = c;
+    h->device = dev;
+    h->nsm = prop.multiProcessorCount;
+    h->stream = static_cast<cudaStream_t>(stream);
+    h->splits = std::max(1, h->nsm / c.n_kv_heads);
+    h->smem_bytes = ll::megakernel_smem_bytes();
+    h->host_layers = layers;
+    const int qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+    if ((c.inter + h->nsm - 1) / h->nsm > ll::GBUF_FLOATS) {
+        delete h;
+        return bad(LL_ERR_SHAPE, "inter too large for the SM count");
+    }
+    int rc = ll::megakernel_prepare(h->smem_bytes);
+    if (rc != LL_OK) {
+        delete h;
+        return bad(rc, "cannot keep one megakernel block resident per SM");
+    }
+    build_lists(h);
+    for (auto &l : h->lists) h->max_instr = std::max<int>(h->max_instr, static_cast<int>(l.size()));
+
+    // ---- library memory: one allocation carved into 256-byte aligned pieces
+    const size_t nctr = size_t(ll::CtrLayout::count(c.n_layers, c.n_kv_heads)) * ll::CTR_STRIDE;
+    struct Piece { void **dst; size_t bytes; };
+    Instr *d_instrs = nullptr;
+    int32_t *d_n_instr = nullptr;
+    ll::LayerW *d_layers = nullptr;
+    float2 *d_rope = nullptr;
+    float *x = nullptr, *qkv = nullptr, *part = nullptr, *o = nullptr, *act = nullptr;
+    float *hbuf = nullptr, *gate = nullptr, *up = nullptr, *logits = nullptr;
+    unsigned long long *keys = nullptr;
+    uint32_t *ctr = nullptr;
+    int32_t *status = nullptr, *tok = nullptr;
+    const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 2);
+    Piece pieces[] = {
+        {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
+        {reinterpret_cast<void **>(&d_n_instr), size_t(h->nsm) * sizeof(int32_t)},
+        {reinterpret_cast<void **>(&d_layers), size_t(c.n_layers) * sizeof(ll::LayerW)},
+        {reinterpret_cast<void **>(&d_rope), size_t(c.max_seq) * (c.head_dim / 2) * sizeof(float2)},
+        {reinterpret_cast<void **>(&x), size_t(c.hidden) * 4},
+        {reinterpret_cast<void **>(&qkv), size_t(qd + 2 * kd) * 4},
+        {reinterpret_cast<void **>(&part), part_floats * 4},
+        {reinterpret_cast<void **>(&o), size_t(qd) * 4},
+        {reinterpret_cast<void **>(&act), size_t(c.inter) * 4},
+        {reinterpret_cast<void **>(&hbuf), size_t(c.hidden) * 4},
+        {reinterpret_cast<void **>(&gate), size_t(c.inter) * 4},
+        {reinterpret_cast<void **>(&up), size_t(c.inter) * 4},
+        {reinterpret_cast<void **>(&logits), size_t(c.vocab) * 4},
+        {reinterpret_cast<void **>(&keys), size_t(h->nsm) * 8},
+        {reinterpret_cast<void **>(&ctr), nctr * 4},
+        {reinterpret_cast<void **>(&status), 4},
+        {reinterpret_cast<void **>(&tok), 4},
+    };
+    size_t total = 0;
+    for (auto &pc : pieces) total += round_up(pc.bytes, 256);
+    if (cudaMalloc(&h->dmem, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return bad(LL_ERR_OOM, "cudaMalloc of " + std::to_string(total) + " bytes failed");
+    }
+    h->dmem_bytes = total;
+    size_t off = 0;
+    for (auto &pc : pieces) {
+        *pc.dst = h->dmem + off;
+        off += round_up(pc.bytes, 256);
+    }
+    if (cudaMallocHost(&h->pinned, 2 * sizeof(int32_t)) != cudaSuccess) {
+        cudaFree(h->dmem);
+        delete h;
+        return bad(LL_ERR_OOM, "pinned host buffer allocation failed");
+    }
+
+    // RoPE table: angle pos * theta^(-2i/hd) taken in double, stored as float (cos, sin).
+    const int half = c.head_dim / 2;
+    std::vector<float2> rope(size_t(c.max_seq) * half);
+    for (int i = 0; i < half; i++) {
+        const double inv = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / c.head_dim);
+        for (int pos = 0; pos < c.max_seq; pos++) {
+            const double a = pos * inv;
+            rope[size_t(pos) * half + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+        }
+    }
+
+    KParams &p = h->kp;
+    p.instrs = d_instrs;
+    p.n_instr = d_n_instr;
+    p.max_instr = h->max_instr;
+    p.nsm = h->nsm;
+    p.layers = d_layers;
+    p.embed = w->embed;
+    p.lm_head = c.tied ? w->embed : w->lm_head;
+    p.final_norm = w->final_norm;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.rope_cs = d_rope;
+    p.L = c.n_layers;
+    p.H = c.hidden;
+    p.nq = c.n_q_heads;
+    p.nkv = c.n_kv_heads;
+    p.hd = c.head_dim;
+    p.I = c.inter;
+    p.V = c.vocab;
+    p.max_seq = c.max_seq;
+    p.eps = c.rms_eps;
+    p.attn_splits = h->splits;
+    p.mv_h = mh;
+    p.mv_q = mq;
+    p.mv_i = mi;
+    p.x = x;
+    p.qkv = qkv;
+    p.part = part;
+    p.o = o;
+    p.act = act;
+    p.lm_keys = keys;
+    p.ctr = ctr;
+    p.status = status;
+    p.token_out = tok;
+    p.timeout_ns = 1000000000ull;
+    h->d_instrs = d_instrs;
+
+    ll::ChainBufs &cb = h->cb;
+    cb.host_layers = h->host_layers.data();
+    cb.x = x;
+    cb.h = hbuf;
+    cb.qkv = qkv;
+    cb.part = part;
+    cb.o = o;
+    cb.gate = gate;
+    cb.up = up;
+    cb.act = act;
+    cb.logits = logits;
+    cb.splits = h->splits;
+
+    bool ok = cudaMemcpy(d_layers, layers.data(), layers.size() * sizeof(ll::LayerW), cudaMemcpyHostToDevice) ==
+                  cudaSuccess &&
+              cudaMemcpy(d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemset(ctr, 0, nctr * 4) == cudaSuccess && cudaMemset(status, 0, 4) == cudaSuccess &&
+              cudaMemset(tok, 0, 4) == cudaSuccess;
+    if (!ok || upload_schedule(h) != LL_OK) {
+        ll_free(h);
+        return bad(LL_ERR_CUDA, "initial upload failed");
+    }
+    *out = h;
+    return LL_OK;
+}
+
+int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev, int32_t *next_token_host) {
+    if (!h) return LL_ERR_ARG;
+    if (token < 0 || token >= h->cfg.vocab) return fail(h, LL_ERR_ARG, "token " + std::to_string(token) + " outside [0, vocab)");
+    int rc = enqueue(h, token, nullptr, pos, logits_dev, nullptr);
+    if (rc != LL_OK) return rc;
+    if (cudaMemcpyAsync(h->pinned, h->kp.token_out, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
+        cudaMemcpyAsync(h->pinned + 1, h->kp.status, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
+        cudaStreamSynchronize(h->stream) != cudaSuccess) {
+        cudaError_t e = cudaGetLastError();
+        return fail(h, LL_ERR_CUDA, std::string("step failed: ") + cudaGetErrorString(e));
+    }
+    const int32_t st = h->pinned[1];
+    if (st != 0) {
+        reset_device_state(h);
+        return fail(h, st, status_text(st));
+    }
+    if (next_token_host) *next_token_host = h->pinned[0];
+    return LL_OK;
+}
+
+int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,
+                         int32_t *next_token_dev) {
+    if (!h) return LL_ERR_ARG;
+    if (!token_dev) return fail(h, LL_ERR_ARG, "token_dev is NULL");
+    return enqueue(h, 0, token_dev, pos, logits_dev, next_token_dev);
+}
+
+int ll_synchronize(ll_handle *h) {
+    if (!h) return LL_ERR_ARG;
+    if (cudaMemcpyAsync(h->pinned + 1, h->kp.status, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
+        cudaStreamSynchronize(h->stream) != cudaSuccess) {
+        cudaError_t e = cudaGetLastError();
+        return fail(h, LL_ERR_CUDA, std::string("synchronize failed: ") + cudaGetErrorString(e));
+    }
+    const int32_t st = h->pinned[1];
+    if (st != 0) {
+        reset_device_state(h);
+        return fail(h, st, status_text(st));
+    }
+    return LL_OK;
+}
+
+int ll_set_timeout_ns(ll_handle *h, uint64_t ns) {
+    if (!h || ns == 0) return LL_ERR_ARG;
+    h->kp.timeout_ns = ns;
+    return LL_OK;
+}
+
+int ll_query(const ll_handle *h, int what, int64_t *value) {
+    if (!h || !value) return LL_ERR_ARG;
+    switch (what) {
+        case LL_Q_NUM_SMS: *value = h->nsm; break;
+        case LL_Q_ATTN_SPLITS: *value = h->splits; break;
+        case LL_Q_PAGE_BYTES: *value = ll::PAGE_BYTES; break;
+        case LL_Q_NUM_PAGES: *value = ll::NPAGES; break;
+        case LL_Q_SCRATCH_BYTES: *value = static_cast<int64_t>(h->dmem_bytes); break;
+        case LL_Q_MAX_INSTRS: *value = h->max_instr; break;
+        case LL_Q_LAUNCHES_PER_STEP:
+            *value = h->cfg.backend == LL_BACKEND_CHAIN ? 1 + 13 * int64_t(h->cfg.n_layers) + 3 : 1;
+            break;
+        case LL_Q_SMEM_BYTES: *value = h->smem_bytes; break;
+        default: return LL_ERR_ARG;
+    }
+    return LL_OK;
+}
+
+int ll_debug_inject(ll_handle *h, int kind, int layer, int op) {
+    if (!h) return LL_ERR_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return fail(h, LL_ERR_CUDA, "synchronize failed");
+    build_lists(h);
+    if (kind == LL_FAULT_DROP_SIGNAL) {
+        if (layer < 0 || layer >= h->cfg.n_layers || op < ll::OP_QKV || op > ll::OP_DOWN)
+            return fail(h, LL_ERR_ARG, "fault target out of range");
+        for (auto &list : h->lists)
+            for (auto &in : list)
+                if (in.layer == layer && in.op == op) in.sig_ctr = -1;
+    } else if (kind != LL_FAULT_NONE) {
+        return fail(h, LL_ERR_ARG, "unknown fault kind");
+    }
+    return upload_schedule(h);
+}
+
+const char *ll_last_error(const ll_handle *h) { return h ? h->err.c_str() : "null handle"; }
+
+void ll_free(ll_handle *h) {
+    if (!h) return;
+    cudaStreamSynchronize(h->stream);
+    if (h->dmem) cudaFree(h->dmem);
+    if (h->pinned) cudaFreeHost(h->pinned);
+    delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// ll_internal.h -- structures shared by the host runtime (api.cpp, schedule.cpp)
+// and the device code (megakernel.cu, chain.cu) of libll.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/ll.h"
+
+namespace ll {
+
+// ---- persistent-kernel geometry -------------------------------------------------
+// One block per SM: NCW consumer warps compute, one producer warp streams bytes
+// from HBM into a ring of NPAGES shared-memory pages of PAGE_BYTES each.
+constexpr int NCW = 8;
+constexpr int NCT = NCW * 32;              // consumer threads
+constexpr int NTHREADS = NCT + 32;         // + producer warp
+constexpr int PAGE_BYTES = 32768;
+constexpr int NPAGES = 6;
+constexpr int MAX_VPL = 8;                 // 16-byte weight vectors per lane per row
+constexpr int MAX_GQA = 8;                 // query heads per KV head
+constexpr int MAX_HD = 128;
+constexpr int MAX_RPP = 64;                // rows per page (hidden 256 at one vector per lane)
+constexpr int GBUF_FLOATS = 1024;          // gate results held per SM between gate and up rows
+
+// Instruction kinds, in the order they appear within a layer.
+enum Op : uint8_t { OP_QKV = 0, OP_ATTN = 1, OP_OPROJ = 2, OP_GATEUP = 3, OP_DOWN = 4, OP_LMHEAD = 5 };
+
+// One entry of an SM's instruction list. For matrix-vector instructions
+// [r0, r1) is the SM's row range (for QKV in the stacked [q; k; v] rows, for
+// gate/up in the intermediate rows of both matrices); for attention r0 is the KV
+// head and r1 the split index.
+struct Instr {
+    uint8_t op;
+    uint8_t pad;
+    uint16_t layer;
+    int32_t r0, r1;
+    int32_t wait_ctr;     // counter to wait on, -1 for none
+    uint32_t wait_count;  // its increments per step (target = epoch * wait_count)
+    int32_t sig_ctr;      // counter to bump when done, -1 for none
+};
+
+// Matrix-vector geometry for one input width K: ws warps share a row, each lane
+// holds vpl 16-byte vectors (8 elements) of the input, rpp rows fill a page.
+struct MvShape {
+    int32_t K, ws, vpl, rpp;
+};
+
+struct LayerW {
+    const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
+};
+
+// Counters, each on its own 128-byte line.
+constexpr int CTR_STRIDE = 32;  // uint32 per counter slot
+struct CtrLayout {
+    // per layer: qkv, attn, oproj, gateup, down; then per (layer, kv head) a ticket
+    static __host__ __device__ inline int qkv(int l) { return l * 5 + 0; }
+    static __host__ __device__ inline int attn(int l) { return l * 5 + 1; }
+    static __host__ __device__ inline int oproj(int l) { return l * 5 + 2; }
+    static __host__ __device__ inline int gateup(int l) { return l * 5 + 3; }
+    static __host__ __device__ inline int down(int l) { return l * 5 + 4; }
+    static __host__ __device__ inline int lm_ticket(int L) { return L * 5; }
+    static __host__ __device__ inline int attn_ticket(int L, int l, int g, int nkv) {
+        return L * 5 + 1 + l * nkv + g;
+    }
+    static __host__ __device__ inline int count(int L, int nkv) { return L * 5 + 1 + L * nkv; }
+};
+
+struct KParams {
+    // schedule
+    const Instr *instrs;      // [nsm][max_instr]
+    const int32_t *n_instr;   // [nsm]
+    int32_t max_instr;
+    int32_t nsm;
+    // model
+    const LayerW *layers;     // [L] (device)
+    const uint16_t *embed, *lm_head, *final_norm;
+    uint16_t *k_cache, *v_cache;
+    const float2 *rope_cs;    // [max_seq][hd/2] (cos, sin)
+    int32_t L, H, nq, nkv, hd, I, V, max_seq;
+    float eps;
+    int32_t attn_splits;
+    MvShape mv_h, mv_q, mv_i; // input widths hidden, n_q*hd, inter
+    // scratch (fp32 unless noted)
+    float *x;                 // [H] residual stream
+    float *qkv;               // [nq*hd + 2*nkv*hd]
+    float *part;              // [nq][splits][hd + 2]: o (unnormalised), m, l
+    float *o;                 // [nq*hd]
+    float *act;               // [I]
+    unsigned long long *lm_keys; // [nsm]
+    uint32_t *ctr;            // counters, CTR_STRIDE apart
+    int32_t *status;          // sticky status word
+    int32_t *token_out;       // [1] library copy of the last next token
+    // step
+    int32_t token;            // used when token_dev is null
+    const int32_t *token_dev;
+    int32_t pos;
+    uint32_t epoch;           // 1-based step count since the last counter reset
+    float *logits;            // [V] or null
+    int32_t *next_token_dev;  // or null
+    unsigned long long timeout_ns;
+};
+
+// Host-side launchers (defined in the .cu files).
+int launch_megakernel(const KParams &p, void *stream, int smem_bytes);
+int megakernel_smem_bytes();
+int megakernel_prepare(int smem_bytes);
+
+struct ChainBufs {
+    const LayerW *host_layers;  // [L], host memory
+    float *x, *h, *qkv, *part, *o, *gate, *up, *act, *logits;
+    int32_t splits;
+};
+int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
+
+// Host-side schedule construction (schedule.cpp).
+void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm, int splits,
+                    std::vector<std::vector<Instr>> &lists);
+bool mv_shape(int K, MvShape &m);
+
+}  // namespace ll

@@ -1,0 +1,222 @@
+"""Thin ctypes binding of libll.so (the C ABI in include/ll.h).
+
+Every function here has the name of the C entry point it calls and does only
+argument marshalling: torch tensors supply device pointers and the stream, and
+every step of the decode runs in the library's CUDA kernels. There is no
+fallback: if libll.so is missing or fails to load, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LL_OK = 0
+LL_ERR_ARG = -1
+LL_ERR_SHAPE = -2
+LL_ERR_CUDA = -3
+LL_ERR_DEP_TIMEOUT = -4
+LL_ERR_OOM = -5
+LL_ERR_DEVICE = -6
+
+LL_BACKEND_MEGAKERNEL = 0
+LL_BACKEND_CHAIN = 1
+
+LL_Q_NUM_SMS = 0
+LL_Q_ATTN_SPLITS = 1
+LL_Q_PAGE_BYTES = 2
+LL_Q_NUM_PAGES = 3
+LL_Q_SCRATCH_BYTES = 4
+LL_Q_MAX_INSTRS = 5
+LL_Q_LAUNCHES_PER_STEP = 6
+LL_Q_SMEM_BYTES = 7
+
+LL_FAULT_NONE = 0
+LL_FAULT_DROP_SIGNAL = 1
+
+OP_QKV, OP_ATTN, OP_OPROJ, OP_GATEUP, OP_DOWN = range(5)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
+
+EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_synchronize",
+           "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_last_error", "ll_free")
+
+
+class LLError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libll error {code}: {msg}")
+        self.code = code
+
+
+class ll_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "inter", "vocab", "max_seq",
+        "tied", "backend")] + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
+_P16 = ctypes.c_void_p
+_PP16 = ctypes.POINTER(ctypes.c_void_p)
+LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
+
+
+class ll_weights(ctypes.Structure):
+    _fields_ = [("embed", _P16), ("lm_head", _P16), ("final_norm", _P16)] + [
+        (k, _PP16) for k in LAYER_KEYS]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Open libll.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64
+    L.ll_init.argtypes = [ctypes.POINTER(ll_config), ctypes.POINTER(ll_weights), vp, vp, vp,
+                          ctypes.POINTER(vp)]
+    L.ll_init.restype = ctypes.c_int
+    L.ll_init_error.argtypes = []
+    L.ll_init_error.restype = ctypes.c_char_p
+    L.ll_decode_step.argtypes = [vp, i32, i32, vp, ctypes.POINTER(i32)]
+    L.ll_decode_step.restype = ctypes.c_int
+    L.ll_decode_step_async.argtypes = [vp, vp, i32, vp, vp]
+    L.ll_decode_step_async.restype = ctypes.c_int
+    L.ll_synchronize.argtypes = [vp]
+    L.ll_synchronize.restype = ctypes.c_int
+    L.ll_set_timeout_ns.argtypes = [vp, u64]
+    L.ll_set_timeout_ns.restype = ctypes.c_int
+    L.ll_query.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]
+    L.ll_query.restype = ctypes.c_int
+    L.ll_debug_inject.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.ll_debug_inject.restype = ctypes.c_int
+    L.ll_last_error.argtypes = [vp]
+    L.ll_last_error.restype = ctypes.c_char_p
+    L.ll_free.argtypes = [vp]
+    L.ll_free.restype = None
+    _lib = L
+    return L
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _check(h, rc: int):
+    if rc != LL_OK:
+        raise LLError(rc, lib().ll_last_error(h).decode())
+
+
+def make_config(shape, max_seq: int, backend: int = LL_BACKEND_MEGAKERNEL) -> ll_config:
+    """ll_config from a shape description with the attributes of synth.ModelShape."""
+    c = ll_config()
+    for n in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "inter", "vocab"):
+        setattr(c, n, int(getattr(shape, n)))
+    c.max_seq = int(max_seq)
+    c.tied = int(bool(shape.tied))
+    c.backend = int(backend)
+    c.rms_eps = float(shape.rms_eps)
+    c.rope_theta = float(shape.rope_theta)
+    return c
+
+
+def ll_init(cfg: ll_config, weights: dict, k_cache, v_cache, stream=None):
+    """Create a handle. ``weights`` maps names to CUDA bf16 tensors (per-layer names
+    to lists); ``stream`` is a torch.cuda.Stream or None for torch's current stream."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    w = ll_weights()
+    w.embed = _ptr(weights["embed"])
+    w.final_norm = _ptr(weights["final_norm"])
+    w.lm_head = _ptr(weights.get("lm_head"))
+    keep = []
+    for k in LAYER_KEYS:
+        arr = (ctypes.c_void_p * max(1, len(weights[k])))(*[_ptr(t) for t in weights[k]])
+        keep.append(arr)
+        setattr(w, k, ctypes.cast(arr, _PP16))
+    h = ctypes.c_void_p()
+    rc = lib().ll_init(ctypes.byref(cfg), ctypes.byref(w), _ptr(k_cache), _ptr(v_cache),
+                       ctypes.c_void_p(stream.cuda_stream), ctypes.byref(h))
+    if rc != LL_OK:
+        raise LLError(rc, lib().ll_init_error().decode())
+    return h
+
+
+def ll_decode_step(h, token: int, pos: int, logits=None) -> int:
+    """Synchronous step; returns the greedy next token."""
+    nxt = ctypes.c_int32(-1)
+    _check(h, lib().ll_decode_step(h, int(token), int(pos), _ptr(logits), ctypes.byref(nxt)))
+    return int(nxt.value)
+
+
+def ll_decode_step_async(h, token_dev, pos: int, logits, next_token_dev) -> None:
+    _check(h, lib().ll_decode_step_async(h, _ptr(token_dev), int(pos), _ptr(logits),
+                                         _ptr(next_token_dev)))
+
+
+def ll_synchronize(h) -> None:
+    _check(h, lib().ll_synchronize(h))
+
+
+def ll_set_timeout_ns(h, ns: int) -> None:
+    _check(h, lib().ll_set_timeout_ns(h, int(ns)))
+
+
+def ll_query(h, what: int) -> int:
+    v = ctypes.c_int64()
+    _check(h, lib().ll_query(h, int(what), ctypes.byref(v)))
+    return int(v.value)
+
+
+def ll_debug_inject(h, kind: int, layer: int = 0, op: int = 0) -> None:
+    _check(h, lib().ll_debug_inject(h, int(kind), int(layer), int(op)))
+
+
+def ll_last_error(h) -> str:
+    return lib().ll_last_error(h).decode()
+
+
+def ll_free(h) -> None:
+    if h:
+        lib().ll_free(h)
+
+
+class Decoder:
+    """Owns a handle plus references to the tensors it points into."""
+
+    def __init__(self, shape, weights: dict, k_cache, v_cache, max_seq: int,
+                 backend: int = LL_BACKEND_MEGAKERNEL, stream=None):
+        import torch
+        self.shape = shape
+        self.weights = weights
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.cfg = make_config(shape, max_seq, backend)
+        self.handle = ll_init(self.cfg, weights, k_cache, v_cache, self.stream)
+
+    def step(self, token: int, pos: int, logits=None) -> int:
+        return ll_decode_step(self.handle, token, pos, logits)
+
+    def step_async(self, token_dev, pos: int, logits, next_token_dev) -> None:
+        ll_decode_step_async(self.handle, token_dev, pos, logits, next_token_dev)
+
+    def synchronize(self) -> None:
+        ll_synchronize(self.handle)
+
+    def query(self, what: int) -> int:
+        return ll_query(self.handle, what)
+
+    def close(self) -> None:
+        if self.handle:
+            ll_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,163 @@
+/*
+ * ll.h -- C ABI of libll.so: batch-1 autoregressive decode of a Llama-style
+ * decoder on one NVIDIA GB300 (sm_103a), one decode step per launch of a
+ * persistent megakernel.
+ *
+ * Source of the method: the page "Hazy Research Llama-3.2-1B Megakernel" (a
+ * Chinese write-up at w2o.qhhnjy.cn/html/17f999973.html). Its instruction list
+ * defines what one step computes: per layer (1) RMSNorm fused with the QKV
+ * projection and RoPE, (2) attention as matrix product plus reduction with GQA
+ * over long sequences, (3) O projection plus residual, (4) MLP RMSNorm with the
+ * SiLU-gated gate and up projections, (5) down projection plus residual; after
+ * the last layer (6) RMSNorm plus the language-modelling head. In front of the
+ * layers the step looks up the token embedding, and after the head it takes
+ * the greedy argmax. The page's paragraphs on the instruction interpreter, the
+ * shared-memory pages and the global-memory counters describe how the library
+ * runs that step as one kernel; the page defines no programming interface, so
+ * the calls below are this library's own.
+ *
+ * Conventions shared by every call:
+ *   - bf16 tensors are passed as uint16_t bit patterns; every matrix is
+ *     row-major [out][in]. All tensor pointers are DEVICE pointers and must be
+ *     16-byte aligned.
+ *   - The caller owns the weights, the KV caches and every output buffer; they
+ *     must stay allocated and unchanged (weights) while the handle lives. The
+ *     library owns its schedule, scratch, counters and status word.
+ *   - All GPU work is enqueued on the stream given to ll_init (a cudaStream_t
+ *     passed as void*; NULL means the legacy default stream).
+ *   - Return codes are LL_OK (0) or one of the negative LL_ERR_* values; after
+ *     an error ll_last_error() holds a one-line explanation.
+ *   - A handle is not thread-safe: calls on one handle must not overlap.
+ */
+#ifndef LL_H
+#define LL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LL_OK 0
+#define LL_ERR_ARG (-1)          /* bad argument: null/misaligned pointer, token or pos out of range */
+#define LL_ERR_SHAPE (-2)        /* model shape the kernels do not support */
+#define LL_ERR_CUDA (-3)         /* a CUDA runtime call failed */
+#define LL_ERR_DEP_TIMEOUT (-4)  /* a device-side wait ran past its time limit; the step was abandoned */
+#define LL_ERR_OOM (-5)          /* library scratch could not be allocated */
+#define LL_ERR_DEVICE (-6)       /* device is not sm_103 or cannot co-schedule one block per SM */
+
+#define LL_BACKEND_MEGAKERNEL 0  /* one persistent kernel per decode step */
+#define LL_BACKEND_CHAIN 1       /* one kernel per operation, for comparison */
+
+typedef struct ll_handle ll_handle;
+
+/* Model shape. Constraints checked by ll_init (LL_ERR_SHAPE otherwise):
+ * n_q_heads % n_kv_heads == 0 and n_q_heads / n_kv_heads <= 8; head_dim 64 or
+ * 128; hidden, n_q_heads*head_dim and inter multiples of 256 and at most 16384;
+ * max_seq >= 1. */
+typedef struct {
+    int32_t n_layers;
+    int32_t hidden;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t inter;      /* SwiGLU intermediate width */
+    int32_t vocab;
+    int32_t max_seq;    /* positions the KV caches hold */
+    int32_t tied;       /* nonzero: the LM head is the embedding matrix */
+    int32_t backend;    /* LL_BACKEND_MEGAKERNEL or LL_BACKEND_CHAIN */
+    float rms_eps;
+    float rope_theta;
+} ll_config;
+
+/* Weight pointers. The per-layer members are HOST arrays of n_layers DEVICE
+ * pointers; ll_init copies them, so the host arrays may be freed afterwards. */
+typedef struct {
+    const uint16_t *embed;        /* [vocab][hidden] */
+    const uint16_t *lm_head;      /* [vocab][hidden]; ignored (may be NULL) when tied */
+    const uint16_t *final_norm;   /* [hidden] */
+    const uint16_t *const *attn_norm; /* [hidden] */
+    const uint16_t *const *wq;    /* [n_q_heads*head_dim][hidden] */
+    const uint16_t *const *wk;    /* [n_kv_heads*head_dim][hidden] */
+    const uint16_t *const *wv;    /* [n_kv_heads*head_dim][hidden] */
+    const uint16_t *const *wo;    /* [hidden][n_q_heads*head_dim] */
+    const uint16_t *const *mlp_norm; /* [hidden] */
+    const uint16_t *const *wg;    /* [inter][hidden] */
+    const uint16_t *const *wu;    /* [inter][hidden] */
+    const uint16_t *const *wd;    /* [hidden][inter] */
+} ll_weights;
+
+/* Create a decoder for one sequence on the current CUDA device.
+ *   k_cache, v_cache: caller-owned device buffers, bf16,
+ *     [n_layers][n_kv_heads][max_seq][head_dim]. Step `pos` writes entry pos and
+ *     reads entries 0..pos; entries the caller filled beforehand are used as is.
+ *   stream: cudaStream_t (as void*) that every later call enqueues on.
+ * Builds the per-SM instruction schedule and the RoPE table, allocates library
+ * scratch, and checks that the device is sm_103 and can keep one block resident
+ * on every SM. On success *out receives the handle; on failure *out is NULL and
+ * the code says why (no handle exists to query, so the reason is printed by
+ * ll_init_error()). */
+int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16_t *v_cache,
+            void *stream, ll_handle **out);
+
+/* Reason for the last ll_init failure in this process (static string). */
+const char *ll_init_error(void);
+
+/* One decode step, synchronous: input token `token` at position `pos`
+ * (0 <= token < vocab, 0 <= pos < max_seq). Writes K/V entry pos, writes the
+ * fp32 logits [vocab] to logits_dev when it is not NULL, stores the greedy next
+ * token (lowest index among equal maxima) to *next_token_host when it is not
+ * NULL, waits for the stream, and returns the step's status. */
+int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev,
+                   int32_t *next_token_host);
+
+/* One decode step, enqueued only: the input token is read on the device from
+ * *token_dev and the next token written to *next_token_dev (both device int32;
+ * they may be the same address, which chains steps without the host). pos is
+ * checked on the host; a token out of range is caught on the device and ends
+ * the step with LL_ERR_ARG. Errors on the device are sticky: later steps return
+ * at once, and ll_synchronize() reports and clears them. */
+int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,
+                         int32_t *next_token_dev);
+
+/* Wait for the handle's stream, then return and clear the device status of the
+ * steps enqueued since the last check (LL_OK if all of them succeeded). After
+ * an error the library resets its counters, so the next step starts clean. */
+int ll_synchronize(ll_handle *h);
+
+/* Upper bound, in nanoseconds, on any single device-side wait (dependency
+ * counters and shared-memory page handoff). Past it the kernel records
+ * LL_ERR_DEP_TIMEOUT, lets its own copies land, and returns. Default 1 s. */
+int ll_set_timeout_ns(ll_handle *h, uint64_t ns);
+
+/* Schedule and memory facts, for tests and reports. */
+#define LL_Q_NUM_SMS 0          /* blocks of the persistent kernel (one per SM) */
+#define LL_Q_ATTN_SPLITS 1      /* KV splits per KV head in the attention instruction */
+#define LL_Q_PAGE_BYTES 2       /* bytes of one shared-memory page */
+#define LL_Q_NUM_PAGES 3        /* pages per SM */
+#define LL_Q_SCRATCH_BYTES 4    /* device bytes the library allocated */
+#define LL_Q_MAX_INSTRS 5       /* longest per-SM instruction list */
+#define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes */
+#define LL_Q_SMEM_BYTES 7       /* dynamic shared memory per block */
+int ll_query(const ll_handle *h, int what, int64_t *value);
+
+/* Fault injection for tests (host side only; nothing faults on the device):
+ * LL_FAULT_DROP_SIGNAL removes the completion signal of every instruction of
+ * kind `op` (0 QKV, 1 attention, 2 O projection, 3 gate/up, 4 down) in layer
+ * `layer`, so the instruction waiting on it runs into its time limit and the
+ * step returns LL_ERR_DEP_TIMEOUT. LL_FAULT_NONE restores the schedule. */
+#define LL_FAULT_NONE 0
+#define LL_FAULT_DROP_SIGNAL 1
+int ll_debug_inject(ll_handle *h, int kind, int layer, int op);
+
+/* Explanation of the last error on this handle (never NULL). */
+const char *ll_last_error(const ll_handle *h);
+
+/* Release library memory (not the caller's weights, caches or buffers). NULL is a no-op. */
+void ll_free(ll_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LL_H */
