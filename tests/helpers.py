@@ -73,15 +73,24 @@ class Pair:
         return nxt, ref_next, stats
 
     def kv_close(self, positions):
-        """GPU and oracle K/V entries at `positions` agree to bf16 rounding."""
+        """GPU and oracle K/V entries at `positions` agree to bf16 rounding.
+
+        Layer 0 sees identical inputs on both sides, so its entries may differ
+        only where fp32 summation order tips a bf16 rounding (well under 1%).
+        Deeper layers inherit the fp32 rounding noise of the layers below, and
+        the random-weight models amplify it with depth (the float and double
+        oracles disagree on later layers as often), so there every entry is only
+        held to within two bf16 steps of the oracle's.
+        """
         gk = synth.to_host_bits(self.k)[:, :, positions]
         gv = synth.to_host_bits(self.v)[:, :, positions]
         ok = self.orc.k_cache[:, :, positions]
         ov = self.orc.v_cache[:, :, positions]
         for g, o, name in ((gk, ok, "K"), (gv, ov, "V")):
             a, b = widen_bits(g).astype(np.float64), widen_bits(o).astype(np.float64)
-            assert np.max(np.abs(a - b)) <= 2e-2 * max(1.0, np.max(np.abs(b))), name
-            assert np.mean(g != o) < 0.05, f"{name}: {np.mean(g != o):.3f} of entries differ"
+            lim = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + 1e-3 * max(1.0, np.max(np.abs(b)))
+            assert np.all(np.abs(a - b) <= lim), f"{name}: max excess {np.max(np.abs(a - b) - lim):.3e}"
+            assert np.mean(g[0] != o[0]) < 0.01, f"{name}: {np.mean(g[0] != o[0]):.4f} of layer-0 entries differ"
 
     def close(self):
         self.dec.close()
