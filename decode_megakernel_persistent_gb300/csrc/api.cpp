@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -62,11 +63,19 @@ int upload_schedule(ll_handle *h) {
     return LL_OK;
 }
 
-void build_lists(ll_handle *h) {
-    const ll_config &c = h->cfg;
-    ll::build_schedule(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim, c.inter,
-                       c.vocab, c.n_kv_heads, h->nsm, h->splits, h->lists);
+// KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
+// longest context, at most one attention item per SM.
+int attn_splits(const ll_config &c, int nsm) {
+    const int want = (c.max_seq + ll::ATTN_SPLIT_POS - 1) / ll::ATTN_SPLIT_POS;
+    return std::max(1, std::min(want, nsm / c.n_kv_heads));
 }
+
+void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::vector<Instr>> &lists) {
+    ll::build_schedule(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim, c.inter,
+                       c.vocab, c.n_kv_heads, nsm, splits, lists);
+}
+
+void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists); }
 
 // Clear counters and the status word after a failed step so the next starts clean.
 int reset_device_state(ll_handle *h) {
@@ -133,6 +142,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     if (c.head_dim != 64 && c.head_dim != 128) return bad(LL_ERR_SHAPE, "head_dim must be 64 or 128");
     if (c.n_q_heads % c.n_kv_heads != 0 || c.n_q_heads / c.n_kv_heads > ll::MAX_GQA)
         return bad(LL_ERR_SHAPE, "n_q_heads must be a multiple (at most 8x) of n_kv_heads");
+    if (int64_t(c.n_q_heads) * c.head_dim > ll::XIN_FLOATS)
+        return bad(LL_ERR_SHAPE, "n_q_heads*head_dim must be at most 4096");
     if (c.backend != LL_BACKEND_MEGAKERNEL && c.backend != LL_BACKEND_CHAIN)
         return bad(LL_ERR_ARG, "unknown backend");
     if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad(LL_ERR_ARG, "rms_eps/rope_theta invalid");
@@ -169,13 +180,18 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     h->device = dev;
     h->nsm = prop.multiProcessorCount;
     h->stream = static_cast<cudaStream_t>(stream);
-    h->splits = std::max(1, h->nsm / c.n_kv_heads);
+    h->splits = attn_splits(c, h->nsm);
     h->smem_bytes = ll::megakernel_smem_bytes();
     h->host_layers = layers;
     const int qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
-    if ((c.inter + h->nsm - 1) / h->nsm > ll::GBUF_FLOATS) {
-        delete h;
-        return bad(LL_ERR_SHAPE, "inter too large for the SM count");
+    {
+        auto per_sm = [&](int64_t rows) { return (rows + h->nsm - 1) / h->nsm; };
+        const int64_t qkv_rows = int64_t(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+        if (per_sm(qkv_rows) > ll::ACC_FLOATS || 2 * per_sm(c.inter) > ll::ACC_FLOATS ||
+            per_sm(c.hidden) > ll::ACC_FLOATS || per_sm(c.vocab) > ll::ACC_FLOATS) {
+            delete h;
+            return bad(LL_ERR_SHAPE, "a projection has more rows per SM than the kernel holds");
+        }
     }
     int rc = ll::megakernel_prepare(h->smem_bytes);
     if (rc != LL_OK) {
@@ -197,7 +213,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     unsigned long long *keys = nullptr;
     uint32_t *ctr = nullptr;
     int32_t *status = nullptr, *tok = nullptr;
-    const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 2);
+    const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 4);
     Piece pieces[] = {
         {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
         {reinterpret_cast<void **>(&d_n_instr), size_t(h->nsm) * sizeof(int32_t)},
@@ -269,6 +285,12 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.max_seq = c.max_seq;
     p.eps = c.rms_eps;
     p.attn_splits = h->splits;
+    {
+        const int P = (c.n_q_heads / c.n_kv_heads) * c.head_dim;
+        int T = 1;
+        while (T * 2 * P <= ll::NCT && T < 32) T *= 2;
+        p.attn_T = T;
+    }
     p.mv_h = mh;
     p.mv_q = mq;
     p.mv_i = mi;
@@ -282,6 +304,14 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.status = status;
     p.token_out = tok;
     p.timeout_ns = 1000000000ull;
+    // tuning knobs (environment, read once here): L2 prefetch distance in pages and
+    // the evict-first hint on weight pages
+    p.l2_prefetch = 16;
+    p.evict_first = 1;
+    if (const char *e = std::getenv("LL_L2_PREFETCH_PAGES")) p.l2_prefetch = static_cast<uint32_t>(std::atoi(e));
+    if (const char *e = std::getenv("LL_EVICT_FIRST")) p.evict_first = static_cast<uint32_t>(std::atoi(e));
+    p.producer_sleep_ns = 64;
+    if (const char *e = std::getenv("LL_PRODUCER_SLEEP_NS")) p.producer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
     h->d_instrs = d_instrs;
 
     ll::ChainBufs &cb = h->cb;
@@ -352,6 +382,23 @@ int ll_synchronize(ll_handle *h) {
     return LL_OK;
 }
 
+int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes) {
+    if (!h) return LL_ERR_ARG;
+    if (!trace_dev) {
+        h->kp.trace = nullptr;
+        h->kp.ptrace = nullptr;
+        return LL_OK;
+    }
+    const size_t instr_words = size_t(h->nsm) * h->max_instr * ll::TRACE_WORDS;
+    const size_t page_words = size_t(h->nsm) * ll::PTRACE_PAGES * 3;
+    const size_t need = (instr_words + page_words) * sizeof(uint64_t);
+    if (bytes < need || !aligned16(trace_dev))
+        return fail(h, LL_ERR_ARG, "trace buffer needs " + std::to_string(need) + " bytes, 16-byte aligned");
+    h->kp.trace = reinterpret_cast<unsigned long long *>(trace_dev);
+    h->kp.ptrace = h->kp.trace + instr_words;
+    return LL_OK;
+}
+
 int ll_set_timeout_ns(ll_handle *h, uint64_t ns) {
     if (!h || ns == 0) return LL_ERR_ARG;
     h->kp.timeout_ns = ns;
@@ -371,6 +418,10 @@ int ll_query(const ll_handle *h, int what, int64_t *value) {
             *value = h->cfg.backend == LL_BACKEND_CHAIN ? 1 + 13 * int64_t(h->cfg.n_layers) + 3 : 1;
             break;
         case LL_Q_SMEM_BYTES: *value = h->smem_bytes; break;
+        case LL_Q_TRACE_BYTES:
+            *value = (int64_t(h->nsm) * h->max_instr * ll::TRACE_WORDS + int64_t(h->nsm) * ll::PTRACE_PAGES * 3) *
+                     int64_t(sizeof(uint64_t));
+            break;
         default: return LL_ERR_ARG;
     }
     return LL_OK;
@@ -390,6 +441,31 @@ int ll_debug_inject(ll_handle *h, int kind, int layer, int op) {
         return fail(h, LL_ERR_ARG, "unknown fault kind");
     }
     return upload_schedule(h);
+}
+
+int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr) {
+    if (!cfg || nsm <= 0 || cfg->n_layers < 1 || cfg->n_kv_heads <= 0 || cfg->n_q_heads % cfg->n_kv_heads != 0)
+        return LL_ERR_ARG;
+    std::vector<std::vector<Instr>> lists;
+    build_lists_for(*cfg, nsm, attn_splits(*cfg, nsm), lists);
+    size_t mx = 0;
+    for (auto &l : lists) mx = std::max(mx, l.size());
+    if (max_instr) *max_instr = static_cast<int32_t>(mx);
+    if (!out) return LL_OK;
+    if (out_len < size_t(nsm) * mx * 7) return LL_ERR_ARG;
+    for (int sm = 0; sm < nsm; sm++) {
+        for (size_t i = 0; i < mx; i++) {
+            int32_t *o = out + (size_t(sm) * mx + i) * 7;
+            if (i < lists[sm].size()) {
+                const Instr &in = lists[sm][i];
+                o[0] = in.op; o[1] = in.layer; o[2] = in.r0; o[3] = in.r1;
+                o[4] = in.wait_ctr; o[5] = static_cast<int32_t>(in.wait_count); o[6] = in.sig_ctr;
+            } else {
+                o[0] = -1; o[1] = o[2] = o[3] = o[5] = 0; o[4] = o[6] = -1;
+            }
+        }
+    }
+    return LL_OK;
 }
 
 const char *ll_last_error(const ll_handle *h) { return h ? h->err.c_str() : "null handle"; }

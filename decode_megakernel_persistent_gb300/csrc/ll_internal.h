@@ -14,16 +14,21 @@ namespace ll {
 // ---- persistent-kernel geometry -------------------------------------------------
 // One block per SM: NCW consumer warps compute, one producer warp streams bytes
 // from HBM into a ring of NPAGES shared-memory pages of PAGE_BYTES each.
-constexpr int NCW = 8;
+constexpr int NCW = 16;
 constexpr int NCT = NCW * 32;              // consumer threads
 constexpr int NTHREADS = NCT + 32;         // + producer warp
 constexpr int PAGE_BYTES = 32768;
 constexpr int NPAGES = 6;
-constexpr int MAX_VPL = 8;                 // 16-byte weight vectors per lane per row
+constexpr int MAX_VPL = 4;                 // 16-byte input vectors per lane (register budget)
 constexpr int MAX_GQA = 8;                 // query heads per KV head
 constexpr int MAX_HD = 128;
 constexpr int MAX_RPP = 64;                // rows per page (hidden 256 at one vector per lane)
-constexpr int GBUF_FLOATS = 1024;          // gate results held per SM between gate and up rows
+constexpr int MAX_PART = 128;              // (row, k-slice) partial sums per page
+constexpr int ACC_FLOATS = 2048;           // per-SM row results held until the instruction ends
+constexpr int XIN_FLOATS = 4096;           // largest O-projection input (n_q_heads * head_dim)
+constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
+constexpr int TRACE_WORDS = 12;            // timestamps per traced instruction
+constexpr int PTRACE_PAGES = 4096;         // pages per SM the page trace keeps (a ring)
 
 // Instruction kinds, in the order they appear within a layer.
 enum Op : uint8_t { OP_QKV = 0, OP_ATTN = 1, OP_OPROJ = 2, OP_GATEUP = 3, OP_DOWN = 4, OP_LMHEAD = 5 };
@@ -42,10 +47,12 @@ struct Instr {
     int32_t sig_ctr;      // counter to bump when done, -1 for none
 };
 
-// Matrix-vector geometry for one input width K: ws warps share a row, each lane
-// holds vpl 16-byte vectors (8 elements) of the input, rpp rows fill a page.
+// Matrix-vector geometry for one input width K. A page holds rpp whole rows. The
+// row is cut into ws k-slices of 256*vpl elements; warp w works on slice w % ws of
+// rows w / ws + q * rg (q < rw) of every page, so ws * rg warps are active and
+// each lane keeps vpl 16-byte vectors of the input in registers.
 struct MvShape {
-    int32_t K, ws, vpl, rpp;
+    int32_t K, ws, vpl, rpp, rg, rw;
 };
 
 struct LayerW {
@@ -55,17 +62,14 @@ struct LayerW {
 // Counters, each on its own 128-byte line.
 constexpr int CTR_STRIDE = 32;  // uint32 per counter slot
 struct CtrLayout {
-    // per layer: qkv, attn, oproj, gateup, down; then per (layer, kv head) a ticket
+    // per layer: qkv, attn, oproj, gateup, down; then the LM-head ticket
     static __host__ __device__ inline int qkv(int l) { return l * 5 + 0; }
     static __host__ __device__ inline int attn(int l) { return l * 5 + 1; }
     static __host__ __device__ inline int oproj(int l) { return l * 5 + 2; }
     static __host__ __device__ inline int gateup(int l) { return l * 5 + 3; }
     static __host__ __device__ inline int down(int l) { return l * 5 + 4; }
     static __host__ __device__ inline int lm_ticket(int L) { return L * 5; }
-    static __host__ __device__ inline int attn_ticket(int L, int l, int g, int nkv) {
-        return L * 5 + 1 + l * nkv + g;
-    }
-    static __host__ __device__ inline int count(int L, int nkv) { return L * 5 + 1 + L * nkv; }
+    static __host__ __device__ inline int count(int L, int) { return L * 5 + 1; }
 };
 
 struct KParams {
@@ -86,7 +90,8 @@ struct KParams {
     // scratch (fp32 unless noted)
     float *x;                 // [H] residual stream
     float *qkv;               // [nq*hd + 2*nkv*hd]
-    float *part;              // [nq][splits][hd + 2]: o (unnormalised), m, l
+    float *part;              // [nq][splits][hd + 4]: o (unnormalised), m, l
+    int32_t attn_T;           // threads per (head, dim) pair in attention P.V
     float *o;                 // [nq*hd]
     float *act;               // [I]
     unsigned long long *lm_keys; // [nsm]
@@ -101,6 +106,17 @@ struct KParams {
     float *logits;            // [V] or null
     int32_t *next_token_dev;  // or null
     unsigned long long timeout_ns;
+    uint32_t l2_prefetch;     // pages the producer may prefetch into L2 beyond its ring
+    uint32_t evict_first;     // weight pages loaded with an L2 evict-first hint
+    uint32_t producer_sleep_ns; // back-off of the producer while the ring is full
+    // optional globaltimer trace, [nsm][max_instr][TRACE_WORDS]: consumer begin,
+    // dependency met + input loaded, pages done, end; producer first and last issue;
+    // first page in hand, compute on the pages done; for attention also the end
+    // of the scores, softmax and P.V phases of its last block, and the partials written
+    unsigned long long *trace;
+    // optional page trace, [nsm][PTRACE_PAGES][3]: producer issue, consumer start,
+    // release, indexed by page number modulo PTRACE_PAGES
+    unsigned long long *ptrace;
 };
 
 // Host-side launchers (defined in the .cu files).

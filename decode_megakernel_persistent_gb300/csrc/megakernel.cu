@@ -21,6 +21,7 @@
 // ticket), so no instruction waits for it; the greedy argmax is reduced the
 // same way. Every wait is bounded by a time limit.
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "ll_internal.h"
@@ -91,6 +92,12 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
@@ -135,12 +142,18 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 // Shared memory
 
 struct alignas(16) Smem {
+    union {
+        float xin[XIN_FLOATS];  // O-projection input: the merged attention output
+        struct {
+            float acc[ACC_FLOATS];  // the SM's row results of the current matrix-vector instruction
+            float qs[MAX_GQA][MAX_HD];
+            float sc[MAX_GQA][132];  // scores, then probabilities, of up to 129 positions
+        };
+    };
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
     uint64_t empty[NPAGES];  // page released by the consumers
-    float red[2][MAX_RPP][NCW];
-    float gbuf[GBUF_FLOATS];
-    alignas(16) float qs[MAX_GQA][MAX_HD];
-    alignas(16) float sc[MAX_GQA][128];
+    int32_t pcnt[NPAGES];    // warps done with the page in the slot
+    float part[NPAGES][MAX_PART];  // per page: (row, k-slice) partial sums
     alignas(16) uint16_t knew[MAX_HD];
     alignas(16) uint16_t vnew[MAX_HD];
     float m_run[MAX_GQA], l_run[MAX_GQA], alpha[MAX_GQA];
@@ -152,6 +165,9 @@ struct alignas(16) Smem {
     volatile int32_t abort;
 };
 
+static_assert(ACC_FLOATS + MAX_GQA * MAX_HD + MAX_GQA * 132 >= XIN_FLOATS, "xin overlaps acc, qs and sc");
+static_assert(offsetof(Smem, xin) % 16 == 0 && offsetof(Smem, qs) % 16 == 0, "alignment");
+
 constexpr int SMEM_BYTES = NPAGES * PAGE_BYTES + static_cast<int>(sizeof(Smem));
 
 // ---------------------------------------------------------------------------------
@@ -161,6 +177,14 @@ constexpr int SMEM_BYTES = NPAGES * PAGE_BYTES + static_cast<int>(sizeof(Smem));
 __device__ __forceinline__ void raise_status(const KParams &p, Smem &s, int32_t code) {
     atomicCAS(p.status, 0, code);
     s.abort = 1;
+}
+
+__device__ __forceinline__ void trace_put(const KParams &p, int ii, int k) {
+    if (p.trace) p.trace[(size_t(blockIdx.x) * p.max_instr + ii) * TRACE_WORDS + k] = gtimer();
+}
+
+__device__ __forceinline__ void ptrace_put(const KParams &p, uint32_t page, int k) {
+    if (p.ptrace) p.ptrace[(size_t(blockIdx.x) * PTRACE_PAGES + page % PTRACE_PAGES) * 3 + k] = gtimer();
 }
 
 __device__ bool wait_counter(const KParams &p, Smem &s, const uint32_t *ctr, uint32_t target) {
@@ -277,6 +301,36 @@ __device__ __forceinline__ void attn_range(const KParams &p, int c, int &c0, int
 
 __device__ __forceinline__ int attn_pp(const KParams &p) { return PAGE_BYTES / (4 * p.hd); }
 
+// O-projection input: merge the KV splits of every query head into s.xin,
+// o = sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c with M = max_c m_c; each
+// thread produces 4 consecutive dimensions of one head.
+__device__ void stage_attention_output(const KParams &p, Smem &s) {
+    const int S = p.attn_splits, stride = p.hd + 4, qd = p.nq * p.hd;
+    for (int t = threadIdx.x; t < qd / 4; t += NCT) {
+        const int e0 = t * 4, h = e0 / p.hd, d0 = e0 % p.hd;
+        const float *base = p.part + size_t(h) * S * stride;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int c = 0; c < S; c++) M = fmaxf(M, __ldcg(base + size_t(c) * stride + p.hd));
+        float L = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int c = 0; c < S; c++) {
+            const float *pc = base + size_t(c) * stride;
+            const float m = __ldcg(pc + p.hd);
+            const float l = __ldcg(pc + p.hd + 1);
+            const float4 oc = __ldcg(reinterpret_cast<const float4 *>(pc + d0));
+            const float w = (m == -INFINITY) ? 0.f : expf(m - M);
+            L = fmaf(w, l, L);
+            o.x = fmaf(w, oc.x, o.x); o.y = fmaf(w, oc.y, o.y);
+            o.z = fmaf(w, oc.z, o.z); o.w = fmaf(w, oc.w, o.w);
+        }
+        const float inv = 1.0f / L;
+        *reinterpret_cast<float4 *>(&s.xin[e0]) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    }
+    consumer_sync();
+}
+
 // Lane-held input vector: element (sw*32*VPL + j*32 + lane)*8 + e sits in xr[j*8+e].
 template <int VPL>
 __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
@@ -294,13 +348,18 @@ __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             break;
         case OP_GATEUP: gain = p.layers[ins.layer].mlp_norm; src = p.x; break;
         case OP_LMHEAD: gain = p.final_norm; src = p.x; break;
-        case OP_OPROJ: src = p.o; break;
+        case OP_OPROJ: stage_attention_output(p, s); break;
         default: src = p.act; break;
     }
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
         const int v = sw * 32 * VPL + j * 32 + lane;
-        if (src16) {
+        if (ins.op == OP_OPROJ) {
+            const float4 a = *reinterpret_cast<const float4 *>(&s.xin[v * 8]);
+            const float4 b = *reinterpret_cast<const float4 *>(&s.xin[v * 8 + 4]);
+            xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
+            xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
+        } else if (src16) {
             uint4 u = __ldg(reinterpret_cast<const uint4 *>(src16) + v);
             xr[j * 8 + 0] = bf_lo(u.x); xr[j * 8 + 1] = bf_hi(u.x);
             xr[j * 8 + 2] = bf_lo(u.y); xr[j * 8 + 3] = bf_hi(u.y);
@@ -337,8 +396,35 @@ __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
     }
 }
 
-template <int VPL>
-__device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, uint32_t &cpage,
+// Sum R per-lane values across the warp so that the lanes of group
+// q = lane / (32 / R) end up holding the full sum of value q.
+template <int R>
+__device__ __forceinline__ float transpose_reduce(float (&v)[R]) {
+    const int lane = threadIdx.x & 31;
+    int n = R;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (n > 1) {
+            const bool upper = (lane & off) != 0;
+            const int half = n / 2;
+#pragma unroll
+            for (int i = 0; i < R / 2; i++) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+    return v[0];
+}
+
+template <int VPL, int RW>
+__device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
                          float &best, int &best_idx) {
     const MvShape &mv = mv_of(p, ins.op);
     Seg seg[3];
@@ -348,24 +434,38 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
 
     float xr[VPL * 8];
     load_input<VPL>(p, s, ins, mv, xr);
+    if (threadIdx.x == 0) trace_put(p, ii, 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int sw = warp % mv.ws, rg = warp / mv.ws, ngroups = NCW / mv.ws;
+    const int active = mv.ws * mv.rg;
+    const int sw = warp % mv.ws, rgi = warp / mv.ws;
     const size_t row_bytes = size_t(mv.K) * 2;
+    const int nrows = ins.r1 - ins.r0;
+    constexpr int GROUP = 32 / RW;  // lanes that end up holding one row's sum
 
     for (int si = 0; si < nseg; si++) {
         const Seg sg = seg[si];
+        // where the segment's rows land in s.acc
+        const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
         for (int pr = 0; pr < sg.nrows; pr += mv.rpp) {
             const int nr = min(mv.rpp, sg.nrows - pr);
             const uint32_t slot = cpage % NPAGES, par = (cpage / NPAGES) & 1u;
+            const uint32_t this_page = cpage++;
+            if (warp >= active) continue;
             if (!wait_page(p, s, &s.full[slot], par)) return false;
-            const uint8_t *page = pages + size_t(slot) * PAGE_BYTES;
-            float(*red)[NCW] = s.red[cpage & 1u];
-            for (int rl = rg; rl < nr; rl += ngroups) {
-                const uint4 *wrow = reinterpret_cast<const uint4 *>(page + size_t(rl) * row_bytes);
+            if (warp == 0 && lane == 0) {
+                ptrace_put(p, this_page, 1);
+                if (si == 0 && pr == 0) trace_put(p, ii, 6);
+            }
+            const uint32_t page = smem_addr(pages) + slot * PAGE_BYTES + (sw * 32 * VPL + lane) * 16;
+            float a[RW][2];
+#pragma unroll
+            for (int q = 0; q < RW; q++) {
+                // rows past nr hold stale bytes; their sums are never used
+                const uint32_t wrow = page + uint32_t(rgi + q * mv.rg) * uint32_t(row_bytes);
                 uint4 wv[VPL];
 #pragma unroll
-                for (int j = 0; j < VPL; j++) wv[j] = wrow[sw * 32 * VPL + j * 32 + lane];
+                for (int j = 0; j < VPL; j++) wv[j] = lds128(wrow + j * 32 * 16);
                 float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < VPL; j++) {
@@ -378,39 +478,73 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
                     a0 = fmaf(bf_lo(wv[j].w), xr[j * 8 + 6], a0);
                     a1 = fmaf(bf_hi(wv[j].w), xr[j * 8 + 7], a1);
                 }
-                const float acc = warp_sum(a0 + a1);
-                if (lane == 0) red[rl][sw] = acc;
+                a[q][0] = a0;
+                a[q][1] = a1;
             }
-            consumer_sync();
-            if (tid == 0) mbar_arrive(&s.empty[slot]);  // page bytes no longer needed
-            ++cpage;
-            if (tid < nr) {
-                float y = 0.f;
-                for (int w = 0; w < mv.ws; w++) y += red[tid][w];
-                const int row = sg.row0 + pr + tid;  // row within the matrix
-                switch (sg.kind) {
-                    case OUT_QKV: p.qkv[sg.out0 + row] = y; break;
-                    case OUT_RESID: {
-                        float base = (ins.op == OP_OPROJ && ins.layer == 0)
-                                         ? bf16_to_f(p.embed[size_t(s.token) * p.H + row])
-                                         : __ldcg(p.x + row);
-                        p.x[row] = base + y;
-                        break;
-                    }
-                    case OUT_GATE: s.gbuf[row - ins.r0] = y; break;
-                    case OUT_UP: {
-                        const float g = s.gbuf[row - ins.r0];
-                        p.act[row] = g / (1.0f + expf(-g)) * y;
-                        break;
-                    }
-                    default:  // OUT_LOGITS
-                        if (p.logits) p.logits[row] = y;
-                        if (y > best) { best = y; best_idx = row; }
-                        break;
+            float v[RW];
+#pragma unroll
+            for (int q = 0; q < RW; q++) v[q] = a[q][0] + a[q][1];
+            const float sum = transpose_reduce<RW>(v);
+            const int q = lane / GROUP;
+            if ((lane % GROUP) == 0) s.part[slot][(rgi + q * mv.rg) * mv.ws + sw] = sum;
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&s.pcnt[slot], 1) == active - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {  // this warp finishes the page: sum the k-slices of every row
+                __threadfence_block();
+                for (int r = lane; r < nr; r += 32) {
+                    float y = 0.f;
+                    for (int w = 0; w < mv.ws; w++) y += s.part[slot][r * mv.ws + w];
+                    s.acc[acc0 + pr + r] = y;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    s.pcnt[slot] = 0;
+                    ptrace_put(p, this_page, 2);
+                    mbar_arrive(&s.empty[slot]);
                 }
             }
         }
     }
+    if (tid == 0) trace_put(p, ii, 7);
+    consumer_sync();  // every page reduced into s.acc
+    const int r0 = ins.r0;
+    switch (ins.op) {
+        case OP_QKV:
+            for (int t = tid; t < nrows; t += NCT) p.qkv[r0 + t] = s.acc[t];
+            break;
+        case OP_OPROJ:
+        case OP_DOWN: {
+            const bool from_embed = ins.op == OP_OPROJ && ins.layer == 0;
+            for (int t = tid; t < nrows; t += NCT) {
+                const int row = r0 + t;
+                const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : __ldcg(p.x + row);
+                p.x[row] = base + s.acc[t];
+            }
+            break;
+        }
+        case OP_GATEUP:
+            for (int t = tid; t < nrows; t += NCT) {
+                const float g = s.acc[t];
+                p.act[r0 + t] = g / (1.0f + expf(-g)) * s.acc[nrows + t];
+            }
+            break;
+        default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
+            for (int t = tid; t < nrows; t += NCT) {
+                const float y = s.acc[t];
+                if (p.logits) p.logits[r0 + t] = y;
+                if (y > best) {
+                    best = y;
+                    best_idx = r0 + t;
+                }
+            }
+            break;
+    }
+    if (threadIdx.x == 0) trace_put(p, ii, 2);
     return true;
 }
 
@@ -451,55 +585,62 @@ __device__ void lm_finish(const KParams &p, Smem &s, float best, int best_idx) {
 }
 
 // ---------------------------------------------------------------------------------
-// Attention instruction: one KV head g, one split c of the cached positions; the
-// split that owns position pos also folds in the new k, v and writes them to the
-// cache. Partial (o, m, l) go to global memory; the last split of the head merges.
+// Attention instruction: one KV head g, one split c of the cached positions
+// 0..pos-1; the split that owns position pos also takes in the new k, v and
+// writes them to the cache. Its unnormalised partial (o, m, l) per query head
+// goes to global memory, and the O projection merges the splits when it loads
+// its input, so no instruction waits for a separate merge.
 
+// Query layout in s.qs: head h, 16-byte chunk c of 8 dims; the two 4-float
+// halves of chunks 4..7 (mod 8) are stored swapped so that lanes reading the
+// same half of different chunks hit different banks.
+__device__ __forceinline__ int qs_index(int i) {
+    const int c = i >> 3, half = (i >> 2) & 1;
+    return (c << 3) + ((half ^ ((c >> 2) & 1)) << 2) + (i & 3);
+}
+
+// Scores, online-softmax statistics and P.V over n cached positions of a page
+// (K, V: [n][hd] bf16 in shared memory), plus the new token as position n when
+// with_new is set. NCH = hd / 8.
+template <int NCH>
 __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const uint16_t *Vv, int n,
-                           float (&oacc)[4], int G) {
-    const int hd = p.hd, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = hd / 8;
-    // scores: one position per thread, all G heads; chunk order rotated by position
-    // so that the 16-byte reads of a warp spread over all banks
-    if (tid < n) {
-        const uint4 *krow = reinterpret_cast<const uint4 *>(K + size_t(tid) * hd);
-        float acc[MAX_GQA];
+                           bool with_new, float (&oacc)[2], int G, int ii) {
+    constexpr int hd = NCH * 8;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nt = n + (with_new ? 1 : 0);
+    // scores: thread per (head, position), head-major so a warp shares its query;
+    // 16-byte chunks visited in an order rotated by position (spreads K over banks)
+    for (int t = tid; t < nt * G; t += NCT) {
+        const int h = t / nt, j = t - h * nt;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(j < n ? K + size_t(j) * hd : s.knew);
+        const float *qh = s.qs[h];
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int h = 0; h < MAX_GQA; h++) acc[h] = 0.f;
-        for (int i = 0; i < nch; i++) {
-            const int c = (i + tid) % nch;
-            const uint4 u = krow[c];
-            const float k8[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                                 bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-#pragma unroll
-            for (int h = 0; h < MAX_GQA; h++) {
-                if (h < G) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(&s.qs[h][c * 8]);
-                    const float4 qb = *reinterpret_cast<const float4 *>(&s.qs[h][c * 8 + 4]);
-                    float a = acc[h];
-                    a = fmaf(qa.x, k8[0], a); a = fmaf(qa.y, k8[1], a);
-                    a = fmaf(qa.z, k8[2], a); a = fmaf(qa.w, k8[3], a);
-                    a = fmaf(qb.x, k8[4], a); a = fmaf(qb.y, k8[5], a);
-                    a = fmaf(qb.z, k8[6], a); a = fmaf(qb.w, k8[7], a);
-                    acc[h] = a;
-                }
-            }
+        for (int i = 0; i < NCH; i++) {
+            const int c = (i + j) & (NCH - 1);
+            const uint4 u = k4[c];
+            const int sw = ((c >> 2) & 1) << 2;
+            const float4 qa = *reinterpret_cast<const float4 *>(qh + (c << 3) + sw);
+            const float4 qb = *reinterpret_cast<const float4 *>(qh + (c << 3) + (4 - sw));
+            a0 = fmaf(qa.x, bf_lo(u.x), a0); a1 = fmaf(qa.y, bf_hi(u.x), a1);
+            a2 = fmaf(qa.z, bf_lo(u.y), a2); a3 = fmaf(qa.w, bf_hi(u.y), a3);
+            a0 = fmaf(qb.x, bf_lo(u.z), a0); a1 = fmaf(qb.y, bf_hi(u.z), a1);
+            a2 = fmaf(qb.z, bf_lo(u.w), a2); a3 = fmaf(qb.w, bf_hi(u.w), a3);
         }
-#pragma unroll
-        for (int h = 0; h < MAX_GQA; h++)
-            if (h < G) s.sc[h][tid] = acc[h];
+        s.sc[h][j] = (a0 + a1) + (a2 + a3);
     }
     consumer_sync();
+    if (tid == 0) trace_put(p, ii, 8);
     // online softmax statistics: warp h handles head h
     if (warp < G) {
         const int h = warp;
         float mx = -INFINITY;
-        for (int j = lane; j < n; j += 32) mx = fmaxf(mx, s.sc[h][j]);
+        for (int j = lane; j < nt; j += 32) mx = fmaxf(mx, s.sc[h][j]);
         mx = warp_max(mx);
         const float m_old = s.m_run[h];
         const float m_new = fmaxf(m_old, mx);
         float sum = 0.f;
-        for (int j = lane; j < n; j += 32) {
+        for (int j = lane; j < nt; j += 32) {
             const float e = expf(s.sc[h][j] - m_new);
             s.sc[h][j] = e;
             sum += e;
@@ -513,25 +654,41 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
         }
     }
     consumer_sync();
-    // P V: one (head, dim) pair per accumulator slot
+    if (tid == 0) trace_put(p, ii, 9);
+    // P.V: T threads per (head, dim) pair split the positions (position j goes to
+    // part j % T); partial sums stay per thread across pages and are combined
+    // once at the end of the item
+    const int P = G * hd, T = p.attn_T;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int pi = tid + k * NCT;
-        if (pi < G * hd) {
-            const int h = pi / hd, d = pi % hd;
-            float a = oacc[k] * s.alpha[h];
-            for (int j = 0; j < n; j++) a = fmaf(s.sc[h][j], bf16_to_f(Vv[size_t(j) * hd + d]), a);
-            oacc[k] = a;
+    for (int k = 0; k < 2; k++) {
+        const int slot = tid + k * NCT;
+        const int pi = slot / T, part = slot % T;
+        if ((T > 1 && k > 0) || pi >= P) continue;
+        const int h = pi / hd, d = pi - h * hd;
+        const float *ph = s.sc[h];
+        const uint16_t *vc = Vv + d;
+        float a0 = oacc[k] * s.alpha[h], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int j = part;
+        for (; j + 3 * T < n; j += 4 * T) {
+            a0 = fmaf(ph[j], bf16_to_f(vc[size_t(j) * hd]), a0);
+            a1 = fmaf(ph[j + T], bf16_to_f(vc[size_t(j + T) * hd]), a1);
+            a2 = fmaf(ph[j + 2 * T], bf16_to_f(vc[size_t(j + 2 * T) * hd]), a2);
+            a3 = fmaf(ph[j + 3 * T], bf16_to_f(vc[size_t(j + 3 * T) * hd]), a3);
         }
+        for (; j < n; j += T) a0 = fmaf(ph[j], bf16_to_f(vc[size_t(j) * hd]), a0);
+        if (with_new && n % T == part) a0 = fmaf(ph[n], bf16_to_f(s.vnew[d]), a0);
+        oacc[k] = (a0 + a1) + (a2 + a3);
     }
     consumer_sync();
+    if (tid == 0) trace_put(p, ii, 10);
 }
 
-__device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, uint32_t &cpage) {
+__device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     if (!dep_wait(p, s, ins)) return false;
     const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
     const int hd = p.hd, half = hd / 2, G = p.nq / p.nkv, tid = threadIdx.x;
     const int qd = p.nq * p.hd, kd = p.nkv * p.hd;
+    const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     const float2 *cs = p.rope_cs + size_t(p.pos) * half;
     // RoPE ("rotate half") on the group's queries and on the new key
@@ -540,143 +697,256 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
         const float *q = p.qkv + size_t(g * G + h) * hd;
         const float a = __ldcg(q + i), b = __ldcg(q + i + half);
         const float2 r = cs[i];
-        s.qs[h][i] = (a * r.x - b * r.y) * scale;
-        s.qs[h][i + half] = (a * r.y + b * r.x) * scale;
+        s.qs[h][qs_index(i)] = (a * r.x - b * r.y) * scale;
+        s.qs[h][qs_index(i + half)] = (a * r.y + b * r.x) * scale;
     }
-    for (int i = tid; i < half; i += NCT) {
-        const float *k = p.qkv + qd + size_t(g) * hd;
-        const float a = __ldcg(k + i), b = __ldcg(k + i + half);
-        const float2 r = cs[i];
-        s.knew[i] = f_to_bf16(a * r.x - b * r.y);
-        s.knew[i + half] = f_to_bf16(a * r.y + b * r.x);
+    if (owner) {
+        for (int i = tid; i < half; i += NCT) {
+            const float *k = p.qkv + qd + size_t(g) * hd;
+            const float a = __ldcg(k + i), b = __ldcg(k + i + half);
+            const float2 r = cs[i];
+            s.knew[i] = f_to_bf16(a * r.x - b * r.y);
+            s.knew[i + half] = f_to_bf16(a * r.y + b * r.x);
+        }
+        for (int d = tid; d < hd; d += NCT) s.vnew[d] = f_to_bf16(__ldcg(p.qkv + qd + kd + size_t(g) * hd + d));
     }
-    for (int d = tid; d < hd; d += NCT) s.vnew[d] = f_to_bf16(__ldcg(p.qkv + qd + kd + size_t(g) * hd + d));
     if (tid < G) {
         s.m_run[tid] = -INFINITY;
         s.l_run[tid] = 0.f;
     }
     consumer_sync();
-    const size_t head_base = (size_t(l) * p.nkv + g) * size_t(p.max_seq) * hd;
-    if (c == S - 1) {  // this split owns position pos: write the new entry
+    if (tid == 0) trace_put(p, ii, 1);
+    if (owner) {
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
         for (int d = tid; d < hd; d += NCT) {
-            p.k_cache[head_base + size_t(p.pos) * hd + d] = s.knew[d];
-            p.v_cache[head_base + size_t(p.pos) * hd + d] = s.vnew[d];
+            p.k_cache[at + d] = s.knew[d];
+            p.v_cache[at + d] = s.vnew[d];
         }
     }
-    float oacc[4] = {0.f, 0.f, 0.f, 0.f};
+    float oacc[2] = {0.f, 0.f};
     int c0, c1;
     attn_range(p, c, c0, c1);
     const int PP = attn_pp(p);
     for (int p0 = c0; p0 < c1; p0 += PP) {
         const int n = min(PP, c1 - p0);
+        const bool with_new = owner && p0 + PP >= c1;  // fold the new token into the last page
         const uint32_t slot = cpage % NPAGES, par = (cpage / NPAGES) & 1u;
         if (!wait_page(p, s, &s.full[slot], par)) return false;
+        if (tid == 0) {
+            ptrace_put(p, cpage, 1);
+            trace_put(p, ii, 6);
+        }
         const uint16_t *pg = reinterpret_cast<const uint16_t *>(pages + size_t(slot) * PAGE_BYTES);
-        attn_block(p, s, pg, pg + PAGE_BYTES / 4, n, oacc, G);  // V at half a page
-        if (tid == 0) mbar_arrive(&s.empty[slot]);
+        if (hd == 64) attn_block<8>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);  // V at half a page
+        else attn_block<16>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);
+        if (tid == 0) {
+            ptrace_put(p, cpage, 2);
+            mbar_arrive(&s.empty[slot]);
+        }
         ++cpage;
     }
-    if (c == S - 1) attn_block(p, s, s.knew, s.vnew, 1, oacc, G);
+    if (owner && c0 == c1) {
+        if (hd == 64) attn_block<8>(p, s, nullptr, nullptr, 0, true, oacc, G, ii);
+        else attn_block<16>(p, s, nullptr, nullptr, 0, true, oacc, G, ii);
+    }
+    if (tid == 0) trace_put(p, ii, 7);
 
-    // partials: part[(qhead * S + c) * (hd + 2) + {d, hd: m, hd+1: l}]
-    const int stride = hd + 2;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int pi = tid + k * NCT;
-        if (pi < G * hd) {
+    // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}]
+    const int stride = hd + 4, P = G * hd, T = p.attn_T;
+    if (T > 1) {
+        float a = oacc[0];
+        for (int off = T / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        const int pi = tid / T;
+        if (tid % T == 0 && pi < P) {
             const int h = pi / hd, d = pi % hd;
-            p.part[(size_t(g * G + h) * S + c) * stride + d] = oacc[k];
+            p.part[(size_t(g * G + h) * S + c) * stride + d] = a;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const int pi = tid + k * NCT;
+            if (pi < P) {
+                const int h = pi / hd, d = pi % hd;
+                p.part[(size_t(g * G + h) * S + c) * stride + d] = oacc[k];
+            }
         }
     }
     if (tid < G) {
         p.part[(size_t(g * G + tid) * S + c) * stride + hd] = s.m_run[tid];
         p.part[(size_t(g * G + tid) * S + c) * stride + hd + 1] = s.l_run[tid];
     }
-    consumer_sync();
-    if (tid == 0) {
-        __threadfence();
-        const int tk = CtrLayout::attn_ticket(p.L, l, g, p.nkv);
-        const uint32_t old = atomicAdd(p.ctr + size_t(tk) * CTR_STRIDE, 1u);
-        s.flag = (old + 1u == p.epoch * static_cast<uint32_t>(S)) ? 1 : 0;
-        __threadfence();
-    }
-    consumer_sync();
-    if (s.flag) {  // last split of this KV head: merge all splits
-        for (int pi = tid; pi < G * hd; pi += NCT) {
-            const int h = pi / hd, d = pi % hd;
-            const float *base = p.part + size_t(g * G + h) * S * stride;
-            float M = -INFINITY;
-            for (int j = 0; j < S; j++) M = fmaxf(M, __ldcg(base + size_t(j) * stride + hd));
-            float L = 0.f, O = 0.f;
-            for (int j = 0; j < S; j++) {
-                const float mj = __ldcg(base + size_t(j) * stride + hd);
-                if (mj == -INFINITY) continue;
-                const float w = expf(mj - M);
-                L = fmaf(__ldcg(base + size_t(j) * stride + hd + 1), w, L);
-                O = fmaf(__ldcg(base + size_t(j) * stride + d), w, O);
-            }
-            p.o[size_t(g * G + h) * hd + d] = O / L;
-        }
-        signal_done(p, ins);
-    }
+    if (tid == 0) trace_put(p, ii, 2);
+    signal_done(p, ins);
+    if (tid == 0) trace_put(p, ii, 11);
     return true;
 }
 
 // ---------------------------------------------------------------------------------
 // Producer: walks the same instruction list and streams every page in order.
+// While the ring is full and the consumers are held up by a dependency, it keeps
+// HBM busy by prefetching the pages that come next into L2
+// (cp.async.bulk.prefetch.L2), up to p.l2_prefetch pages ahead of the ring, so
+// that the ring refills from L2 once the dependency is met.
 
-__device__ bool issue_page(const KParams &p, Smem &s, uint8_t *pages, uint32_t &ppage, const void *src0,
-                           uint32_t bytes0, const void *src1, uint32_t bytes1) {
-    const uint32_t slot = ppage % NPAGES;
-    if (ppage >= NPAGES) {
-        if (!wait_page(p, s, &s.empty[slot], ((ppage / NPAGES) - 1u) & 1u)) return false;
-    }
-    uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
-    mbar_expect_tx(&s.full[slot], bytes0 + bytes1);
-    if (bytes0) bulk_load(dst, src0, bytes0, &s.full[slot]);
-    if (bytes1) bulk_load(dst + PAGE_BYTES / 2, src1, bytes1, &s.full[slot]);
-    ++ppage;
-    return true;
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+struct PageDesc {
+    const void *src0, *src1;
+    uint32_t b0, b1;
+    int instr;
+    bool weights;  // streamed once per step: evict first from L2
+};
+
+// Yields the pages of an SM's instruction list in consumption order.
+struct PageIter {
+    const Instr *list;
+    int n, i;
+    bool open;
+    Seg seg[3];
+    int nseg, si, pr;
+    int p0, c1;
+    size_t head_base;
+
+    __device__ void init(const Instr *l, int nn) {
+        list = l;
+        n = nn;
+        i = 0;
+        open = false;
+    }
+
+    __device__ bool next(const KParams &p, PageDesc &d) {
+        while (i < n) {
+            const Instr ins = list[i];
+            if (!open) {
+                if (ins.op == OP_ATTN) {
+                    int c0;
+                    attn_range(p, ins.r1, c0, c1);
+                    p0 = c0;
+                    head_base = (size_t(ins.layer) * p.nkv + ins.r0) * size_t(p.max_seq) * p.hd;
+                } else {
+                    nseg = mv_segments(p, ins, seg);
+                    si = 0;
+                    pr = 0;
+                }
+                open = true;
+            }
+            d.instr = i;
+            if (ins.op == OP_ATTN) {
+                if (p0 < c1) {
+                    const int nn = min(attn_pp(p), c1 - p0);
+                    const uint32_t b = uint32_t(nn) * p.hd * 2;
+                    d.src0 = p.k_cache + head_base + size_t(p0) * p.hd;
+                    d.src1 = p.v_cache + head_base + size_t(p0) * p.hd;
+                    d.b0 = d.b1 = b;
+                    d.weights = false;
+                    p0 += nn;
+                    return true;
+                }
+            } else {
+                const MvShape &mv = mv_of(p, ins.op);
+                while (si < nseg) {
+                    if (pr < seg[si].nrows) {
+                        const int nr = min(mv.rpp, seg[si].nrows - pr);
+                        d.src0 = seg[si].w + size_t(seg[si].row0 + pr) * mv.K;
+                        d.b0 = uint32_t(nr) * mv.K * 2;
+                        d.src1 = nullptr;
+                        d.b1 = 0;
+                        d.weights = true;
+                        pr += nr;
+                        return true;
+                    }
+                    ++si;
+                    pr = 0;
+                }
+            }
+            ++i;
+            open = false;
+        }
+        return false;
+    }
+};
 
 __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
     const int n = p.n_instr[blockIdx.x];
-    uint32_t ppage = 0;
-    bool ok = true;
-    for (int i = 0; i < n && ok; i++) {
-        const Instr ins = list[i];
-        if (ins.op == OP_ATTN) {
-            int c0, c1;
-            attn_range(p, ins.r1, c0, c1);
-            const int PP = attn_pp(p), hd = p.hd;
-            const size_t head_base = (size_t(ins.layer) * p.nkv + ins.r0) * size_t(p.max_seq) * hd;
-            for (int p0 = c0; p0 < c1 && ok; p0 += PP) {
-                const int nn = min(PP, c1 - p0);
-                const uint32_t b = uint32_t(nn) * hd * 2;
-                ok = issue_page(p, s, pages, ppage, p.k_cache + head_base + size_t(p0) * hd, b,
-                                p.v_cache + head_base + size_t(p0) * hd, b);
+    uint64_t evict_first;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+    PageIter ld, pf;
+    ld.init(list, n);
+    pf.init(list, n);
+    uint32_t ppage = 0, pfidx = 0;
+    bool pf_more = true;
+    int last_instr = -1;
+    PageDesc d, q;
+    while (ld.next(p, d)) {
+        const uint32_t slot = ppage % NPAGES;
+        if (ppage >= NPAGES) {
+            uint64_t *bar = &s.empty[slot];
+            const uint32_t par = ((ppage / NPAGES) - 1u) & 1u;
+            if (!mbar_test(bar, par)) {
+                while (pf_more && pfidx < ppage) {  // pages already in the ring need no prefetch
+                    pf_more = pf.next(p, q);
+                    ++pfidx;
+                }
+                const uint64_t t0 = gtimer();
+                bool ok = true;
+                for (uint32_t it = 1;; ++it) {
+                    if (mbar_test(bar, par)) break;
+                    if (pf_more && pfidx < ppage + p.l2_prefetch) {
+                        pf_more = pf.next(p, q);
+                        if (pf_more) {
+                            bulk_prefetch_l2(q.src0, q.b0);
+                            if (q.b1) bulk_prefetch_l2(q.src1, q.b1);
+                            ++pfidx;
+                        }
+                        continue;
+                    }
+                    // back off: a spinning producer would take issue slots from the
+                    // consumer warps that share its scheduler
+                    __nanosleep(p.producer_sleep_ns);
+                    if ((it & 15u) == 0) {
+                        if (s.abort) { ok = false; break; }
+                        if (gtimer() - t0 > p.timeout_ns) {
+                            raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!ok) break;
             }
-            continue;
         }
-        const MvShape &mv = mv_of(p, ins.op);
-        Seg seg[3];
-        const int nseg = mv_segments(p, ins, seg);
-        for (int si = 0; si < nseg && ok; si++) {
-            for (int pr = 0; pr < seg[si].nrows && ok; pr += mv.rpp) {
-                const int nr = min(mv.rpp, seg[si].nrows - pr);
-                const uint16_t *src = seg[si].w + size_t(seg[si].row0 + pr) * mv.K;
-                ok = issue_page(p, s, pages, ppage, src, uint32_t(nr) * mv.K * 2, nullptr, 0);
-            }
+        uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
+        ptrace_put(p, ppage, 0);
+        mbar_expect_tx(&s.full[slot], d.b0 + d.b1);
+        if (d.weights && p.evict_first) bulk_load_hint(dst, d.src0, d.b0, &s.full[slot], evict_first);
+        else bulk_load(dst, d.src0, d.b0, &s.full[slot]);
+        if (d.b1) bulk_load(dst + PAGE_BYTES / 2, d.src1, d.b1, &s.full[slot]);
+        if (d.instr != last_instr) {
+            trace_put(p, d.instr, 4);
+            last_instr = d.instr;
         }
+        trace_put(p, d.instr, 5);
+        ++ppage;
     }
     // Never leave with copies in flight into this block's shared memory: wait for
     // the newest page of every slot (older ones completed before their slot was
     // reused). In a normal step the consumers wait for the same pages.
     const uint32_t first = ppage > NPAGES ? ppage - NPAGES : 0;
-    for (uint32_t q = first; q < ppage; q++) {
-        uint64_t *bar = &s.full[q % NPAGES];
-        const uint32_t par = (q / NPAGES) & 1u;
+    for (uint32_t qi = first; qi < ppage; qi++) {
+        uint64_t *bar = &s.full[qi % NPAGES];
+        const uint32_t par = (qi / NPAGES) & 1u;
         const uint64_t t0 = gtimer();
         while (!mbar_test(bar, par)) {
             if (gtimer() - t0 > p.timeout_ns) {
@@ -695,19 +965,21 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     int best_idx = -1;
     for (int i = 0; i < n; i++) {
         const Instr ins = list[i];
+        if (threadIdx.x == 0) trace_put(p, i, 0);
         bool ok;
         if (ins.op == OP_ATTN) {
-            ok = attn_instr(p, s, pages, ins, cpage);
+            ok = attn_instr(p, s, pages, ins, i, cpage);
         } else {
-            switch (mv_of(p, ins.op).vpl) {
-                case 1: ok = mv_instr<1>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 2: ok = mv_instr<2>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 3: ok = mv_instr<3>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 4: ok = mv_instr<4>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 5: ok = mv_instr<5>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 6: ok = mv_instr<6>(p, s, pages, ins, cpage, best, best_idx); break;
-                case 7: ok = mv_instr<7>(p, s, pages, ins, cpage, best, best_idx); break;
-                default: ok = mv_instr<8>(p, s, pages, ins, cpage, best, best_idx); break;
+            const MvShape &mv = mv_of(p, ins.op);
+            switch (mv.vpl * 16 + mv.rw) {
+#define LL_MV_CASE(V, R) \
+    case V * 16 + R: ok = mv_instr<V, R>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                LL_MV_CASE(1, 1) LL_MV_CASE(1, 2) LL_MV_CASE(1, 4) LL_MV_CASE(1, 8)
+                LL_MV_CASE(2, 1) LL_MV_CASE(2, 2) LL_MV_CASE(2, 4)
+                LL_MV_CASE(3, 1) LL_MV_CASE(3, 2)
+                LL_MV_CASE(4, 1) LL_MV_CASE(4, 2)
+#undef LL_MV_CASE
+                default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
             }
             if (ok && ins.op == OP_LMHEAD) {
                 lm_finish(p, s, best, best_idx);
@@ -716,6 +988,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
             }
         }
         if (!ok) return;
+        if (threadIdx.x == 0) trace_put(p, i, 3);
     }
 }
 
@@ -727,6 +1000,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         for (int i = 0; i < NPAGES; i++) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
+            s.pcnt[i] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.abort = 0;

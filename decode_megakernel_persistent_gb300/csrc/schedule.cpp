@@ -54,7 +54,7 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
                 lists[sm].push_back(make(OP_ATTN, l, sm / splits, sm % splits, CtrLayout::qkv(l), all,
                                          CtrLayout::attn(l)));
             split_rows(H, nsm, sm, r0, r1);
-            lists[sm].push_back(make(OP_OPROJ, l, r0, r1, CtrLayout::attn(l), static_cast<uint32_t>(nkv),
+            lists[sm].push_back(make(OP_OPROJ, l, r0, r1, CtrLayout::attn(l), static_cast<uint32_t>(nkv * splits),
                                      CtrLayout::oproj(l)));
             split_rows(I, nsm, sm, r0, r1);
             lists[sm].push_back(make(OP_GATEUP, l, r0, r1, CtrLayout::oproj(l), all, CtrLayout::gateup(l)));
@@ -69,26 +69,31 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
     }
 }
 
-// Input-vector geometry for width K (see MvShape). Returns false if K is not
-// supported: K must split into 256-element warp slices with at most 8 16-byte
-// vectors per lane.
+// Input-vector geometry for width K (see MvShape): among the splits of a row
+// into k-slices of 256*vpl elements (vpl <= 8), pick the one that keeps the most
+// consumer warps busy, rows per warp a power of two and vpl * rw <= 8 (register
+// budget), then the smallest vpl. Returns false if K admits none.
 bool mv_shape(int K, MvShape &m) {
-    for (int ws = 1; ws <= NCW; ws *= 2) {
-        if (K % (256 * ws) != 0) continue;
-        const int vpl = K / (256 * ws);
-        if (vpl > MAX_VPL) continue;
-        const int groups = NCW / ws;
-        const int64_t group_bytes = int64_t(groups) * K * 2;
-        if (group_bytes > PAGE_BYTES) return false;
-        const int rpp = groups * static_cast<int>(PAGE_BYTES / group_bytes);
-        if (rpp > MAX_RPP) continue;
-        m.K = K;
-        m.ws = ws;
-        m.vpl = vpl;
-        m.rpp = rpp;
-        return true;
+    if (K <= 0 || K % 256 != 0 || K > 16384) return false;
+    const int rows_fit = PAGE_BYTES / (2 * K);
+    int best_active = 0;
+    for (int vpl = 1; vpl <= MAX_VPL; vpl++) {
+        if (K % (256 * vpl) != 0) continue;
+        const int ws = K / (256 * vpl);
+        if (ws > NCW) continue;
+        int rg = std::min(NCW / ws, rows_fit);
+        if (rg < 1) continue;
+        int rw = 1;
+        while (rw * 2 * rg <= rows_fit && rw * 2 <= 8 && vpl * rw * 2 <= 8) rw *= 2;
+        const int rpp = rg * rw;
+        if (rpp > MAX_RPP || rpp * ws > MAX_PART) continue;
+        const int active = ws * rg;
+        if (active > best_active) {
+            best_active = active;
+            m = MvShape{K, ws, vpl, rpp, rg, rw};
+        }
     }
-    return false;
+    return best_active > 0;
 }
 
 }  // namespace ll

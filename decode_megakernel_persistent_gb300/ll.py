@@ -29,6 +29,7 @@ LL_Q_SCRATCH_BYTES = 4
 LL_Q_MAX_INSTRS = 5
 LL_Q_LAUNCHES_PER_STEP = 6
 LL_Q_SMEM_BYTES = 7
+LL_Q_TRACE_BYTES = 8
 
 LL_FAULT_NONE = 0
 LL_FAULT_DROP_SIGNAL = 1
@@ -38,7 +39,8 @@ OP_QKV, OP_ATTN, OP_OPROJ, OP_GATEUP, OP_DOWN = range(5)
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
 EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_synchronize",
-           "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_last_error", "ll_free")
+           "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
+           "ll_free")
 
 
 class LLError(RuntimeError):
@@ -87,12 +89,16 @@ def lib() -> ctypes.CDLL:
     L.ll_decode_step_async.restype = ctypes.c_int
     L.ll_synchronize.argtypes = [vp]
     L.ll_synchronize.restype = ctypes.c_int
+    L.ll_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
+    L.ll_set_trace.restype = ctypes.c_int
     L.ll_set_timeout_ns.argtypes = [vp, u64]
     L.ll_set_timeout_ns.restype = ctypes.c_int
     L.ll_query.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]
     L.ll_query.restype = ctypes.c_int
     L.ll_debug_inject.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     L.ll_debug_inject.restype = ctypes.c_int
+    L.ll_plan.argtypes = [ctypes.POINTER(ll_config), i32, vp, ctypes.c_size_t, ctypes.POINTER(i32)]
+    L.ll_plan.restype = ctypes.c_int
     L.ll_last_error.argtypes = [vp]
     L.ll_last_error.restype = ctypes.c_char_p
     L.ll_free.argtypes = [vp]
@@ -162,6 +168,12 @@ def ll_synchronize(h) -> None:
     _check(h, lib().ll_synchronize(h))
 
 
+def ll_set_trace(h, trace_dev=None) -> None:
+    """Enable (a CUDA uint64/int64 tensor of LL_Q_TRACE_BYTES bytes) or disable (None) tracing."""
+    nbytes = 0 if trace_dev is None else trace_dev.numel() * trace_dev.element_size()
+    _check(h, lib().ll_set_trace(h, _ptr(trace_dev), nbytes))
+
+
 def ll_set_timeout_ns(h, ns: int) -> None:
     _check(h, lib().ll_set_timeout_ns(h, int(ns)))
 
@@ -174,6 +186,20 @@ def ll_query(h, what: int) -> int:
 
 def ll_debug_inject(h, kind: int, layer: int = 0, op: int = 0) -> None:
     _check(h, lib().ll_debug_inject(h, int(kind), int(layer), int(op)))
+
+
+def ll_plan(cfg: ll_config, nsm: int):
+    """The schedule for `nsm` SMs as an int32 numpy array [nsm, max_instr, 7] (host only)."""
+    import numpy as np
+    mx = ctypes.c_int32()
+    rc = lib().ll_plan(ctypes.byref(cfg), int(nsm), None, 0, ctypes.byref(mx))
+    if rc != LL_OK:
+        raise LLError(rc, "ll_plan rejected the configuration")
+    out = np.zeros((int(nsm), mx.value, 7), dtype=np.int32)
+    rc = lib().ll_plan(ctypes.byref(cfg), int(nsm), out.ctypes.data, out.size, ctypes.byref(mx))
+    if rc != LL_OK:
+        raise LLError(rc, "ll_plan failed")
+    return out
 
 
 def ll_last_error(h) -> str:

@@ -55,7 +55,8 @@ typedef struct ll_handle ll_handle;
 /* Model shape. Constraints checked by ll_init (LL_ERR_SHAPE otherwise):
  * n_q_heads % n_kv_heads == 0 and n_q_heads / n_kv_heads <= 8; head_dim 64 or
  * 128; hidden, n_q_heads*head_dim and inter multiples of 256 and at most 16384;
- * max_seq >= 1. */
+ * n_q_heads*head_dim at most 4096; each of those widths must split into at most
+ * 16 slices of 256, 512, 768 or 1024 elements; max_seq >= 1. */
 typedef struct {
     int32_t n_layers;
     int32_t hidden;
@@ -131,6 +132,19 @@ int ll_synchronize(ll_handle *h);
  * LL_ERR_DEP_TIMEOUT, lets its own copies land, and returns. Default 1 s. */
 int ll_set_timeout_ns(ll_handle *h, uint64_t ns);
 
+/* Timing trace of the megakernel (the page's time breakdown of one forward pass
+ * is what it is for). trace_dev is a caller-owned device buffer of at least
+ * LL_Q_TRACE_BYTES bytes. Its first part, [sm][instr][12] uint64 (max_instr from
+ * ll_plan), holds per instruction: consumer begin, dependency met and input
+ * loaded, pages consumed, end, the producer's first and last page issue, the
+ * first page in the consumers' hands, the compute on the pages done, and for
+ * attention the ends of the scores, softmax and P.V phases and of its signal.
+ * The second part, [sm][4096][3] uint64, holds per shared-memory page (page
+ * number modulo 4096): producer issue, consumer start, release. All values are
+ * %globaltimer nanoseconds; each traced step overwrites them. NULL turns tracing
+ * off (the default). Returns LL_ERR_ARG if the buffer is too small or misaligned. */
+int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
+
 /* Schedule and memory facts, for tests and reports. */
 #define LL_Q_NUM_SMS 0          /* blocks of the persistent kernel (one per SM) */
 #define LL_Q_ATTN_SPLITS 1      /* KV splits per KV head in the attention instruction */
@@ -140,6 +154,7 @@ int ll_set_timeout_ns(ll_handle *h, uint64_t ns);
 #define LL_Q_MAX_INSTRS 5       /* longest per-SM instruction list */
 #define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes */
 #define LL_Q_SMEM_BYTES 7       /* dynamic shared memory per block */
+#define LL_Q_TRACE_BYTES 8      /* size of the buffer ll_set_trace needs */
 int ll_query(const ll_handle *h, int what, int64_t *value);
 
 /* Fault injection for tests (host side only; nothing faults on the device):
@@ -150,6 +165,15 @@ int ll_query(const ll_handle *h, int what, int64_t *value);
 #define LL_FAULT_NONE 0
 #define LL_FAULT_DROP_SIGNAL 1
 int ll_debug_inject(ll_handle *h, int kind, int layer, int op);
+
+/* The per-SM instruction schedule ll_init would build for `cfg` on a device
+ * with `nsm` SMs; host only, needs no GPU. *max_instr receives the longest list.
+ * When out is not NULL it must hold nsm*max_instr*7 int32, filled [sm][i] with
+ * (op, layer, r0, r1, wait_counter, wait_count, signal_counter); op is 0 QKV,
+ * 1 attention, 2 O projection, 3 gate/up, 4 down, 5 LM head, -1 an unused slot;
+ * [r0, r1) is the SM's row range, or (KV head, split) for attention; counters
+ * are -1 where there is none. */
+int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr);
 
 /* Explanation of the last error on this handle (never NULL). */
 const char *ll_last_error(const ll_handle *h);

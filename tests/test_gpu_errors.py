@@ -72,7 +72,7 @@ def test_query_reports_schedule():
     h = pr.dec.handle
     nsm = ll.ll_query(h, ll.LL_Q_NUM_SMS)
     assert nsm == torch.cuda.get_device_properties(0).multi_processor_count
-    assert ll.ll_query(h, ll.LL_Q_ATTN_SPLITS) == nsm // synth.TINY.n_kv_heads
+    assert ll.ll_query(h, ll.LL_Q_ATTN_SPLITS) == max(1, min(1, nsm // synth.TINY.n_kv_heads))  # max_seq 8
     assert ll.ll_query(h, ll.LL_Q_LAUNCHES_PER_STEP) == 1
     assert ll.ll_query(h, ll.LL_Q_PAGE_BYTES) * ll.ll_query(h, ll.LL_Q_NUM_PAGES) <= ll.ll_query(h, ll.LL_Q_SMEM_BYTES)
     pr.close()
