@@ -36,6 +36,8 @@ def _inputs():
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
+    if os.environ.get("LL_DEBUG_CHECKS") == "1":
+        return True
     t = os.path.getmtime(LIB)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
@@ -48,6 +50,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]
     if verbose:
         flags += ["-Xptxas", "-v"]
+    if os.environ.get("LL_DEBUG_CHECKS") == "1":
+        # self-checking build: every hot-path index is bounds-checked on the device
+        flags += ["-DLL_DEBUG_CHECKS"]
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")

@@ -66,7 +66,9 @@ int upload_schedule(ll_handle *h) {
 // KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
 // longest context, at most one attention item per SM.
 int attn_splits(const ll_config &c, int nsm) {
-    const int want = (c.max_seq + ll::ATTN_SPLIT_POS - 1) / ll::ATTN_SPLIT_POS;
+    int per = ll::ATTN_SPLIT_POS;  // tuning knob (environment), read at init
+    if (const char *e = std::getenv("LL_ATTN_SPLIT_POS")) per = std::max(1, std::atoi(e));
+    const int want = (c.max_seq + per - 1) / per;
     return std::max(1, std::min(want, nsm / c.n_kv_heads));
 }
 
@@ -188,7 +190,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         auto per_sm = [&](int64_t rows) { return (rows + h->nsm - 1) / h->nsm; };
         const int64_t qkv_rows = int64_t(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
         if (per_sm(qkv_rows) > ll::ACC_FLOATS || 2 * per_sm(c.inter) > ll::ACC_FLOATS ||
-            per_sm(c.hidden) > ll::ACC_FLOATS || per_sm(c.vocab) > ll::ACC_FLOATS) {
+            per_sm(c.hidden) > ll::XOWN_MAX || per_sm(c.vocab) > ll::ACC_FLOATS) {
             delete h;
             return bad(LL_ERR_SHAPE, "a projection has more rows per SM than the kernel holds");
         }
@@ -200,6 +202,10 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     }
     build_lists(h);
     for (auto &l : h->lists) h->max_instr = std::max<int>(h->max_instr, static_cast<int>(l.size()));
+    std::vector<ll::PDesc> pdesc;
+    std::vector<int32_t> pdesc_off;
+    ll::build_pdesc(h->lists, layers, c.tied ? w->embed : w->lm_head, c.hidden, qd, kd, c.inter, mh, mq, mi, pdesc,
+                    pdesc_off);
 
     // ---- library memory: one allocation carved into 256-byte aligned pieces
     const size_t nctr = size_t(ll::CtrLayout::count(c.n_layers, c.n_kv_heads)) * ll::CTR_STRIDE;
@@ -207,17 +213,22 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     Instr *d_instrs = nullptr;
     int32_t *d_n_instr = nullptr;
     ll::LayerW *d_layers = nullptr;
+    ll::PDesc *d_pdesc = nullptr;
+    int32_t *d_pdesc_off = nullptr;
     float2 *d_rope = nullptr;
     float *x = nullptr, *qkv = nullptr, *part = nullptr, *o = nullptr, *act = nullptr;
     float *hbuf = nullptr, *gate = nullptr, *up = nullptr, *logits = nullptr;
     unsigned long long *keys = nullptr;
     uint32_t *ctr = nullptr;
     int32_t *status = nullptr, *tok = nullptr;
+    long long *dbg = nullptr;
     const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 4);
     Piece pieces[] = {
         {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
         {reinterpret_cast<void **>(&d_n_instr), size_t(h->nsm) * sizeof(int32_t)},
         {reinterpret_cast<void **>(&d_layers), size_t(c.n_layers) * sizeof(ll::LayerW)},
+        {reinterpret_cast<void **>(&d_pdesc), pdesc.size() * sizeof(ll::PDesc)},
+        {reinterpret_cast<void **>(&d_pdesc_off), pdesc_off.size() * sizeof(int32_t)},
         {reinterpret_cast<void **>(&d_rope), size_t(c.max_seq) * (c.head_dim / 2) * sizeof(float2)},
         {reinterpret_cast<void **>(&x), size_t(c.hidden) * 4},
         {reinterpret_cast<void **>(&qkv), size_t(qd + 2 * kd) * 4},
@@ -232,6 +243,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&ctr), nctr * 4},
         {reinterpret_cast<void **>(&status), 4},
         {reinterpret_cast<void **>(&tok), 4},
+        {reinterpret_cast<void **>(&dbg), 64},
     };
     size_t total = 0;
     for (auto &pc : pieces) total += round_up(pc.bytes, 256);
@@ -266,6 +278,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     KParams &p = h->kp;
     p.instrs = d_instrs;
     p.n_instr = d_n_instr;
+    p.pdesc = d_pdesc;
+    p.pdesc_off = d_pdesc_off;
     p.max_instr = h->max_instr;
     p.nsm = h->nsm;
     p.layers = d_layers;
@@ -303,10 +317,13 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.ctr = ctr;
     p.status = status;
     p.token_out = tok;
+#ifdef LL_DEBUG_CHECKS
+    p.dbg = dbg;
+#endif
     p.timeout_ns = 1000000000ull;
     // tuning knobs (environment, read once here): L2 prefetch distance in pages and
     // the evict-first hint on weight pages
-    p.l2_prefetch = 16;
+    p.l2_prefetch = 4;
     p.evict_first = 1;
     if (const char *e = std::getenv("LL_L2_PREFETCH_PAGES")) p.l2_prefetch = static_cast<uint32_t>(std::atoi(e));
     if (const char *e = std::getenv("LL_EVICT_FIRST")) p.evict_first = static_cast<uint32_t>(std::atoi(e));
@@ -329,9 +346,13 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
 
     bool ok = cudaMemcpy(d_layers, layers.data(), layers.size() * sizeof(ll::LayerW), cudaMemcpyHostToDevice) ==
                   cudaSuccess &&
+              cudaMemcpy(d_pdesc, pdesc.data(), pdesc.size() * sizeof(ll::PDesc), cudaMemcpyHostToDevice) ==
+                  cudaSuccess &&
+              cudaMemcpy(d_pdesc_off, pdesc_off.data(), pdesc_off.size() * sizeof(int32_t), cudaMemcpyHostToDevice) ==
+                  cudaSuccess &&
               cudaMemcpy(d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemset(ctr, 0, nctr * 4) == cudaSuccess && cudaMemset(status, 0, 4) == cudaSuccess &&
-              cudaMemset(tok, 0, 4) == cudaSuccess;
+              cudaMemset(tok, 0, 4) == cudaSuccess && cudaMemset(dbg, 0, 64) == cudaSuccess;
     if (!ok || upload_schedule(h) != LL_OK) {
         ll_free(h);
         return bad(LL_ERR_CUDA, "initial upload failed");
@@ -339,6 +360,17 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     *out = h;
     return LL_OK;
 }
+
+#ifdef LL_DEBUG_CHECKS
+static void report_debug(ll_handle *h) {
+    long long rec[8] = {0};
+    if (h->kp.dbg && cudaMemcpy(rec, h->kp.dbg, sizeof rec, cudaMemcpyDeviceToHost) == cudaSuccess && rec[0])
+        std::fprintf(stderr, "LL_DEBUG_CHECKS: code %lld sm %lld thread %lld index %lld limit %lld\n", rec[1], rec[2],
+                     rec[3], rec[4], rec[5]);
+}
+#else
+static void report_debug(ll_handle *) {}
+#endif
 
 int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev, int32_t *next_token_host) {
     if (!h) return LL_ERR_ARG;
@@ -351,6 +383,7 @@ int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev, 
         cudaError_t e = cudaGetLastError();
         return fail(h, LL_ERR_CUDA, std::string("step failed: ") + cudaGetErrorString(e));
     }
+    report_debug(h);
     const int32_t st = h->pinned[1];
     if (st != 0) {
         reset_device_state(h);

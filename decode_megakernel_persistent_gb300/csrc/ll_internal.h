@@ -26,6 +26,7 @@ constexpr int MAX_RPP = 64;                // rows per page (hidden 256 at one v
 constexpr int MAX_PART = 128;              // (row, k-slice) partial sums per page
 constexpr int ACC_FLOATS = 2048;           // per-SM row results held until the instruction ends
 constexpr int XIN_FLOATS = 4096;           // largest O-projection input (n_q_heads * head_dim)
+constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden / SMs, rounded up)
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
 constexpr int TRACE_WORDS = 12;            // timestamps per traced instruction
 constexpr int PTRACE_PAGES = 4096;         // pages per SM the page trace keeps (a ring)
@@ -47,13 +48,27 @@ struct Instr {
     int32_t sig_ctr;      // counter to bump when done, -1 for none
 };
 
-// Matrix-vector geometry for one input width K. A page holds rpp whole rows. The
-// row is cut into ws k-slices of 256*vpl elements; warp w works on slice w % ws of
-// rows w / ws + q * rg (q < rw) of every page, so ws * rg warps are active and
-// each lane keeps vpl 16-byte vectors of the input in registers.
+// Matrix-vector geometry for one input width K. The consumer warps form `teams`
+// teams of NCW / teams warps; page number p of the SM goes to team p % teams, so
+// several pages are worked on at once. A page holds rpp whole rows. Within a
+// team the row is cut into ws k-slices of 256*vpl elements; team warp w works on
+// slice w % ws of rows w / ws + q * rg (q < rw) of each of its pages, so ws * rg
+// warps of the team are active and each lane keeps vpl 16-byte vectors of the
+// input in registers.
 struct MvShape {
-    int32_t K, ws, vpl, rpp, rg, rw;
+    int32_t K, ws, vpl, rpp, rg, rw, teams;
 };
+
+// One entry of an SM's producer list, in consumption order: a weight page
+// (src, bytes), or an attention item whose K/V pages depend on pos and are
+// expanded on the device (src then packs layer << 32 | kv_head << 16 | split).
+struct PDesc {
+    unsigned long long src;
+    uint32_t bytes;
+    uint16_t instr;  // index of the instruction the page belongs to
+    uint16_t kind;   // PD_WEIGHTS or PD_ATTN
+};
+enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1 };
 
 struct LayerW {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
@@ -76,6 +91,8 @@ struct KParams {
     // schedule
     const Instr *instrs;      // [nsm][max_instr]
     const int32_t *n_instr;   // [nsm]
+    const PDesc *pdesc;       // producer lists of all SMs, back to back
+    const int32_t *pdesc_off; // [nsm + 1] start of each SM's list
     int32_t max_instr;
     int32_t nsm;
     // model
@@ -117,6 +134,8 @@ struct KParams {
     // optional page trace, [nsm][PTRACE_PAGES][3]: producer issue, consumer start,
     // release, indexed by page number modulo PTRACE_PAGES
     unsigned long long *ptrace;
+    // debug builds (LL_DEBUG_CHECKS): first out-of-range access seen, else null
+    long long *dbg;
 };
 
 // Host-side launchers (defined in the .cu files).
@@ -135,5 +154,8 @@ int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
 void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm, int splits,
                     std::vector<std::vector<Instr>> &lists);
 bool mv_shape(int K, MvShape &m);
+void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector<LayerW> &layers,
+                 const uint16_t *lm_head, int H, int qd, int kd, int I, const MvShape &mh, const MvShape &mq,
+                 const MvShape &mi, std::vector<PDesc> &out, std::vector<int32_t> &off);
 
 }  // namespace ll

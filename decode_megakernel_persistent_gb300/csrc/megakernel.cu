@@ -98,6 +98,24 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
@@ -153,10 +171,12 @@ struct alignas(16) Smem {
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
     uint64_t empty[NPAGES];  // page released by the consumers
     int32_t pcnt[NPAGES];    // warps done with the page in the slot
+    volatile uint32_t slot_page[NPAGES];  // page number the producer last put in the slot
     float part[NPAGES][MAX_PART];  // per page: (row, k-slice) partial sums
     alignas(16) uint16_t knew[MAX_HD];
     alignas(16) uint16_t vnew[MAX_HD];
     float m_run[MAX_GQA], l_run[MAX_GQA], alpha[MAX_GQA];
+    float xown[XOWN_MAX];  // this SM's rows of the residual stream (the O and down rows)
     float nred[NCW];
     unsigned long long kred[NCW];
     int32_t token;
@@ -183,6 +203,27 @@ __device__ __forceinline__ void trace_put(const KParams &p, int ii, int k) {
     if (p.trace) p.trace[(size_t(blockIdx.x) * p.max_instr + ii) * TRACE_WORDS + k] = gtimer();
 }
 
+// Debug builds check every shared- and global-memory index of the hot paths;
+// the first out-of-range access is recorded in p.dbg (code, sm, thread, index,
+// limit) and skipped. Release builds compile the checks away.
+#ifdef LL_DEBUG_CHECKS
+__device__ __noinline__ bool ll_check_fail(const KParams &p, int code, long long a, long long b) {
+    if (p.dbg && atomicCAS(reinterpret_cast<unsigned long long *>(p.dbg), 0ull, 1ull) == 0ull) {
+        p.dbg[1] = code;
+        p.dbg[2] = blockIdx.x;
+        p.dbg[3] = threadIdx.x;
+        p.dbg[4] = a;
+        p.dbg[5] = b;
+    }
+    return false;
+}
+#define LL_OK_IDX(code, idx, lim) \
+    ((static_cast<long long>(idx) >= 0 && static_cast<long long>(idx) < static_cast<long long>(lim)) || \
+     ll_check_fail(p, (code), static_cast<long long>(idx), static_cast<long long>(lim)))
+#else
+#define LL_OK_IDX(code, idx, lim) true
+#endif
+
 __device__ __forceinline__ void ptrace_put(const KParams &p, uint32_t page, int k) {
     if (p.ptrace) p.ptrace[(size_t(blockIdx.x) * PTRACE_PAGES + page % PTRACE_PAGES) * 3 + k] = gtimer();
 }
@@ -206,7 +247,7 @@ __device__ bool wait_counter(const KParams &p, Smem &s, const uint32_t *ctr, uin
     }
 }
 
-__device__ bool wait_page(const KParams &p, Smem &s, uint64_t *bar, uint32_t parity) {
+__device__ bool wait_mbar(const KParams &p, Smem &s, uint64_t *bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
@@ -219,6 +260,27 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint64_t *bar, uint32_t par
             }
         }
     }
+}
+
+// Consumer wait for page number `page` in its ring slot. A phase-parity wait is
+// only unambiguous once the slot holds this page (consumers of different teams
+// may run more than one ring lap apart), so first wait until the producer has
+// put the page in the slot, then for its bytes.
+__device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
+    const uint32_t slot = page % NPAGES;
+    if (s.slot_page[slot] != page) {
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1; s.slot_page[slot] != page; ++it) {
+            if ((it & 15u) == 0) {
+                if (s.abort) return false;
+                if (gtimer() - t0 > p.timeout_ns) {
+                    raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+    return wait_mbar(p, s, &s.full[slot], (page / NPAGES) & 1u);
 }
 
 // Consumer-side dependency wait: thread 0 polls, everyone learns the outcome.
@@ -308,6 +370,8 @@ __device__ void stage_attention_output(const KParams &p, Smem &s) {
     const int S = p.attn_splits, stride = p.hd + 4, qd = p.nq * p.hd;
     for (int t = threadIdx.x; t < qd / 4; t += NCT) {
         const int e0 = t * 4, h = e0 / p.hd, d0 = e0 % p.hd;
+        if (!LL_OK_IDX(12, e0 + 4, XIN_FLOATS + 1) || !LL_OK_IDX(13, (size_t(h) * S + S) * stride, size_t(p.nq) * S * stride + 1))
+            continue;
         const float *base = p.part + size_t(h) * S * stride;
         float M = -INFINITY;
 #pragma unroll 4
@@ -332,28 +396,49 @@ __device__ void stage_attention_output(const KParams &p, Smem &s) {
 }
 
 // Lane-held input vector: element (sw*32*VPL + j*32 + lane)*8 + e sits in xr[j*8+e].
+// The RMSNorm gain of a normed instruction (QKV, gate/up, LM head), or null.
+__device__ __forceinline__ const uint16_t *norm_gain(const KParams &p, const Instr &ins) {
+    switch (ins.op) {
+        case OP_QKV: return p.layers[ins.layer].attn_norm;
+        case OP_GATEUP: return p.layers[ins.layer].mlp_norm;
+        case OP_LMHEAD: return p.final_norm;
+        default: return nullptr;
+    }
+}
+
+// Gains are weights: a lane's slice is fetched before the dependency wait.
+template <int VPL>
+__device__ __forceinline__ void load_gain(const KParams &p, const Instr &ins, const MvShape &mv, uint4 (&gv)[VPL]) {
+    const uint16_t *gain = norm_gain(p, ins);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sw = (warp % (NCW / mv.teams)) % mv.ws;
+#pragma unroll
+    for (int j = 0; j < VPL; j++)
+        gv[j] = gain ? __ldg(reinterpret_cast<const uint4 *>(gain) + sw * 32 * VPL + j * 32 + lane) : make_uint4(0, 0, 0, 0);
+}
+
 template <int VPL>
 __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
-                           float (&xr)[VPL * 8]) {
+                           float (&xr)[VPL * 8], const uint4 (&gv)[VPL]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sw = warp % mv.ws;
-    const uint16_t *gain = nullptr;
+    const int sw = (warp % (NCW / mv.teams)) % mv.ws;
+    const bool normed = norm_gain(p, ins) != nullptr;
     const float *src = nullptr;
     const uint16_t *src16 = nullptr;
     switch (ins.op) {
         case OP_QKV:
-            gain = p.layers[ins.layer].attn_norm;
             if (ins.layer == 0) src16 = p.embed + size_t(s.token) * p.H;
             else src = p.x;
             break;
-        case OP_GATEUP: gain = p.layers[ins.layer].mlp_norm; src = p.x; break;
-        case OP_LMHEAD: gain = p.final_norm; src = p.x; break;
+        case OP_GATEUP: src = p.x; break;
+        case OP_LMHEAD: src = p.x; break;
         case OP_OPROJ: stage_attention_output(p, s); break;
         default: src = p.act; break;
     }
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
         const int v = sw * 32 * VPL + j * 32 + lane;
+        if (!LL_OK_IDX(11, v * 8 + 8, mv.K + 1)) continue;
         if (ins.op == OP_OPROJ) {
             const float4 a = *reinterpret_cast<const float4 *>(&s.xin[v * 8]);
             const float4 b = *reinterpret_cast<const float4 *>(&s.xin[v * 8 + 4]);
@@ -372,7 +457,7 @@ __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
         }
     }
-    if (!gain) return;
+    if (!normed) return;
     // RMSNorm: the warps w < ws together hold every element once.
     float ss = 0.f;
 #pragma unroll
@@ -385,9 +470,7 @@ __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
     const float r = 1.0f / sqrtf(tot / static_cast<float>(mv.K) + p.eps);
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
-        const int v = sw * 32 * VPL + j * 32 + lane;
-        uint4 u = __ldg(reinterpret_cast<const uint4 *>(gain) + v);
-        const uint32_t g[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             xr[j * 8 + 2 * q] = xr[j * 8 + 2 * q] * r * bf_lo(g[q]);
@@ -430,18 +513,25 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     Seg seg[3];
     const int nseg = mv_segments(p, ins, seg);
     if (nseg == 0) return true;  // no rows here: nothing to read or wait for
+    uint4 gv[VPL];
+    load_gain<VPL>(p, ins, mv, gv);
     if (!dep_wait(p, s, ins)) return false;
 
     float xr[VPL * 8];
-    load_input<VPL>(p, s, ins, mv, xr);
+    load_input<VPL>(p, s, ins, mv, xr, gv);
+    // s.acc shares space with the O projection's staged input: every warp must
+    // hold its input before any team writes row results
+    if (ins.op == OP_OPROJ) consumer_sync();
     if (threadIdx.x == 0) trace_put(p, ii, 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int active = mv.ws * mv.rg;
-    const int sw = warp % mv.ws, rgi = warp / mv.ws;
-    const size_t row_bytes = size_t(mv.K) * 2;
+    const int W = NCW / mv.teams, team = warp / W, wt = warp % W;
+    const int active = mv.ws * mv.rg;  // working warps per team
+    const int sw = wt % mv.ws, rgi = wt / mv.ws;
+    const uint32_t row_bytes = uint32_t(mv.K) * 2;
     const int nrows = ins.r1 - ins.r0;
     constexpr int GROUP = 32 / RW;  // lanes that end up holding one row's sum
+    constexpr int QB = (RW < 4 / VPL) ? RW : (4 / VPL > 0 ? 4 / VPL : 1);  // rows loaded together
 
     for (int si = 0; si < nseg; si++) {
         const Seg sg = seg[si];
@@ -449,44 +539,53 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
         const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
         for (int pr = 0; pr < sg.nrows; pr += mv.rpp) {
             const int nr = min(mv.rpp, sg.nrows - pr);
-            const uint32_t slot = cpage % NPAGES, par = (cpage / NPAGES) & 1u;
+            const uint32_t slot = cpage % NPAGES;
             const uint32_t this_page = cpage++;
-            if (warp >= active) continue;
-            if (!wait_page(p, s, &s.full[slot], par)) return false;
-            if (warp == 0 && lane == 0) {
+            if (int(this_page % uint32_t(mv.teams)) != team || wt >= active) continue;
+            if (!wait_page(p, s, this_page)) return false;
+            if (wt == 0 && lane == 0) {
                 ptrace_put(p, this_page, 1);
                 if (si == 0 && pr == 0) trace_put(p, ii, 6);
             }
             const uint32_t page = smem_addr(pages) + slot * PAGE_BYTES + (sw * 32 * VPL + lane) * 16;
-            float a[RW][2];
-#pragma unroll
-            for (int q = 0; q < RW; q++) {
-                // rows past nr hold stale bytes; their sums are never used
-                const uint32_t wrow = page + uint32_t(rgi + q * mv.rg) * uint32_t(row_bytes);
-                uint4 wv[VPL];
-#pragma unroll
-                for (int j = 0; j < VPL; j++) wv[j] = lds128(wrow + j * 32 * 16);
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int j = 0; j < VPL; j++) {
-                    a0 = fmaf(bf_lo(wv[j].x), xr[j * 8 + 0], a0);
-                    a1 = fmaf(bf_hi(wv[j].x), xr[j * 8 + 1], a1);
-                    a0 = fmaf(bf_lo(wv[j].y), xr[j * 8 + 2], a0);
-                    a1 = fmaf(bf_hi(wv[j].y), xr[j * 8 + 3], a1);
-                    a0 = fmaf(bf_lo(wv[j].z), xr[j * 8 + 4], a0);
-                    a1 = fmaf(bf_hi(wv[j].z), xr[j * 8 + 5], a1);
-                    a0 = fmaf(bf_lo(wv[j].w), xr[j * 8 + 6], a0);
-                    a1 = fmaf(bf_hi(wv[j].w), xr[j * 8 + 7], a1);
-                }
-                a[q][0] = a0;
-                a[q][1] = a1;
-            }
             float v[RW];
 #pragma unroll
-            for (int q = 0; q < RW; q++) v[q] = a[q][0] + a[q][1];
+            for (int q0 = 0; q0 < RW; q0 += QB) {
+                // rows past nr hold stale bytes; their sums are never used
+                uint4 wv[QB][VPL];
+#pragma unroll
+                for (int qq = 0; qq < QB; qq++) {
+                    const uint32_t wrow = page + uint32_t(rgi + (q0 + qq) * mv.rg) * row_bytes;
+#pragma unroll
+                    for (int j = 0; j < VPL; j++) {
+                        if (LL_OK_IDX(1, (wrow + j * 32 * 16 + 16) - smem_addr(pages), NPAGES * PAGE_BYTES + 1))
+                            wv[qq][j] = lds128(wrow + j * 32 * 16);
+                        else
+                            wv[qq][j] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int qq = 0; qq < QB; qq++) {
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < VPL; j++) {
+                        const uint4 w = wv[qq][j];
+                        a0 = fmaf(bf_lo(w.x), xr[j * 8 + 0], a0);
+                        a1 = fmaf(bf_hi(w.x), xr[j * 8 + 1], a1);
+                        a0 = fmaf(bf_lo(w.y), xr[j * 8 + 2], a0);
+                        a1 = fmaf(bf_hi(w.y), xr[j * 8 + 3], a1);
+                        a0 = fmaf(bf_lo(w.z), xr[j * 8 + 4], a0);
+                        a1 = fmaf(bf_hi(w.z), xr[j * 8 + 5], a1);
+                        a0 = fmaf(bf_lo(w.w), xr[j * 8 + 6], a0);
+                        a1 = fmaf(bf_hi(w.w), xr[j * 8 + 7], a1);
+                    }
+                    v[q0 + qq] = a0 + a1;
+                }
+            }
             const float sum = transpose_reduce<RW>(v);
             const int q = lane / GROUP;
-            if ((lane % GROUP) == 0) s.part[slot][(rgi + q * mv.rg) * mv.ws + sw] = sum;
+            if ((lane % GROUP) == 0 && LL_OK_IDX(2, (rgi + q * mv.rg) * mv.ws + sw, MAX_PART))
+                s.part[slot][(rgi + q * mv.rg) * mv.ws + sw] = sum;
             __syncwarp();
             int last = 0;
             if (lane == 0) {
@@ -498,8 +597,9 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
                 __threadfence_block();
                 for (int r = lane; r < nr; r += 32) {
                     float y = 0.f;
-                    for (int w = 0; w < mv.ws; w++) y += s.part[slot][r * mv.ws + w];
-                    s.acc[acc0 + pr + r] = y;
+                    for (int w = 0; w < mv.ws; w++)
+                        if (LL_OK_IDX(3, r * mv.ws + w, MAX_PART)) y += s.part[slot][r * mv.ws + w];
+                    if (LL_OK_IDX(4, acc0 + pr + r, ACC_FLOATS)) s.acc[acc0 + pr + r] = y;
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -515,28 +615,35 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     const int r0 = ins.r0;
     switch (ins.op) {
         case OP_QKV:
-            for (int t = tid; t < nrows; t += NCT) p.qkv[r0 + t] = s.acc[t];
+            for (int t = tid; t < nrows; t += NCT)
+                if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS)) p.qkv[r0 + t] = s.acc[t];
             break;
         case OP_OPROJ:
         case OP_DOWN: {
+            // this SM owns rows [r0, r1) of the residual stream in both projections
+            // (same row split), so it keeps them in shared memory across layers
             const bool from_embed = ins.op == OP_OPROJ && ins.layer == 0;
             for (int t = tid; t < nrows; t += NCT) {
                 const int row = r0 + t;
-                const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : __ldcg(p.x + row);
-                p.x[row] = base + s.acc[t];
+                if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) continue;
+                const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : s.xown[t];
+                const float v = base + s.acc[t];
+                s.xown[t] = v;
+                p.x[row] = v;
             }
             break;
         }
         case OP_GATEUP:
             for (int t = tid; t < nrows; t += NCT) {
                 const float g = s.acc[t];
-                p.act[r0 + t] = g / (1.0f + expf(-g)) * s.acc[nrows + t];
+                if (LL_OK_IDX(8, r0 + t, p.I) && LL_OK_IDX(9, nrows + t, ACC_FLOATS))
+                    p.act[r0 + t] = g / (1.0f + expf(-g)) * s.acc[nrows + t];
             }
             break;
         default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
             for (int t = tid; t < nrows; t += NCT) {
                 const float y = s.acc[t];
-                if (p.logits) p.logits[r0 + t] = y;
+                if (p.logits && LL_OK_IDX(10, r0 + t, p.V)) p.logits[r0 + t] = y;
                 if (y > best) {
                     best = y;
                     best_idx = r0 + t;
@@ -610,18 +717,20 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
     const int nt = n + (with_new ? 1 : 0);
     // scores: thread per (head, position), head-major so a warp shares its query;
     // 16-byte chunks visited in an order rotated by position (spreads K over banks)
+    const uint32_t kbase = K ? smem_addr(K) : 0u, knew = smem_addr(s.knew);
     for (int t = tid; t < nt * G; t += NCT) {
         const int h = t / nt, j = t - h * nt;
-        const uint4 *k4 = reinterpret_cast<const uint4 *>(j < n ? K + size_t(j) * hd : s.knew);
-        const float *qh = s.qs[h];
+        if (!LL_OK_IDX(14, j, 132) || !LL_OK_IDX(15, h, MAX_GQA)) continue;
+        const uint32_t krow = j < n ? kbase + uint32_t(j) * (hd * 2) : knew;
+        const uint32_t qh = smem_addr(&s.qs[h][0]);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
+#pragma unroll 8
         for (int i = 0; i < NCH; i++) {
             const int c = (i + j) & (NCH - 1);
-            const uint4 u = k4[c];
+            const uint4 u = lds128(krow + c * 16);
             const int sw = ((c >> 2) & 1) << 2;
-            const float4 qa = *reinterpret_cast<const float4 *>(qh + (c << 3) + sw);
-            const float4 qb = *reinterpret_cast<const float4 *>(qh + (c << 3) + (4 - sw));
+            const float4 qa = lds_f4(qh + ((c << 3) + sw) * 4);
+            const float4 qb = lds_f4(qh + ((c << 3) + (4 - sw)) * 4);
             a0 = fmaf(qa.x, bf_lo(u.x), a0); a1 = fmaf(qa.y, bf_hi(u.x), a1);
             a2 = fmaf(qa.z, bf_lo(u.y), a2); a3 = fmaf(qa.w, bf_hi(u.y), a3);
             a0 = fmaf(qb.x, bf_lo(u.z), a0); a1 = fmaf(qb.y, bf_hi(u.z), a1);
@@ -665,18 +774,18 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
         const int pi = slot / T, part = slot % T;
         if ((T > 1 && k > 0) || pi >= P) continue;
         const int h = pi / hd, d = pi - h * hd;
-        const float *ph = s.sc[h];
-        const uint16_t *vc = Vv + d;
+        const uint32_t ph = smem_addr(&s.sc[h][0]);
+        const uint32_t vc = (Vv ? smem_addr(Vv) : 0u) + uint32_t(d) * 2;
         float a0 = oacc[k] * s.alpha[h], a1 = 0.f, a2 = 0.f, a3 = 0.f;
         int j = part;
         for (; j + 3 * T < n; j += 4 * T) {
-            a0 = fmaf(ph[j], bf16_to_f(vc[size_t(j) * hd]), a0);
-            a1 = fmaf(ph[j + T], bf16_to_f(vc[size_t(j + T) * hd]), a1);
-            a2 = fmaf(ph[j + 2 * T], bf16_to_f(vc[size_t(j + 2 * T) * hd]), a2);
-            a3 = fmaf(ph[j + 3 * T], bf16_to_f(vc[size_t(j + 3 * T) * hd]), a3);
+            a0 = fmaf(lds_f32(ph + j * 4), bf16_to_f(lds_u16(vc + uint32_t(j) * (hd * 2))), a0);
+            a1 = fmaf(lds_f32(ph + (j + T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + T) * (hd * 2))), a1);
+            a2 = fmaf(lds_f32(ph + (j + 2 * T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + 2 * T) * (hd * 2))), a2);
+            a3 = fmaf(lds_f32(ph + (j + 3 * T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + 3 * T) * (hd * 2))), a3);
         }
-        for (; j < n; j += T) a0 = fmaf(ph[j], bf16_to_f(vc[size_t(j) * hd]), a0);
-        if (with_new && n % T == part) a0 = fmaf(ph[n], bf16_to_f(s.vnew[d]), a0);
+        for (; j < n; j += T) a0 = fmaf(lds_f32(ph + j * 4), bf16_to_f(lds_u16(vc + uint32_t(j) * (hd * 2))), a0);
+        if (with_new && n % T == part) a0 = fmaf(lds_f32(ph + n * 4), bf16_to_f(s.vnew[d]), a0);
         oacc[k] = (a0 + a1) + (a2 + a3);
     }
     consumer_sync();
@@ -718,6 +827,7 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
         const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
+        if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
         for (int d = tid; d < hd; d += NCT) {
             p.k_cache[at + d] = s.knew[d];
             p.v_cache[at + d] = s.vnew[d];
@@ -730,8 +840,8 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
     for (int p0 = c0; p0 < c1; p0 += PP) {
         const int n = min(PP, c1 - p0);
         const bool with_new = owner && p0 + PP >= c1;  // fold the new token into the last page
-        const uint32_t slot = cpage % NPAGES, par = (cpage / NPAGES) & 1u;
-        if (!wait_page(p, s, &s.full[slot], par)) return false;
+        const uint32_t slot = cpage % NPAGES;
+        if (!wait_page(p, s, cpage)) return false;
         if (tid == 0) {
             ptrace_put(p, cpage, 1);
             trace_put(p, ii, 6);
@@ -771,7 +881,7 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
             }
         }
     }
-    if (tid < G) {
+    if (tid < G && LL_OK_IDX(17, (size_t(g * G + tid) * S + c) * stride + hd + 1, size_t(p.nq) * S * stride)) {
         p.part[(size_t(g * G + tid) * S + c) * stride + hd] = s.m_run[tid];
         p.part[(size_t(g * G + tid) * S + c) * stride + hd + 1] = s.l_run[tid];
     }
@@ -801,144 +911,90 @@ __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint3
         : "memory");
 }
 
-struct PageDesc {
-    const void *src0, *src1;
-    uint32_t b0, b1;
-    int instr;
-    bool weights;  // streamed once per step: evict first from L2
-};
-
-// Yields the pages of an SM's instruction list in consumption order.
-struct PageIter {
-    const Instr *list;
-    int n, i;
-    bool open;
-    Seg seg[3];
-    int nseg, si, pr;
-    int p0, c1;
-    size_t head_base;
-
-    __device__ void init(const Instr *l, int nn) {
-        list = l;
-        n = nn;
-        i = 0;
-        open = false;
-    }
-
-    __device__ bool next(const KParams &p, PageDesc &d) {
-        while (i < n) {
-            const Instr ins = list[i];
-            if (!open) {
-                if (ins.op == OP_ATTN) {
-                    int c0;
-                    attn_range(p, ins.r1, c0, c1);
-                    p0 = c0;
-                    head_base = (size_t(ins.layer) * p.nkv + ins.r0) * size_t(p.max_seq) * p.hd;
-                } else {
-                    nseg = mv_segments(p, ins, seg);
-                    si = 0;
-                    pr = 0;
-                }
-                open = true;
-            }
-            d.instr = i;
-            if (ins.op == OP_ATTN) {
-                if (p0 < c1) {
-                    const int nn = min(attn_pp(p), c1 - p0);
-                    const uint32_t b = uint32_t(nn) * p.hd * 2;
-                    d.src0 = p.k_cache + head_base + size_t(p0) * p.hd;
-                    d.src1 = p.v_cache + head_base + size_t(p0) * p.hd;
-                    d.b0 = d.b1 = b;
-                    d.weights = false;
-                    p0 += nn;
-                    return true;
-                }
-            } else {
-                const MvShape &mv = mv_of(p, ins.op);
-                while (si < nseg) {
-                    if (pr < seg[si].nrows) {
-                        const int nr = min(mv.rpp, seg[si].nrows - pr);
-                        d.src0 = seg[si].w + size_t(seg[si].row0 + pr) * mv.K;
-                        d.b0 = uint32_t(nr) * mv.K * 2;
-                        d.src1 = nullptr;
-                        d.b1 = 0;
-                        d.weights = true;
-                        pr += nr;
-                        return true;
-                    }
-                    ++si;
-                    pr = 0;
-                }
-            }
-            ++i;
-            open = false;
-        }
-        return false;
-    }
-};
-
+// The producer thread walks its SM's host-built page list (weight pages with
+// their addresses, attention items expanded from pos here), so that issuing a
+// page costs it only a few instructions: it shares its scheduler with consumer
+// warps and gets a small share of the issue slots.
 __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
-    const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
-    const int n = p.n_instr[blockIdx.x];
+    const PDesc *dl = p.pdesc + p.pdesc_off[blockIdx.x];
+    const int nd = p.pdesc_off[blockIdx.x + 1] - p.pdesc_off[blockIdx.x];
     uint64_t evict_first;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
-    PageIter ld, pf;
-    ld.init(list, n);
-    pf.init(list, n);
-    uint32_t ppage = 0, pfidx = 0;
-    bool pf_more = true;
+    uint32_t ppage = 0;
+    int pfi = 0;  // next list entry the L2 prefetch may touch
     int last_instr = -1;
-    PageDesc d, q;
-    while (ld.next(p, d)) {
-        const uint32_t slot = ppage % NPAGES;
-        if (ppage >= NPAGES) {
-            uint64_t *bar = &s.empty[slot];
-            const uint32_t par = ((ppage / NPAGES) - 1u) & 1u;
-            if (!mbar_test(bar, par)) {
-                while (pf_more && pfidx < ppage) {  // pages already in the ring need no prefetch
-                    pf_more = pf.next(p, q);
-                    ++pfidx;
-                }
-                const uint64_t t0 = gtimer();
-                bool ok = true;
-                for (uint32_t it = 1;; ++it) {
-                    if (mbar_test(bar, par)) break;
-                    if (pf_more && pfidx < ppage + p.l2_prefetch) {
-                        pf_more = pf.next(p, q);
-                        if (pf_more) {
-                            bulk_prefetch_l2(q.src0, q.b0);
-                            if (q.b1) bulk_prefetch_l2(q.src1, q.b1);
-                            ++pfidx;
-                        }
-                        continue;
-                    }
-                    // back off: a spinning producer would take issue slots from the
-                    // consumer warps that share its scheduler
-                    __nanosleep(p.producer_sleep_ns);
-                    if ((it & 15u) == 0) {
-                        if (s.abort) { ok = false; break; }
-                        if (gtimer() - t0 > p.timeout_ns) {
-                            raise_status(p, s, LL_ERR_DEP_TIMEOUT);
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                if (!ok) break;
+    bool ok = true;
+    const int PP = attn_pp(p);
+    const uint32_t l2_ahead = p.l2_prefetch;
+    for (int di = 0; di < nd && ok; di++) {
+        const PDesc e = dl[di];
+        int a_c0 = 0, a_c1 = 1, a_p0 = 0;
+        size_t head_base = 0;
+        if (e.kind == PD_ATTN) {
+            const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
+            attn_range(p, c, a_c0, a_c1);
+            a_p0 = a_c0;
+            head_base = (size_t(layer) * p.nkv + g) * size_t(p.max_seq) * p.hd;
+            if (a_c0 >= a_c1) continue;  // empty split: no pages
+        }
+        // weight entries are one page; attention entries one page per PP positions
+        while (ok) {
+            const void *src0, *src1 = nullptr;
+            uint32_t b0, b1 = 0;
+            if (e.kind == PD_ATTN) {
+                if (a_p0 >= a_c1) break;
+                const int n = min(PP, a_c1 - a_p0);
+                b0 = b1 = uint32_t(n) * p.hd * 2;
+                src0 = p.k_cache + head_base + size_t(a_p0) * p.hd;
+                src1 = p.v_cache + head_base + size_t(a_p0) * p.hd;
+                a_p0 += n;
+            } else {
+                src0 = reinterpret_cast<const void *>(e.src);
+                b0 = e.bytes;
             }
+            const uint32_t slot = ppage % NPAGES;
+            if (ppage >= NPAGES) {
+                uint64_t *bar = &s.empty[slot];
+                const uint32_t par = ((ppage / NPAGES) - 1u) & 1u;
+                if (!mbar_test(bar, par)) {
+                    if (pfi < di) pfi = di;  // from the page that is waiting for this slot
+                    const uint64_t t0 = gtimer();
+                    for (uint32_t it = 1;; ++it) {
+                        if (mbar_test(bar, par)) break;
+                        // while held up, pull the weight pages that come next into L2
+                        if (pfi < nd && uint32_t(pfi - di) < l2_ahead) {
+                            const PDesc f = dl[pfi++];
+                            if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
+                            continue;
+                        }
+                        __nanosleep(p.producer_sleep_ns);
+                        if ((it & 15u) == 0) {
+                            if (s.abort) { ok = false; break; }
+                            if (gtimer() - t0 > p.timeout_ns) {
+                                raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                }
+            }
+            uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
+            ptrace_put(p, ppage, 0);
+            s.slot_page[slot] = ppage;
+            mbar_expect_tx(&s.full[slot], b0 + b1);
+            if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
+            else bulk_load(dst, src0, b0, &s.full[slot]);
+            if (b1) bulk_load(dst + PAGE_BYTES / 2, src1, b1, &s.full[slot]);
+            if (int(e.instr) != last_instr) {
+                trace_put(p, e.instr, 4);
+                last_instr = e.instr;
+            }
+            trace_put(p, e.instr, 5);
+            ++ppage;
+            if (e.kind == PD_WEIGHTS) break;
         }
-        uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
-        ptrace_put(p, ppage, 0);
-        mbar_expect_tx(&s.full[slot], d.b0 + d.b1);
-        if (d.weights && p.evict_first) bulk_load_hint(dst, d.src0, d.b0, &s.full[slot], evict_first);
-        else bulk_load(dst, d.src0, d.b0, &s.full[slot]);
-        if (d.b1) bulk_load(dst + PAGE_BYTES / 2, d.src1, d.b1, &s.full[slot]);
-        if (d.instr != last_instr) {
-            trace_put(p, d.instr, 4);
-            last_instr = d.instr;
-        }
-        trace_put(p, d.instr, 5);
-        ++ppage;
     }
     // Never leave with copies in flight into this block's shared memory: wait for
     // the newest page of every slot (older ones completed before their slot was
@@ -974,10 +1030,9 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
             switch (mv.vpl * 16 + mv.rw) {
 #define LL_MV_CASE(V, R) \
     case V * 16 + R: ok = mv_instr<V, R>(p, s, pages, ins, i, cpage, best, best_idx); break;
-                LL_MV_CASE(1, 1) LL_MV_CASE(1, 2) LL_MV_CASE(1, 4) LL_MV_CASE(1, 8)
-                LL_MV_CASE(2, 1) LL_MV_CASE(2, 2) LL_MV_CASE(2, 4)
-                LL_MV_CASE(3, 1) LL_MV_CASE(3, 2)
-                LL_MV_CASE(4, 1) LL_MV_CASE(4, 2)
+                // the (vpl, rw) pairs mv_shape can choose (see mv_combo_ok)
+                LL_MV_CASE(1, 8) LL_MV_CASE(2, 8) LL_MV_CASE(3, 1) LL_MV_CASE(3, 2)
+                LL_MV_CASE(3, 4) LL_MV_CASE(4, 1) LL_MV_CASE(4, 2) LL_MV_CASE(4, 4)
 #undef LL_MV_CASE
                 default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
             }
@@ -1001,6 +1056,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
             s.pcnt[i] = 0;
+            s.slot_page[i] = 0xffffffffu;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.abort = 0;

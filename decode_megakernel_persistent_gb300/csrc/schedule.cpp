@@ -69,31 +69,105 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
     }
 }
 
-// Input-vector geometry for width K (see MvShape): among the splits of a row
-// into k-slices of 256*vpl elements (vpl <= 8), pick the one that keeps the most
-// consumer warps busy, rows per warp a power of two and vpl * rw <= 8 (register
-// budget), then the smallest vpl. Returns false if K admits none.
+// Input-vector geometry for width K (see MvShape). Teams: as many as keep each
+// lane's share of the input at or under 32 floats (a team holds a full copy of
+// the input). Within a team: among the splits of a row into k-slices of
+// 256*vpl elements (vpl <= 4), the one that keeps the most warps busy, then the
+// most rows per page (rows per warp a power of two, at most 8). Returns false
+// if K admits none.
+// (vpl, rw) pairs the megakernel is compiled for.
+static bool mv_combo_ok(int vpl, int rw) {
+    static const int ok[][2] = {{1, 8}, {2, 8}, {3, 1}, {3, 2}, {3, 4}, {4, 1}, {4, 2}, {4, 4}};
+    for (auto &c : ok)
+        if (c[0] == vpl && c[1] == rw) return true;
+    return false;
+}
+
 bool mv_shape(int K, MvShape &m) {
     if (K <= 0 || K % 256 != 0 || K > 16384) return false;
     const int rows_fit = PAGE_BYTES / (2 * K);
-    int best_active = 0;
+    if (rows_fit < 1) return false;
+    int teams = 1;
+    while (teams < 4 && K * teams * 2 <= 32 * 32 * NCW) teams *= 2;
+    const int W = NCW / teams;
+    int best_active = 0, best_rpp = 0;
     for (int vpl = 1; vpl <= MAX_VPL; vpl++) {
         if (K % (256 * vpl) != 0) continue;
         const int ws = K / (256 * vpl);
-        if (ws > NCW) continue;
-        int rg = std::min(NCW / ws, rows_fit);
+        if (ws > W) continue;
+        const int rg = std::min(W / ws, rows_fit);
         if (rg < 1) continue;
         int rw = 1;
-        while (rw * 2 * rg <= rows_fit && rw * 2 <= 8 && vpl * rw * 2 <= 8) rw *= 2;
+        while (rw * 2 * rg <= rows_fit && rw * 2 <= 8) rw *= 2;
         const int rpp = rg * rw;
-        if (rpp > MAX_RPP || rpp * ws > MAX_PART) continue;
+        if (rpp > MAX_RPP || rpp * ws > MAX_PART || !mv_combo_ok(vpl, rw)) continue;
         const int active = ws * rg;
-        if (active > best_active) {
+        if (active > best_active || (active == best_active && rpp > best_rpp)) {
             best_active = active;
-            m = MvShape{K, ws, vpl, rpp, rg, rw};
+            best_rpp = rpp;
+            m = MvShape{K, ws, vpl, rpp, rg, rw, teams};
         }
     }
     return best_active > 0;
+}
+
+// The producer lists: for every SM, the pages its consumers will take, in the
+// order they take them (the same segment and row-page walk as the consumers).
+void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector<LayerW> &layers,
+                 const uint16_t *lm_head, int H, int qd, int kd, int I, const MvShape &mh, const MvShape &mq,
+                 const MvShape &mi, std::vector<PDesc> &out, std::vector<int32_t> &off) {
+    out.clear();
+    off.assign(lists.size() + 1, 0);
+    auto pages = [&](const uint16_t *w, int row0, int nrows, const MvShape &mv, int instr) {
+        for (int pr = 0; pr < nrows; pr += mv.rpp) {
+            const int nr = std::min(mv.rpp, nrows - pr);
+            PDesc d{};
+            d.src = reinterpret_cast<unsigned long long>(w + size_t(row0 + pr) * mv.K);
+            d.bytes = uint32_t(nr) * uint32_t(mv.K) * 2u;
+            d.instr = static_cast<uint16_t>(instr);
+            d.kind = PD_WEIGHTS;
+            out.push_back(d);
+        }
+    };
+    for (size_t sm = 0; sm < lists.size(); sm++) {
+        off[sm] = static_cast<int32_t>(out.size());
+        for (size_t i = 0; i < lists[sm].size(); i++) {
+            const Instr &in = lists[sm][i];
+            const int r0 = in.r0, r1 = in.r1;
+            if (in.op == OP_ATTN) {
+                PDesc d{};
+                d.src = (static_cast<unsigned long long>(in.layer) << 32) | (static_cast<unsigned long long>(r0) << 16) |
+                        static_cast<unsigned long long>(r1);
+                d.instr = static_cast<uint16_t>(i);
+                d.kind = PD_ATTN;
+                out.push_back(d);
+                continue;
+            }
+            if (r0 >= r1) continue;
+            const LayerW *lw = in.op == OP_LMHEAD ? nullptr : &layers[in.layer];
+            switch (in.op) {
+                case OP_QKV: {
+                    const int b[4] = {0, qd, qd + kd, qd + 2 * kd};
+                    const uint16_t *m[3] = {lw->wq, lw->wk, lw->wv};
+                    for (int k = 0; k < 3; k++) {
+                        const int a = std::max(r0, b[k]), e = std::min(r1, b[k + 1]);
+                        if (a < e) pages(m[k], a - b[k], e - a, mh, int(i));
+                    }
+                    break;
+                }
+                case OP_OPROJ: pages(lw->wo, r0, r1 - r0, mq, int(i)); break;
+                case OP_GATEUP:
+                    pages(lw->wg, r0, r1 - r0, mh, int(i));
+                    pages(lw->wu, r0, r1 - r0, mh, int(i));
+                    break;
+                case OP_DOWN: pages(lw->wd, r0, r1 - r0, mi, int(i)); break;
+                default: pages(lm_head, r0, r1 - r0, mh, int(i)); break;
+            }
+        }
+    }
+    off[lists.size()] = static_cast<int32_t>(out.size());
+    (void)H;
+    (void)I;
 }
 
 }  // namespace ll
