@@ -144,6 +144,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     if (c.head_dim != 64 && c.head_dim != 128) return bad(LL_ERR_SHAPE, "head_dim must be 64 or 128");
     if (c.n_q_heads % c.n_kv_heads != 0 || c.n_q_heads / c.n_kv_heads > ll::MAX_GQA)
         return bad(LL_ERR_SHAPE, "n_q_heads must be a multiple (at most 8x) of n_kv_heads");
+    if ((c.n_q_heads / std::max(1, c.n_kv_heads)) * c.head_dim > 512)
+        return bad(LL_ERR_SHAPE, "(n_q_heads / n_kv_heads) * head_dim must be at most 512");
     if (int64_t(c.n_q_heads) * c.head_dim > ll::XIN_FLOATS)
         return bad(LL_ERR_SHAPE, "n_q_heads*head_dim must be at most 4096");
     if (c.backend != LL_BACKEND_MEGAKERNEL && c.backend != LL_BACKEND_CHAIN)

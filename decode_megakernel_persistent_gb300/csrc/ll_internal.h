@@ -28,6 +28,7 @@ constexpr int ACC_FLOATS = 2048;           // per-SM row results held until the 
 constexpr int XIN_FLOATS = 4096;           // largest O-projection input (n_q_heads * head_dim)
 constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden / SMs, rounded up)
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
+constexpr int ATT_WARPS = 8;               // warps that split an attention page's P.V
 constexpr int TRACE_WORDS = 12;            // timestamps per traced instruction
 constexpr int PTRACE_PAGES = 4096;         // pages per SM the page trace keeps (a ring)
 

@@ -161,11 +161,13 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 
 struct alignas(16) Smem {
     union {
-        float xin[XIN_FLOATS];  // O-projection input: the merged attention output
+        float xin[XIN_FLOATS];  // O-projection input: the merged attention output; also the
+                                // attention P.V partials of the P.V warps
+        float acc[ACC_FLOATS];  // the SM's row results of the current matrix-vector instruction
         struct {
-            float acc[ACC_FLOATS];  // the SM's row results of the current matrix-vector instruction
-            float qs[MAX_GQA][MAX_HD];
-            float sc[MAX_GQA][132];  // scores, then probabilities, of up to 129 positions
+            float ared_lo[ATT_WARPS * 4 * 64];  // P.V partials of four heads of 64 dims
+            float sc[MAX_GQA][132];             // attention scores of up to 129 positions
+            float pt[132][MAX_GQA];             // their probabilities, position-major
         };
     };
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
@@ -173,6 +175,7 @@ struct alignas(16) Smem {
     int32_t pcnt[NPAGES];    // warps done with the page in the slot
     volatile uint32_t slot_page[NPAGES];  // page number the producer last put in the slot
     float part[NPAGES][MAX_PART];  // per page: (row, k-slice) partial sums
+    float qr[MAX_GQA][MAX_HD];  // the attention item's rotated, scaled query heads
     alignas(16) uint16_t knew[MAX_HD];
     alignas(16) uint16_t vnew[MAX_HD];
     float m_run[MAX_GQA], l_run[MAX_GQA], alpha[MAX_GQA];
@@ -185,8 +188,8 @@ struct alignas(16) Smem {
     volatile int32_t abort;
 };
 
-static_assert(ACC_FLOATS + MAX_GQA * MAX_HD + MAX_GQA * 132 >= XIN_FLOATS, "xin overlaps acc, qs and sc");
-static_assert(offsetof(Smem, xin) % 16 == 0 && offsetof(Smem, qs) % 16 == 0, "alignment");
+static_assert(offsetof(Smem, xin) % 16 == 0 && offsetof(Smem, pt) % 16 == 0, "alignment");
+static_assert(ATT_WARPS * 4 * MAX_HD <= XIN_FLOATS, "P.V partials of four heads fit the O input space");
 
 constexpr int SMEM_BYTES = NPAGES * PAGE_BYTES + static_cast<int>(sizeof(Smem));
 
@@ -698,49 +701,68 @@ __device__ void lm_finish(const KParams &p, Smem &s, float best, int best_idx) {
 // goes to global memory, and the O projection merges the splits when it loads
 // its input, so no instruction waits for a separate merge.
 
-// Query layout in s.qs: head h, 16-byte chunk c of 8 dims; the two 4-float
-// halves of chunks 4..7 (mod 8) are stored swapped so that lanes reading the
-// same half of different chunks hit different banks.
-__device__ __forceinline__ int qs_index(int i) {
-    const int c = i >> 3, half = (i >> 2) & 1;
-    return (c << 3) + ((half ^ ((c >> 2) & 1)) << 2) + (i & 3);
+// DL consecutive bf16 from shared memory, widened.
+template <int DL>
+__device__ __forceinline__ void lds_bf16(uint32_t addr, float (&out)[DL]) {
+    if constexpr (DL == 2) {
+        uint32_t u;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u) : "r"(addr));
+        out[0] = bf_lo(u);
+        out[1] = bf_hi(u);
+    } else {
+        static_assert(DL == 4, "head_dim 64 or 128");
+        uint32_t u0, u1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(u0), "=r"(u1) : "r"(addr));
+        out[0] = bf_lo(u0);
+        out[1] = bf_hi(u0);
+        out[2] = bf_lo(u1);
+        out[3] = bf_hi(u1);
+    }
 }
 
-// Scores, online-softmax statistics and P.V over n cached positions of a page
-// (K, V: [n][hd] bf16 in shared memory), plus the new token as position n when
-// with_new is set. NCH = hd / 8.
-template <int NCH>
+// Attention over one page. Lane l of a warp owns dims [l*DL, l*DL + DL) of the
+// query heads, taken four at a time from the rotated queries in shared memory; a
+// position's K or V row is then one 128/256-byte conflict-free access per warp.
+// Scores: warp w takes positions w, w + NCW, ... and reduces its per-head partial
+// dots across lanes. Softmax statistics: warp h for head h. P.V: ATT_WARPS warps
+// split the positions, each reading a position's probabilities with one
+// broadcast load, and their partial sums are added through shared memory by one
+// thread per (head, dim).
+template <int DL>
 __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const uint16_t *Vv, int n,
-                           bool with_new, float (&oacc)[2], int G, int ii) {
-    constexpr int hd = NCH * 8;
+                           bool with_new, float &oacc, int G, int ii) {
+    constexpr int hd = DL * 32, GP = 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = n + (with_new ? 1 : 0);
-    // scores: thread per (head, position), head-major so a warp shares its query;
-    // 16-byte chunks visited in an order rotated by position (spreads K over banks)
-    const uint32_t kbase = K ? smem_addr(K) : 0u, knew = smem_addr(s.knew);
-    for (int t = tid; t < nt * G; t += NCT) {
-        const int h = t / nt, j = t - h * nt;
-        if (!LL_OK_IDX(14, j, 132) || !LL_OK_IDX(15, h, MAX_GQA)) continue;
-        const uint32_t krow = j < n ? kbase + uint32_t(j) * (hd * 2) : knew;
-        const uint32_t qh = smem_addr(&s.qs[h][0]);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < NCH; i++) {
-            const int c = (i + j) & (NCH - 1);
-            const uint4 u = lds128(krow + c * 16);
-            const int sw = ((c >> 2) & 1) << 2;
-            const float4 qa = lds_f4(qh + ((c << 3) + sw) * 4);
-            const float4 qb = lds_f4(qh + ((c << 3) + (4 - sw)) * 4);
-            a0 = fmaf(qa.x, bf_lo(u.x), a0); a1 = fmaf(qa.y, bf_hi(u.x), a1);
-            a2 = fmaf(qa.z, bf_lo(u.y), a2); a3 = fmaf(qa.w, bf_hi(u.y), a3);
-            a0 = fmaf(qb.x, bf_lo(u.z), a0); a1 = fmaf(qb.y, bf_hi(u.z), a1);
-            a2 = fmaf(qb.z, bf_lo(u.w), a2); a3 = fmaf(qb.w, bf_hi(u.w), a3);
+    const uint32_t kbase = K ? smem_addr(K) : 0u, vbase = Vv ? smem_addr(Vv) : 0u;
+    const uint32_t knew = smem_addr(s.knew), vnew = smem_addr(s.vnew);
+    // scores
+    for (int h0 = 0; h0 < G; h0 += GP) {
+        float q[GP][DL];
+#pragma unroll
+        for (int h = 0; h < GP; h++)
+#pragma unroll
+            for (int e = 0; e < DL; e++) q[h][e] = h0 + h < G ? s.qr[h0 + h][lane * DL + e] : 0.f;
+        for (int j = warp; j < nt; j += NCW) {
+            const uint32_t kr = (j < n ? kbase + uint32_t(j) * (hd * 2) : knew) + lane * (DL * 2);
+            float k[DL];
+            lds_bf16<DL>(kr, k);
+            float v[GP];
+#pragma unroll
+            for (int h = 0; h < GP; h++) {
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < DL; e++) a = fmaf(q[h][e], k[e], a);
+                v[h] = a;
+            }
+            const float sum = transpose_reduce<GP>(v);
+            const int h = h0 + lane / (32 / GP);
+            if ((lane % (32 / GP)) == 0 && h < G && LL_OK_IDX(14, j, 132)) s.sc[h][j] = sum;
         }
-        s.sc[h][j] = (a0 + a1) + (a2 + a3);
     }
     consumer_sync();
     if (tid == 0) trace_put(p, ii, 8);
-    // online softmax statistics: warp h handles head h
+    // online softmax statistics: warp h handles head h; probabilities go out position-major
     if (warp < G) {
         const int h = warp;
         float mx = -INFINITY;
@@ -751,7 +773,7 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
         float sum = 0.f;
         for (int j = lane; j < nt; j += 32) {
             const float e = expf(s.sc[h][j] - m_new);
-            s.sc[h][j] = e;
+            s.pt[j][h] = e;
             sum += e;
         }
         sum = warp_sum(sum);
@@ -764,50 +786,66 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
     }
     consumer_sync();
     if (tid == 0) trace_put(p, ii, 9);
-    // P.V: T threads per (head, dim) pair split the positions (position j goes to
-    // part j % T); partial sums stay per thread across pages and are combined
-    // once at the end of the item
-    const int P = G * hd, T = p.attn_T;
+    // P.V partial sums of ATT_WARPS warps, four heads at a time. The partials of a
+    // group use ATT_WARPS*4*hd floats from the start of the union: with 64-dim heads
+    // that ends below sc/pt (up to eight heads, two groups); with 128-dim heads
+    // (at most four, one group) it overlaps them, read by then.
+    float *ared = s.xin;
+    for (int h0 = 0; h0 < G; h0 += GP) {
+        float o[GP][DL];
 #pragma unroll
-    for (int k = 0; k < 2; k++) {
-        const int slot = tid + k * NCT;
-        const int pi = slot / T, part = slot % T;
-        if ((T > 1 && k > 0) || pi >= P) continue;
-        const int h = pi / hd, d = pi - h * hd;
-        const uint32_t ph = smem_addr(&s.sc[h][0]);
-        const uint32_t vc = (Vv ? smem_addr(Vv) : 0u) + uint32_t(d) * 2;
-        float a0 = oacc[k] * s.alpha[h], a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int j = part;
-        for (; j + 3 * T < n; j += 4 * T) {
-            a0 = fmaf(lds_f32(ph + j * 4), bf16_to_f(lds_u16(vc + uint32_t(j) * (hd * 2))), a0);
-            a1 = fmaf(lds_f32(ph + (j + T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + T) * (hd * 2))), a1);
-            a2 = fmaf(lds_f32(ph + (j + 2 * T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + 2 * T) * (hd * 2))), a2);
-            a3 = fmaf(lds_f32(ph + (j + 3 * T) * 4), bf16_to_f(lds_u16(vc + uint32_t(j + 3 * T) * (hd * 2))), a3);
+        for (int h = 0; h < GP; h++)
+#pragma unroll
+            for (int e = 0; e < DL; e++) o[h][e] = 0.f;
+        if (warp < ATT_WARPS) {
+            for (int j = warp; j < nt; j += ATT_WARPS) {
+                const uint32_t vr = (j < n ? vbase + uint32_t(j) * (hd * 2) : vnew) + lane * (DL * 2);
+                float v[DL];
+                lds_bf16<DL>(vr, v);
+                const float4 t4 = lds_f4(smem_addr(&s.pt[j][h0]));
+                const float pj[GP] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int h = 0; h < GP; h++)
+#pragma unroll
+                    for (int e = 0; e < DL; e++) o[h][e] = fmaf(pj[h], v[e], o[h][e]);
+            }
         }
-        for (; j < n; j += T) a0 = fmaf(lds_f32(ph + j * 4), bf16_to_f(lds_u16(vc + uint32_t(j) * (hd * 2))), a0);
-        if (with_new && n % T == part) a0 = fmaf(lds_f32(ph + n * 4), bf16_to_f(s.vnew[d]), a0);
-        oacc[k] = (a0 + a1) + (a2 + a3);
+        consumer_sync();  // s.pt read (128-dim heads) and the previous group's partials summed
+        if (warp < ATT_WARPS) {
+#pragma unroll
+            for (int h = 0; h < GP; h++)
+                if (h0 + h < G)
+#pragma unroll
+                    for (int e = 0; e < DL; e++) ared[(warp * GP + h) * hd + lane * DL + e] = o[h][e];
+        }
+        consumer_sync();
+        const int t = tid - h0 * hd;
+        if (t >= 0 && t < GP * hd && tid < G * hd) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; w++) a += ared[w * GP * hd + t];
+            oacc = oacc * s.alpha[h0 + t / hd] + a;
+        }
     }
-    consumer_sync();
     if (tid == 0) trace_put(p, ii, 10);
 }
 
-__device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
-    if (!dep_wait(p, s, ins)) return false;
+template <int DL>
+__device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
-    const int hd = p.hd, half = hd / 2, G = p.nq / p.nkv, tid = threadIdx.x;
-    const int qd = p.nq * p.hd, kd = p.nkv * p.hd;
+    constexpr int hd = DL * 32, half = hd / 2;
+    const int G = p.nq / p.nkv, tid = threadIdx.x;
+    const int qd = p.nq * hd, kd = p.nkv * hd;
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     const float2 *cs = p.rope_cs + size_t(p.pos) * half;
-    // RoPE ("rotate half") on the group's queries and on the new key
-    for (int t = tid; t < G * half; t += NCT) {
-        const int h = t / half, i = t % half;
-        const float *q = p.qkv + size_t(g * G + h) * hd;
-        const float a = __ldcg(q + i), b = __ldcg(q + i + half);
+    // the group's query heads with RoPE ("rotate half") applied, pre-scaled by 1/sqrt(hd)
+    if (tid < G * hd) {
+        const int h = tid / hd, d = tid % hd, i = d < half ? d : d - half;
+        const float *qh = p.qkv + size_t(g * G + h) * hd;
+        const float a = __ldcg(qh + i), b = __ldcg(qh + i + half);
         const float2 r = cs[i];
-        s.qs[h][qs_index(i)] = (a * r.x - b * r.y) * scale;
-        s.qs[h][qs_index(i + half)] = (a * r.y + b * r.x) * scale;
+        s.qr[h][d] = (d < half ? a * r.x - b * r.y : a * r.y + b * r.x) * scale;
     }
     if (owner) {
         for (int i = tid; i < half; i += NCT) {
@@ -828,12 +866,12 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
     if (owner) {
         const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
         if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
-        for (int d = tid; d < hd; d += NCT) {
-            p.k_cache[at + d] = s.knew[d];
-            p.v_cache[at + d] = s.vnew[d];
-        }
+            for (int d = tid; d < hd; d += NCT) {
+                p.k_cache[at + d] = s.knew[d];
+                p.v_cache[at + d] = s.vnew[d];
+            }
     }
-    float oacc[2] = {0.f, 0.f};
+    float oacc = 0.f;
     int c0, c1;
     attn_range(p, c, c0, c1);
     const int PP = attn_pp(p);
@@ -847,39 +885,21 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
             trace_put(p, ii, 6);
         }
         const uint16_t *pg = reinterpret_cast<const uint16_t *>(pages + size_t(slot) * PAGE_BYTES);
-        if (hd == 64) attn_block<8>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);  // V at half a page
-        else attn_block<16>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);
+        attn_block<DL>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);  // V at half a page
         if (tid == 0) {
             ptrace_put(p, cpage, 2);
             mbar_arrive(&s.empty[slot]);
         }
         ++cpage;
     }
-    if (owner && c0 == c1) {
-        if (hd == 64) attn_block<8>(p, s, nullptr, nullptr, 0, true, oacc, G, ii);
-        else attn_block<16>(p, s, nullptr, nullptr, 0, true, oacc, G, ii);
-    }
+    if (owner && c0 == c1) attn_block<DL>(p, s, nullptr, nullptr, 0, true, oacc, G, ii);
     if (tid == 0) trace_put(p, ii, 7);
 
     // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}]
-    const int stride = hd + 4, P = G * hd, T = p.attn_T;
-    if (T > 1) {
-        float a = oacc[0];
-        for (int off = T / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        const int pi = tid / T;
-        if (tid % T == 0 && pi < P) {
-            const int h = pi / hd, d = pi % hd;
-            p.part[(size_t(g * G + h) * S + c) * stride + d] = a;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 2; k++) {
-            const int pi = tid + k * NCT;
-            if (pi < P) {
-                const int h = pi / hd, d = pi % hd;
-                p.part[(size_t(g * G + h) * S + c) * stride + d] = oacc[k];
-            }
-        }
+    const int stride = hd + 4;
+    if (tid < G * hd) {
+        const int h = tid / hd, d = tid % hd;
+        p.part[(size_t(g * G + h) * S + c) * stride + d] = oacc;
     }
     if (tid < G && LL_OK_IDX(17, (size_t(g * G + tid) * S + c) * stride + hd + 1, size_t(p.nq) * S * stride)) {
         p.part[(size_t(g * G + tid) * S + c) * stride + hd] = s.m_run[tid];
@@ -889,6 +909,11 @@ __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Inst
     signal_done(p, ins);
     if (tid == 0) trace_put(p, ii, 11);
     return true;
+}
+
+__device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
+    if (!dep_wait(p, s, ins)) return false;
+    return p.hd == 64 ? attn_item<2>(p, s, pages, ins, ii, cpage) : attn_item<4>(p, s, pages, ins, ii, cpage);
 }
 
 // ---------------------------------------------------------------------------------

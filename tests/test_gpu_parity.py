@@ -58,6 +58,28 @@ def test_tiny_last_position_and_ragged_splits(backend):
         pr.close()
 
 
+# Head layouts beyond the Llama shapes: eight query heads per KV head, plain
+# multi-head attention, and four 128-dim query heads per KV head.
+GQA_SHAPES = [
+    synth.ModelShape("gqa8-hd64", 2, 512, 8, 1, 64, 1024, 4096, True),
+    synth.ModelShape("mha-hd64", 2, 512, 4, 4, 64, 1024, 4096, False),
+    synth.ModelShape("gqa4-hd128", 2, 512, 8, 2, 128, 1536, 4096, True),
+]
+
+
+@pytest.mark.parametrize("shape", GQA_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_head_layouts(shape, backend):
+    # positions on both sides of a 128-position split and of a page boundary
+    max_seq = 300
+    pr = Pair(shape, max_seq, backend, kv_fill=260, gain_jitter=0.25)
+    tok = 11
+    for pos in (260, 261):
+        _, tok, _ = pr.step(tok, pos, what=f"{shape.name} pos {pos}")
+    pr.kv_close(slice(260, 262))
+    pr.close()
+
+
 def _full_size(key, backend, steps=2):
     wl = synth.WORKLOADS[key]
     shape, ctx = wl.shape, wl.context
