@@ -1,6 +1,6 @@
 """Build libll.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Four translation units are compiled in parallel and linked into
+Five translation units are compiled in parallel and linked into
 ``decode_megakernel_persistent_gb300/libll.so`` with the CUDA runtime linked
 statically, so the library needs nothing but the driver at run time.
 """
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libll.so")
-SOURCES = ("megakernel.cu", "chain.cu", "schedule.cpp", "api.cpp")
+SOURCES = ("megakernel.cu", "chain.cu", "schedule.cpp", "api.cpp", "static_step.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -31,6 +31,9 @@ LL_Q_LAUNCHES_PER_STEP = 6
 LL_Q_SMEM_BYTES = 7
 LL_Q_TRACE_BYTES = 8
 
+LL_STATIC_SCRATCH_BYTES = 4194304
+LL_STATIC_MAX_LAYERS = 256
+
 LL_FAULT_NONE = 0
 LL_FAULT_DROP_SIGNAL = 1
 
@@ -40,7 +43,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
 EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_synchronize",
            "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
-           "ll_free")
+           "ll_free", "ll_decode_step_static")
 
 
 class LLError(RuntimeError):
@@ -103,6 +106,9 @@ def lib() -> ctypes.CDLL:
     L.ll_last_error.restype = ctypes.c_char_p
     L.ll_free.argtypes = [vp]
     L.ll_free.restype = None
+    L.ll_decode_step_static.argtypes = [ctypes.POINTER(ll_config), ctypes.POINTER(ll_weights), vp, vp, i32, i32,
+                                        vp, ctypes.POINTER(i32), vp, ctypes.c_char_p, ctypes.c_size_t]
+    L.ll_decode_step_static.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -129,12 +135,8 @@ def make_config(shape, max_seq: int, backend: int = LL_BACKEND_MEGAKERNEL) -> ll
     return c
 
 
-def ll_init(cfg: ll_config, weights: dict, k_cache, v_cache, stream=None):
-    """Create a handle. ``weights`` maps names to CUDA bf16 tensors (per-layer names
-    to lists); ``stream`` is a torch.cuda.Stream or None for torch's current stream."""
-    import torch
-    if stream is None:
-        stream = torch.cuda.current_stream()
+def _weights_struct(weights: dict):
+    """ll_weights for a dict of CUDA bf16 tensors, plus the host arrays it points into."""
     w = ll_weights()
     w.embed = _ptr(weights["embed"])
     w.final_norm = _ptr(weights["final_norm"])
@@ -144,6 +146,16 @@ def ll_init(cfg: ll_config, weights: dict, k_cache, v_cache, stream=None):
         arr = (ctypes.c_void_p * max(1, len(weights[k])))(*[_ptr(t) for t in weights[k]])
         keep.append(arr)
         setattr(w, k, ctypes.cast(arr, _PP16))
+    return w, keep
+
+
+def ll_init(cfg: ll_config, weights: dict, k_cache, v_cache, stream=None):
+    """Create a handle. ``weights`` maps names to CUDA bf16 tensors (per-layer names
+    to lists); ``stream`` is a torch.cuda.Stream or None for torch's current stream."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    w, keep = _weights_struct(weights)
     h = ctypes.c_void_p()
     rc = lib().ll_init(ctypes.byref(cfg), ctypes.byref(w), _ptr(k_cache), _ptr(v_cache),
                        ctypes.c_void_p(stream.cuda_stream), ctypes.byref(h))
@@ -200,6 +212,25 @@ def ll_plan(cfg: ll_config, nsm: int):
     if rc != LL_OK:
         raise LLError(rc, "ll_plan failed")
     return out
+
+
+def ll_decode_step_static(cfg: ll_config, weights: dict, k_cache, v_cache, token: int, pos: int,
+                          logits=None, stream=None) -> int:
+    """One decode step without a handle and without device allocation; returns the
+    greedy next token. ``stream`` is a torch.cuda.Stream or None for torch's current one."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    w, keep = _weights_struct(weights)
+    nxt = ctypes.c_int32(-1)
+    err = ctypes.create_string_buffer(256)
+    rc = lib().ll_decode_step_static(ctypes.byref(cfg), ctypes.byref(w), _ptr(k_cache), _ptr(v_cache), int(token),
+                                     int(pos), _ptr(logits), ctypes.byref(nxt), ctypes.c_void_p(stream.cuda_stream),
+                                     err, len(err))
+    del keep
+    if rc != LL_OK:
+        raise LLError(rc, err.value.decode())
+    return int(nxt.value)
 
 
 def ll_last_error(h) -> str:

@@ -181,6 +181,36 @@ const char *ll_last_error(const ll_handle *h);
 /* Release library memory (not the caller's weights, caches or buffers). NULL is a no-op. */
 void ll_free(ll_handle *h);
 
+/* One decode step that allocates no device memory, for callers that cannot
+ * call cudaMalloc. The pages define no such call (they have no counterpart to
+ * it): it is the one-kernel-per-operation path of LL_BACKEND_CHAIN with all of
+ * its scratch (activations, attention partials, the RoPE row of pos, the status
+ * word and the next token) in one file-scope device array of
+ * LL_STATIC_SCRATCH_BYTES bytes per device, shared by every call.
+ *   cfg, w: as for ll_init (cfg->backend is ignored); the per-layer host arrays
+ *     are read during the call only. n_layers is at most LL_STATIC_MAX_LAYERS.
+ *   k_cache, v_cache, token, pos, logits_dev, next_token_host: as for
+ *     ll_decode_step; logits_dev may be NULL (the logits then use the array).
+ *   stream: cudaStream_t (as void*) the work is enqueued on; the call waits for
+ *     it before returning.
+ *   err, err_len: optional caller buffer that receives a one-line reason on
+ *     failure (truncated to err_len bytes, NUL-terminated); NULL for none.
+ * Returns LL_OK or LL_ERR_ARG / LL_ERR_SHAPE / LL_ERR_CUDA / LL_ERR_DEVICE. A
+ * shape whose scratch would exceed LL_STATIC_SCRATCH_BYTES is rejected with
+ * LL_ERR_SHAPE and a message giving the bytes it needs; nothing is launched.
+ * The first call on a device (the device current at the call) sets up that
+ * device: it looks up the array's device address (cudaGetSymbolAddress) and
+ * the SM count. Make that first call before any stream capture. The call
+ * itself calls no cudaMalloc, cudaFree or other allocating routine; it clears
+ * the status word at the start of every step (everything else is written
+ * before it is read). Calls whose GPU work overlaps in time, on any streams or
+ * threads, race on the shared array: serialise them. */
+#define LL_STATIC_SCRATCH_BYTES 4194304
+#define LL_STATIC_MAX_LAYERS 256
+int ll_decode_step_static(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16_t *v_cache,
+                          int32_t token, int32_t pos, float *logits_dev, int32_t *next_token_host, void *stream,
+                          char *err, size_t err_len);
+
 #ifdef __cplusplus
 }
 #endif
