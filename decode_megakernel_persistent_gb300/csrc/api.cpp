@@ -33,6 +33,8 @@ struct ll_handle {
     int max_instr = 0;
     uint32_t epoch = 0;
     int32_t *pinned = nullptr;  // [0] next token, [1] status
+    uint8_t *tagged = nullptr;  // the megakernel's tagged activation words (cleared on reset)
+    size_t tagged_bytes = 0;
     std::string err;
 };
 
@@ -79,10 +81,13 @@ void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::v
 
 void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists); }
 
-// Clear counters and the status word after a failed step so the next starts clean.
+// Clear counters, tagged activation words and the status word after a failed
+// step so the next starts clean (the step count restarts, so no stale tag may
+// survive).
 int reset_device_state(ll_handle *h) {
     const size_t nctr = size_t(ll::CtrLayout::count(h->cfg.n_layers, h->cfg.n_kv_heads)) * ll::CTR_STRIDE;
     if (cudaMemsetAsync(h->kp.ctr, 0, nctr * sizeof(uint32_t), h->stream) != cudaSuccess ||
+        cudaMemsetAsync(h->tagged, 0, h->tagged_bytes, h->stream) != cudaSuccess ||
         cudaMemsetAsync(h->kp.status, 0, sizeof(int32_t), h->stream) != cudaSuccess ||
         cudaStreamSynchronize(h->stream) != cudaSuccess)
         return LL_ERR_CUDA;
@@ -224,6 +229,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     uint32_t *ctr = nullptr;
     int32_t *status = nullptr, *tok = nullptr;
     long long *dbg = nullptr;
+    uint64_t *t_qkv = nullptr, *t_part = nullptr, *t_o = nullptr, *t_xmid = nullptr, *t_act = nullptr,
+             *t_xout = nullptr;
     const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 4);
     Piece pieces[] = {
         {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
@@ -246,6 +253,13 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&status), 4},
         {reinterpret_cast<void **>(&tok), 4},
         {reinterpret_cast<void **>(&dbg), 64},
+        // the megakernel's tagged activations (one contiguous run, cleared together)
+        {reinterpret_cast<void **>(&t_qkv), size_t(qd + 2 * kd) * 8},
+        {reinterpret_cast<void **>(&t_part), part_floats * 8},
+        {reinterpret_cast<void **>(&t_o), size_t(qd) * 8},
+        {reinterpret_cast<void **>(&t_xmid), size_t(c.hidden) * 8},
+        {reinterpret_cast<void **>(&t_act), size_t(c.inter) * 8},
+        {reinterpret_cast<void **>(&t_xout), size_t(c.hidden) * 8},
     };
     size_t total = 0;
     for (auto &pc : pieces) total += round_up(pc.bytes, 256);
@@ -301,20 +315,18 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.max_seq = c.max_seq;
     p.eps = c.rms_eps;
     p.attn_splits = h->splits;
-    {
-        const int P = (c.n_q_heads / c.n_kv_heads) * c.head_dim;
-        int T = 1;
-        while (T * 2 * P <= ll::NCT && T < 32) T *= 2;
-        p.attn_T = T;
-    }
     p.mv_h = mh;
     p.mv_q = mq;
     p.mv_i = mi;
-    p.x = x;
-    p.qkv = qkv;
-    p.part = part;
-    p.o = o;
-    p.act = act;
+    p.t_qkv = t_qkv;
+    p.t_part = t_part;
+    p.t_o = t_o;
+    p.t_xmid = t_xmid;
+    p.t_act = t_act;
+    p.t_xout = t_xout;
+    h->tagged = reinterpret_cast<uint8_t *>(t_qkv);
+    h->tagged_bytes = static_cast<size_t>(reinterpret_cast<uint8_t *>(t_xout) + round_up(size_t(c.hidden) * 8, 256) -
+                                          reinterpret_cast<uint8_t *>(t_qkv));
     p.lm_keys = keys;
     p.ctr = ctr;
     p.status = status;
@@ -329,6 +341,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.evict_first = 1;
     if (const char *e = std::getenv("LL_L2_PREFETCH_PAGES")) p.l2_prefetch = static_cast<uint32_t>(std::atoi(e));
     if (const char *e = std::getenv("LL_EVICT_FIRST")) p.evict_first = static_cast<uint32_t>(std::atoi(e));
+    p.max_inflight = ll::NPAGES;
+    if (const char *e = std::getenv("LL_MAX_INFLIGHT")) p.max_inflight = static_cast<uint32_t>(std::atoi(e));
     p.producer_sleep_ns = 64;
     if (const char *e = std::getenv("LL_PRODUCER_SLEEP_NS")) p.producer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
     h->d_instrs = d_instrs;
@@ -354,7 +368,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
                   cudaSuccess &&
               cudaMemcpy(d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemset(ctr, 0, nctr * 4) == cudaSuccess && cudaMemset(status, 0, 4) == cudaSuccess &&
-              cudaMemset(tok, 0, 4) == cudaSuccess && cudaMemset(dbg, 0, 64) == cudaSuccess;
+              cudaMemset(tok, 0, 4) == cudaSuccess && cudaMemset(dbg, 0, 64) == cudaSuccess &&
+              cudaMemset(h->tagged, 0, h->tagged_bytes) == cudaSuccess;
     if (!ok || upload_schedule(h) != LL_OK) {
         ll_free(h);
         return bad(LL_ERR_CUDA, "initial upload failed");

@@ -105,13 +105,16 @@ struct KParams {
     float eps;
     int32_t attn_splits;
     MvShape mv_h, mv_q, mv_i; // input widths hidden, n_q*hd, inter
-    // scratch (fp32 unless noted)
-    float *x;                 // [H] residual stream
-    float *qkv;               // [nq*hd + 2*nkv*hd]
-    float *part;              // [nq][splits][hd + 4]: o (unnormalised), m, l
-    int32_t attn_T;           // threads per (head, dim) pair in attention P.V
-    float *o;                 // [nq*hd]
-    float *act;               // [I]
+    // Activations between instructions, as tagged words: (tag << 32) | fp32 bits,
+    // stored and loaded as single 8-byte accesses. A reader takes a word only
+    // when its tag is the one of the current step and layer (tag_of), so the
+    // data itself tells the reader it is ready.
+    uint64_t *t_qkv;          // [nq*hd + 2*nkv*hd] QKV projection (before RoPE)
+    uint64_t *t_part;         // [nq][splits][hd + 4] attention partials: o (unnormalised), m, l
+    uint64_t *t_o;            // [nq*hd] attention output, the splits merged
+    uint64_t *t_xmid;         // [H] residual stream after the O projection
+    uint64_t *t_act;          // [I] silu(gate) * up
+    uint64_t *t_xout;         // [H] residual stream after the down projection
     unsigned long long *lm_keys; // [nsm]
     uint32_t *ctr;            // counters, CTR_STRIDE apart
     int32_t *status;          // sticky status word
@@ -120,13 +123,14 @@ struct KParams {
     int32_t token;            // used when token_dev is null
     const int32_t *token_dev;
     int32_t pos;
-    uint32_t epoch;           // 1-based step count since the last counter reset
+    uint32_t epoch;           // 1-based step count since the last reset of counters and tagged words
     float *logits;            // [V] or null
     int32_t *next_token_dev;  // or null
     unsigned long long timeout_ns;
     uint32_t l2_prefetch;     // pages the producer may prefetch into L2 beyond its ring
     uint32_t evict_first;     // weight pages loaded with an L2 evict-first hint
     uint32_t producer_sleep_ns; // back-off of the producer while the ring is full
+    uint32_t max_inflight;    // pages issued but not yet landed, at most (NPAGES: only the ring bounds it)
     // optional globaltimer trace, [nsm][max_instr][TRACE_WORDS]: consumer begin,
     // dependency met + input loaded, pages done, end; producer first and last issue;
     // first page in hand, compute on the pages done; for attention also the end

@@ -10,16 +10,21 @@
 //     producer warp fills them with the bytes the next instructions will read,
 //     so loads for later instructions start while earlier ones still wait
 //     (paragraph on paging);
-//   * counters: instead of kernel boundaries, each finished instruction bumps a
-//     global-memory integer and a dependent instruction waits until that
-//     integer reaches its target (paragraph on the counter system).
+//   * dependencies in global memory instead of kernel boundaries (paragraph on
+//     the counter system). The page counts finished instructions in integers;
+//     here the data carries its own readiness: every activation an instruction
+//     hands to another SM is stored as one 8-byte word holding the fp32 value
+//     and a tag (step, layer), and the reader polls the words it needs until
+//     their tags are current. Nothing is fenced or counted per instruction, and
+//     the reader's wait and its input load are the same reads.
 //
 // GB300 choices (not from the page): pages are filled with one-dimensional
 // bulk async copies (cp.async.bulk) completing on mbarriers; matrix-vector
 // products run on CUDA cores with the input vector held in registers; the
-// split-KV attention merge is done by the last split to finish (an atomic
-// ticket), so no instruction waits for it; the greedy argmax is reduced the
-// same way. Every wait is bounded by a time limit.
+// split-KV attention partials are merged by the attention SMs of each KV head
+// between them, so the O projection reads one merged vector; the greedy argmax
+// is reduced by the last SM to finish (an atomic ticket). Every wait is bounded
+// by a time limit.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -88,8 +93,41 @@ __device__ __forceinline__ int32_t ld_relaxed(const int32_t *p) {
     return v;
 }
 
+// Tagged activation words: (tag << 32) | fp32 bits, one 8-byte access each, so a
+// reader that sees the tag also sees the value stored with it.
+__device__ __forceinline__ void st_tag(uint64_t *p, float v, uint32_t tag) {
+    const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tag(const uint64_t *p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+__device__ __forceinline__ void ld_tag2(const uint64_t *p, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+__device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return static_cast<uint32_t>(w >> 32) == tag; }
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
+}
+
+// Consumer barrier that also returns, to every consumer thread alike, whether
+// any of them passed true: failures leave an instruction together, so no
+// thread is left waiting at a later barrier for threads that have gone.
+__device__ __forceinline__ bool consumer_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(NCT)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -231,25 +269,6 @@ __device__ __forceinline__ void ptrace_put(const KParams &p, uint32_t page, int 
     if (p.ptrace) p.ptrace[(size_t(blockIdx.x) * PTRACE_PAGES + page % PTRACE_PAGES) * 3 + k] = gtimer();
 }
 
-__device__ bool wait_counter(const KParams &p, Smem &s, const uint32_t *ctr, uint32_t target) {
-    if (static_cast<int32_t>(ld_acquire(ctr) - target) >= 0) return true;
-    const uint64_t t0 = gtimer();
-    for (uint32_t it = 1;; ++it) {
-        if (static_cast<int32_t>(ld_acquire(ctr) - target) >= 0) return true;
-        if ((it & 31u) == 0) {
-            if (s.abort) return false;
-            if (ld_relaxed(p.status) != 0) {
-                s.abort = 1;
-                return false;
-            }
-            if (gtimer() - t0 > p.timeout_ns) {
-                raise_status(p, s, LL_ERR_DEP_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 __device__ bool wait_mbar(const KParams &p, Smem &s, uint64_t *bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = gtimer();
@@ -286,22 +305,69 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
     return wait_mbar(p, s, &s.full[slot], (page / NPAGES) & 1u);
 }
 
-// Consumer-side dependency wait: thread 0 polls, everyone learns the outcome.
-__device__ bool dep_wait(const KParams &p, Smem &s, const Instr &ins) {
-    if (ins.wait_ctr >= 0 && threadIdx.x == 0) {
-        wait_counter(p, s, p.ctr + size_t(ins.wait_ctr) * CTR_STRIDE, p.epoch * ins.wait_count);
-    }
-    consumer_sync();
-    return !s.abort;
+// Tag of the words an instruction of `layer` writes in the current step (never 0
+// for a live step, so cleared memory never passes).
+__device__ __forceinline__ uint32_t tag_of(const KParams &p, int layer) {
+    return p.epoch * static_cast<uint32_t>(p.L + 1) + static_cast<uint32_t>(layer) + 1u;
 }
 
-__device__ void signal_done(const KParams &p, const Instr &ins) {
-    consumer_sync();
-    if (threadIdx.x == 0 && ins.sig_ctr >= 0) {
-        __threadfence();
-        atomicAdd(p.ctr + size_t(ins.sig_ctr) * CTR_STRIDE, 1u);
+// The tag an instruction writes: its layer's, or 0 when its completion has been
+// removed from the schedule (fault injection), so that its readers time out.
+__device__ __forceinline__ uint32_t write_tag(const KParams &p, const Instr &ins) {
+    return ins.sig_ctr >= 0 ? tag_of(p, ins.layer) : 0u;
+}
+
+// Bounded polling of tagged words: called after a round of loads found a stale
+// tag (it > 0; round 0 only starts the clock). Returns true once the thread
+// should give up: another thread or block failed (s.abort, the status word), or
+// the time limit passed (then it records LL_ERR_DEP_TIMEOUT). The caller's
+// threads learn of it through consumer_any(s.abort).
+__device__ __forceinline__ bool poll_give_up(const KParams &p, Smem &s, uint32_t it, uint64_t &t0) {
+    if (it == 0) {
+        t0 = gtimer();
+        return false;
+    }
+    if (s.abort) return true;
+    if ((it & 7u) == 0) {
+        if (ld_relaxed(p.status) != 0) {
+            s.abort = 1;
+            return true;
+        }
+        if (gtimer() - t0 > p.timeout_ns) {
+            raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+            return true;
+        }
+    }
+    return false;
+}
+
+// Load N tagged words with `load(w)` (which fills every entry; entries it does
+// not need it sets to a word with the expected tag; word i sits at addr(i))
+// until all carry `tag`. While one is stale the thread re-reads that word alone,
+// so a block waiting on a wide input puts one load per thread on L2 per round,
+// not the whole input.
+template <int N, class Load, class Addr>
+__device__ __forceinline__ void poll_words(const KParams &p, Smem &s, uint64_t (&w)[N], uint32_t tag, Load load,
+                                           Addr addr) {
+    uint64_t t0 = 0;
+    uint32_t it = 0;
+    for (;;) {
+        load(w);
+        const uint64_t *stale = nullptr;
+#pragma unroll
+        for (int i = N - 1; i >= 0; i--)
+            if (!tag_ok(w[i], tag)) stale = addr(i);
+        if (!stale) return;
+        do {
+            if (poll_give_up(p, s, it++, t0)) return;
+        } while (!tag_ok(ld_tag(stale), tag));
     }
 }
+
+// Instruction boundary: every consumer thread is done with the shared-memory
+// scratch of this instruction before the next one writes it; reports, to all
+// alike, a failure any thread saw.
+__device__ __forceinline__ bool instr_sync(Smem &s) { return !consumer_any(s.abort); }
 
 // ---------------------------------------------------------------------------------
 // Matrix-vector instructions: the rows an SM owns are cut into segments (one per
@@ -366,38 +432,6 @@ __device__ __forceinline__ void attn_range(const KParams &p, int c, int &c0, int
 
 __device__ __forceinline__ int attn_pp(const KParams &p) { return PAGE_BYTES / (4 * p.hd); }
 
-// O-projection input: merge the KV splits of every query head into s.xin,
-// o = sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c with M = max_c m_c; each
-// thread produces 4 consecutive dimensions of one head.
-__device__ void stage_attention_output(const KParams &p, Smem &s) {
-    const int S = p.attn_splits, stride = p.hd + 4, qd = p.nq * p.hd;
-    for (int t = threadIdx.x; t < qd / 4; t += NCT) {
-        const int e0 = t * 4, h = e0 / p.hd, d0 = e0 % p.hd;
-        if (!LL_OK_IDX(12, e0 + 4, XIN_FLOATS + 1) || !LL_OK_IDX(13, (size_t(h) * S + S) * stride, size_t(p.nq) * S * stride + 1))
-            continue;
-        const float *base = p.part + size_t(h) * S * stride;
-        float M = -INFINITY;
-#pragma unroll 4
-        for (int c = 0; c < S; c++) M = fmaxf(M, __ldcg(base + size_t(c) * stride + p.hd));
-        float L = 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < S; c++) {
-            const float *pc = base + size_t(c) * stride;
-            const float m = __ldcg(pc + p.hd);
-            const float l = __ldcg(pc + p.hd + 1);
-            const float4 oc = __ldcg(reinterpret_cast<const float4 *>(pc + d0));
-            const float w = (m == -INFINITY) ? 0.f : expf(m - M);
-            L = fmaf(w, l, L);
-            o.x = fmaf(w, oc.x, o.x); o.y = fmaf(w, oc.y, o.y);
-            o.z = fmaf(w, oc.z, o.z); o.w = fmaf(w, oc.w, o.w);
-        }
-        const float inv = 1.0f / L;
-        *reinterpret_cast<float4 *>(&s.xin[e0]) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-    }
-    consumer_sync();
-}
-
 // Lane-held input vector: element (sw*32*VPL + j*32 + lane)*8 + e sits in xr[j*8+e].
 // The RMSNorm gain of a normed instruction (QKV, gate/up, LM head), or null.
 __device__ __forceinline__ const uint16_t *norm_gain(const KParams &p, const Instr &ins) {
@@ -420,47 +454,88 @@ __device__ __forceinline__ void load_gain(const KParams &p, const Instr &ins, co
         gv[j] = gain ? __ldg(reinterpret_cast<const uint4 *>(gain) + sw * 32 * VPL + j * 32 + lane) : make_uint4(0, 0, 0, 0);
 }
 
+// The instruction's input vector into registers (layout above), RMS-normed for
+// QKV, gate/up and the LM head. Inputs that fit s.xin are staged there first, so
+// that each tagged word is read once per block whatever the number of teams;
+// wider ones (the down projection's) are read straight into the lanes. Returns
+// false, in every consumer thread alike, if a wait failed.
 template <int VPL>
-__device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
+__device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
                            float (&xr)[VPL * 8], const uint4 (&gv)[VPL]) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int sw = (warp % (NCW / mv.teams)) % mv.ws;
     const bool normed = norm_gain(p, ins) != nullptr;
-    const float *src = nullptr;
-    const uint16_t *src16 = nullptr;
+    const uint64_t *src = nullptr;
+    uint32_t tag = 0;
     switch (ins.op) {
         case OP_QKV:
-            if (ins.layer == 0) src16 = p.embed + size_t(s.token) * p.H;
-            else src = p.x;
+            if (ins.layer > 0) {
+                src = p.t_xout;
+                tag = tag_of(p, ins.layer - 1);
+            }
             break;
-        case OP_GATEUP: src = p.x; break;
-        case OP_LMHEAD: src = p.x; break;
-        case OP_OPROJ: stage_attention_output(p, s); break;
-        default: src = p.act; break;
+        case OP_GATEUP: src = p.t_xmid; tag = tag_of(p, ins.layer); break;
+        case OP_LMHEAD: src = p.t_xout; tag = tag_of(p, p.L - 1); break;
+        case OP_DOWN: src = p.t_act; tag = tag_of(p, ins.layer); break;
+        case OP_OPROJ: src = p.t_o; tag = tag_of(p, ins.layer); break;
+        default: break;
     }
+    const bool staged = src && mv.K <= XIN_FLOATS;
+    if (staged) {
+        constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
+        uint64_t w[2 * PAIRS];
+        const int K = mv.K;
+        poll_words(p, s, w, tag, [&](uint64_t (&ww)[2 * PAIRS]) {
+#pragma unroll
+            for (int k = 0; k < PAIRS; k++) {
+                const int i = (tid + k * NCT) * 2;
+                if (i < K) ld_tag2(src + i, ww[2 * k], ww[2 * k + 1]);
+                else ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
+            }
+        }, [&](int i) { return src + (tid + (i / 2) * NCT) * 2 + (i & 1); });
+#pragma unroll
+        for (int k = 0; k < PAIRS; k++) {
+            const int i = (tid + k * NCT) * 2;
+            if (i < K) {
+                s.xin[i] = tag_val(w[2 * k]);
+                s.xin[i + 1] = tag_val(w[2 * k + 1]);
+            }
+        }
+    }
+    if (staged && consumer_any(s.abort)) return false;  // also publishes s.xin
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
         const int v = sw * 32 * VPL + j * 32 + lane;
         if (!LL_OK_IDX(11, v * 8 + 8, mv.K + 1)) continue;
-        if (ins.op == OP_OPROJ) {
+        if (staged) {
             const float4 a = *reinterpret_cast<const float4 *>(&s.xin[v * 8]);
             const float4 b = *reinterpret_cast<const float4 *>(&s.xin[v * 8 + 4]);
             xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
             xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
-        } else if (src16) {
-            uint4 u = __ldg(reinterpret_cast<const uint4 *>(src16) + v);
+        } else if (!src) {  // layer 0: the token's embedding row
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p.embed + size_t(s.token) * p.H) + v);
             xr[j * 8 + 0] = bf_lo(u.x); xr[j * 8 + 1] = bf_hi(u.x);
             xr[j * 8 + 2] = bf_lo(u.y); xr[j * 8 + 3] = bf_hi(u.y);
             xr[j * 8 + 4] = bf_lo(u.z); xr[j * 8 + 5] = bf_hi(u.z);
             xr[j * 8 + 6] = bf_lo(u.w); xr[j * 8 + 7] = bf_hi(u.w);
         } else {
-            float4 a = __ldcg(reinterpret_cast<const float4 *>(src) + 2 * v);
-            float4 b = __ldcg(reinterpret_cast<const float4 *>(src) + 2 * v + 1);
-            xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
-            xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
+            uint64_t w[8];
+            const uint64_t *at = src + size_t(v) * 8;
+            poll_words(p, s, w, tag, [&](uint64_t (&ww)[8]) {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) ld_tag2(at + e, ww[e], ww[e + 1]);
+            }, [&](int i) { return at + i; });
+#pragma unroll
+            for (int e = 0; e < 8; e++) xr[j * 8 + e] = tag_val(w[e]);
         }
     }
-    if (!normed) return;
+    if (!staged && src && consumer_any(s.abort)) return false;
+    if (!normed) {
+        // s.acc shares space with s.xin: every warp holds its input before any
+        // team writes row results
+        if (staged) consumer_sync();
+        return true;
+    }
     // RMSNorm: the warps w < ws together hold every element once.
     float ss = 0.f;
 #pragma unroll
@@ -480,6 +555,7 @@ __device__ void load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             xr[j * 8 + 2 * q + 1] = xr[j * 8 + 2 * q + 1] * r * bf_hi(g[q]);
         }
     }
+    return true;
 }
 
 // Sum R per-lane values across the warp so that the lanes of group
@@ -518,13 +594,8 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     if (nseg == 0) return true;  // no rows here: nothing to read or wait for
     uint4 gv[VPL];
     load_gain<VPL>(p, ins, mv, gv);
-    if (!dep_wait(p, s, ins)) return false;
-
     float xr[VPL * 8];
-    load_input<VPL>(p, s, ins, mv, xr, gv);
-    // s.acc shares space with the O projection's staged input: every warp must
-    // hold its input before any team writes row results
-    if (ins.op == OP_OPROJ) consumer_sync();
+    if (!load_input<VPL>(p, s, ins, mv, xr, gv)) return false;
     if (threadIdx.x == 0) trace_put(p, ii, 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -535,6 +606,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     const int nrows = ins.r1 - ins.r0;
     constexpr int GROUP = 32 / RW;  // lanes that end up holding one row's sum
     constexpr int QB = (RW < 4 / VPL) ? RW : (4 / VPL > 0 ? 4 / VPL : 1);  // rows loaded together
+    bool bad = false;  // a page wait failed: walk on without work, leave together below
 
     for (int si = 0; si < nseg; si++) {
         const Seg sg = seg[si];
@@ -545,7 +617,10 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
             const uint32_t slot = cpage % NPAGES;
             const uint32_t this_page = cpage++;
             if (int(this_page % uint32_t(mv.teams)) != team || wt >= active) continue;
-            if (!wait_page(p, s, this_page)) return false;
+            if (bad || !wait_page(p, s, this_page)) {
+                bad = true;
+                continue;
+            }
             if (wt == 0 && lane == 0) {
                 ptrace_put(p, this_page, 1);
                 if (si == 0 && pr == 0) trace_put(p, ii, 6);
@@ -614,12 +689,14 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
         }
     }
     if (tid == 0) trace_put(p, ii, 7);
-    consumer_sync();  // every page reduced into s.acc
+    if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
     const int r0 = ins.r0;
+    const uint32_t wtag = write_tag(p, ins);
     switch (ins.op) {
         case OP_QKV:
             for (int t = tid; t < nrows; t += NCT)
-                if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS)) p.qkv[r0 + t] = s.acc[t];
+                if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS))
+                    st_tag(p.t_qkv + r0 + t, s.acc[t], wtag);
             break;
         case OP_OPROJ:
         case OP_DOWN: {
@@ -632,7 +709,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
                 const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : s.xown[t];
                 const float v = base + s.acc[t];
                 s.xown[t] = v;
-                p.x[row] = v;
+                st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + row, v, wtag);
             }
             break;
         }
@@ -640,7 +717,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
             for (int t = tid; t < nrows; t += NCT) {
                 const float g = s.acc[t];
                 if (LL_OK_IDX(8, r0 + t, p.I) && LL_OK_IDX(9, nrows + t, ACC_FLOATS))
-                    p.act[r0 + t] = g / (1.0f + expf(-g)) * s.acc[nrows + t];
+                    st_tag(p.t_act + r0 + t, g / (1.0f + expf(-g)) * s.acc[nrows + t], wtag);
             }
             break;
         default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
@@ -830,6 +907,74 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
     if (tid == 0) trace_put(p, ii, 10);
 }
 
+// The S splits of KV head g merge their partials between them: split c takes
+// outputs [c*G*hd/S, (c+1)*G*hd/S) of the group's G*hd, for each
+//   o = sum_c' exp(m_c' - M) o_c' / sum_c' exp(m_c' - M) l_c',  M = max_c' m_c',
+// and stores them, tagged, to t_o. The threads of one output split the S partials
+// between them (a running maximum each), then one thread combines theirs through
+// shared memory.
+__device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int hd, uint32_t tag, uint32_t wtag) {
+    const int S = p.attn_splits, GH = G * hd, stride = hd + 4, tid = threadIdx.x;
+    const int v0 = static_cast<int>(static_cast<long long>(c) * GH / S);
+    const int nv = static_cast<int>(static_cast<long long>(c + 1) * GH / S) - v0;
+    if (nv <= 0) return true;  // uniform: no outputs for this split
+    const int T = NCT / nv;    // threads per output (nv <= 512)
+    const int v = tid % nv, j = tid / nv;
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    if (j < T) {
+        const int h = (v0 + v) / hd, d = (v0 + v) % hd;
+        const uint64_t *base = p.t_part + size_t(g * G + h) * S * stride;
+        for (int cb = j; cb < S; cb += 4 * T) {
+            uint64_t w[12];  // per split: m, l, o[d]
+            poll_words(p, s, w, tag, [&](uint64_t (&ww)[12]) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int c2 = cb + k * T;
+                    if (c2 < S) {
+                        const uint64_t *pc = base + size_t(c2) * stride;
+                        ld_tag2(pc + hd, ww[3 * k], ww[3 * k + 1]);
+                        ww[3 * k + 2] = ld_tag(pc + d);
+                    } else {
+                        ww[3 * k] = ww[3 * k + 1] = ww[3 * k + 2] = static_cast<uint64_t>(tag) << 32;
+                    }
+                }
+            }, [&](int i) {
+                const uint64_t *pc = base + size_t(cb + (i / 3) * T) * stride;
+                return i % 3 == 2 ? pc + d : pc + hd + i % 3;
+            });
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                if (cb + k * T >= S) break;
+                const float m = tag_val(w[3 * k]);
+                if (m == -INFINITY) continue;  // a split with no positions
+                const float Mn = fmaxf(M, m);
+                const float a = (M == -INFINITY) ? 0.f : expf(M - Mn), b = expf(m - Mn);
+                L = L * a + tag_val(w[3 * k + 1]) * b;
+                O = O * a + tag_val(w[3 * k + 2]) * b;
+                M = Mn;
+            }
+        }
+        s.xin[(j * nv + v) * 3 + 0] = M;
+        s.xin[(j * nv + v) * 3 + 1] = L;
+        s.xin[(j * nv + v) * 3 + 2] = O;
+    }
+    if (consumer_any(s.abort)) return false;
+    if (tid < nv) {
+        float Mx = -INFINITY;
+        for (int jj = 0; jj < T; jj++) Mx = fmaxf(Mx, s.xin[(jj * nv + tid) * 3]);
+        float Ls = 0.f, Os = 0.f;
+        for (int jj = 0; jj < T; jj++) {
+            const float m = s.xin[(jj * nv + tid) * 3];
+            if (m == -INFINITY) continue;
+            const float b = expf(m - Mx);
+            Ls = fmaf(s.xin[(jj * nv + tid) * 3 + 1], b, Ls);
+            Os = fmaf(s.xin[(jj * nv + tid) * 3 + 2], b, Os);
+        }
+        st_tag(p.t_o + size_t(g) * GH + v0 + tid, Os / Ls, wtag);
+    }
+    return true;
+}
+
 template <int DL>
 __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
@@ -839,29 +984,46 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     const float2 *cs = p.rope_cs + size_t(p.pos) * half;
-    // the group's query heads with RoPE ("rotate half") applied, pre-scaled by 1/sqrt(hd)
-    if (tid < G * hd) {
+    const uint32_t tag = tag_of(p, l);
+    // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
+    // 1/sqrt(hd); the owner also rotates the new key and takes the new value
+    {
+        const uint64_t *qh = p.t_qkv + size_t(g * G) * hd;
+        const uint64_t *kh = p.t_qkv + qd + size_t(g) * hd;
+        const uint64_t *vh = p.t_qkv + qd + kd + size_t(g) * hd;
+        const bool has_q = tid < G * hd, has_k = owner && tid < half, has_v = owner && tid < hd;
         const int h = tid / hd, d = tid % hd, i = d < half ? d : d - half;
-        const float *qh = p.qkv + size_t(g * G + h) * hd;
-        const float a = __ldcg(qh + i), b = __ldcg(qh + i + half);
-        const float2 r = cs[i];
-        s.qr[h][d] = (d < half ? a * r.x - b * r.y : a * r.y + b * r.x) * scale;
-    }
-    if (owner) {
-        for (int i = tid; i < half; i += NCT) {
-            const float *k = p.qkv + qd + size_t(g) * hd;
-            const float a = __ldcg(k + i), b = __ldcg(k + i + half);
+        uint64_t w[5];
+        poll_words(p, s, w, tag, [&](uint64_t (&ww)[5]) {
+            const uint64_t ok = static_cast<uint64_t>(tag) << 32;
+            ww[0] = has_q ? ld_tag(qh + size_t(h) * hd + i) : ok;
+            ww[1] = has_q ? ld_tag(qh + size_t(h) * hd + i + half) : ok;
+            ww[2] = has_k ? ld_tag(kh + tid) : ok;
+            ww[3] = has_k ? ld_tag(kh + tid + half) : ok;
+            ww[4] = has_v ? ld_tag(vh + tid) : ok;
+        }, [&](int k) {
+            const uint64_t *a[5] = {qh + size_t(h) * hd + i, qh + size_t(h) * hd + i + half, kh + tid, kh + tid + half,
+                                    vh + tid};
+            return a[k];
+        });
+        if (has_q) {
+            const float a = tag_val(w[0]), b = tag_val(w[1]);
             const float2 r = cs[i];
-            s.knew[i] = f_to_bf16(a * r.x - b * r.y);
-            s.knew[i + half] = f_to_bf16(a * r.y + b * r.x);
+            s.qr[h][d] = (d < half ? a * r.x - b * r.y : a * r.y + b * r.x) * scale;
         }
-        for (int d = tid; d < hd; d += NCT) s.vnew[d] = f_to_bf16(__ldcg(p.qkv + qd + kd + size_t(g) * hd + d));
+        if (has_k) {
+            const float a = tag_val(w[2]), b = tag_val(w[3]);
+            const float2 r = cs[tid];
+            s.knew[tid] = f_to_bf16(a * r.x - b * r.y);
+            s.knew[tid + half] = f_to_bf16(a * r.y + b * r.x);
+        }
+        if (has_v) s.vnew[tid] = f_to_bf16(tag_val(w[4]));
     }
     if (tid < G) {
         s.m_run[tid] = -INFINITY;
         s.l_run[tid] = 0.f;
     }
-    consumer_sync();
+    if (consumer_any(s.abort)) return false;
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
         const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
@@ -879,7 +1041,7 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
         const int n = min(PP, c1 - p0);
         const bool with_new = owner && p0 + PP >= c1;  // fold the new token into the last page
         const uint32_t slot = cpage % NPAGES;
-        if (!wait_page(p, s, cpage)) return false;
+        if (consumer_any(!wait_page(p, s, cpage))) return false;
         if (tid == 0) {
             ptrace_put(p, cpage, 1);
             trace_put(p, ii, 6);
@@ -897,22 +1059,20 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
 
     // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}]
     const int stride = hd + 4;
+    const uint32_t wtag = write_tag(p, ins);
     if (tid < G * hd) {
         const int h = tid / hd, d = tid % hd;
-        p.part[(size_t(g * G + h) * S + c) * stride + d] = oacc;
+        st_tag(p.t_part + (size_t(g * G + h) * S + c) * stride + d, oacc, wtag);
     }
     if (tid < G && LL_OK_IDX(17, (size_t(g * G + tid) * S + c) * stride + hd + 1, size_t(p.nq) * S * stride)) {
-        p.part[(size_t(g * G + tid) * S + c) * stride + hd] = s.m_run[tid];
-        p.part[(size_t(g * G + tid) * S + c) * stride + hd + 1] = s.l_run[tid];
+        st_tag(p.t_part + (size_t(g * G + tid) * S + c) * stride + hd, s.m_run[tid], wtag);
+        st_tag(p.t_part + (size_t(g * G + tid) * S + c) * stride + hd + 1, s.l_run[tid], wtag);
     }
     if (tid == 0) trace_put(p, ii, 2);
-    signal_done(p, ins);
-    if (tid == 0) trace_put(p, ii, 11);
-    return true;
+    return merge_splits(p, s, g, c, G, hd, tag, wtag);
 }
 
 __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
-    if (!dep_wait(p, s, ins)) return false;
     return p.hd == 64 ? attn_item<2>(p, s, pages, ins, ii, cpage) : attn_item<4>(p, s, pages, ins, ii, cpage);
 }
 
@@ -951,6 +1111,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     bool ok = true;
     const int PP = attn_pp(p);
     const uint32_t l2_ahead = p.l2_prefetch;
+    const uint32_t lim = p.max_inflight >= 1 && p.max_inflight < NPAGES ? p.max_inflight : NPAGES;
     for (int di = 0; di < nd && ok; di++) {
         const PDesc e = dl[di];
         int a_c0 = 0, a_c1 = 1, a_p0 = 0;
@@ -978,32 +1139,38 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                 b0 = e.bytes;
             }
             const uint32_t slot = ppage % NPAGES;
-            if (ppage >= NPAGES) {
-                uint64_t *bar = &s.empty[slot];
-                const uint32_t par = ((ppage / NPAGES) - 1u) & 1u;
-                if (!mbar_test(bar, par)) {
-                    if (pfi < di) pfi = di;  // from the page that is waiting for this slot
-                    const uint64_t t0 = gtimer();
-                    for (uint32_t it = 1;; ++it) {
-                        if (mbar_test(bar, par)) break;
-                        // while held up, pull the weight pages that come next into L2
-                        if (pfi < nd && uint32_t(pfi - di) < l2_ahead) {
-                            const PDesc f = dl[pfi++];
-                            if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
-                            continue;
-                        }
-                        __nanosleep(p.producer_sleep_ns);
-                        if ((it & 15u) == 0) {
-                            if (s.abort) { ok = false; break; }
-                            if (gtimer() - t0 > p.timeout_ns) {
-                                raise_status(p, s, LL_ERR_DEP_TIMEOUT);
-                                ok = false;
-                                break;
-                            }
+            // a page goes out once its slot is free and fewer than p.max_inflight
+            // earlier pages are still landing
+            auto can_issue = [&]() -> bool {
+                if (ppage >= NPAGES && !mbar_test(&s.empty[slot], ((ppage / NPAGES) - 1u) & 1u)) return false;
+                if (ppage >= lim) {
+                    const uint32_t q = ppage - lim;
+                    if (!mbar_test(&s.full[q % NPAGES], (q / NPAGES) & 1u)) return false;
+                }
+                return true;
+            };
+            if (!can_issue()) {
+                if (pfi < di) pfi = di;  // from the page that is waiting
+                const uint64_t t0 = gtimer();
+                for (uint32_t it = 1;; ++it) {
+                    if (can_issue()) break;
+                    // while held up, pull the weight pages that come next into L2
+                    if (pfi < nd && uint32_t(pfi - di) < l2_ahead) {
+                        const PDesc f = dl[pfi++];
+                        if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
+                        continue;
+                    }
+                    __nanosleep(p.producer_sleep_ns);
+                    if ((it & 15u) == 0) {
+                        if (s.abort) { ok = false; break; }
+                        if (gtimer() - t0 > p.timeout_ns) {
+                            raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                            ok = false;
+                            break;
                         }
                     }
-                    if (!ok) break;
                 }
+                if (!ok) break;
             }
             uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
             ptrace_put(p, ppage, 0);
@@ -1061,12 +1228,9 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
 #undef LL_MV_CASE
                 default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
             }
-            if (ok && ins.op == OP_LMHEAD) {
-                lm_finish(p, s, best, best_idx);
-            } else if (ok && ins.op != OP_ATTN) {
-                signal_done(p, ins);
-            }
+            if (ok && ins.op == OP_LMHEAD) lm_finish(p, s, best, best_idx);
         }
+        if (ok) ok = instr_sync(s);
         if (!ok) return;
         if (threadIdx.x == 0) trace_put(p, i, 3);
     }

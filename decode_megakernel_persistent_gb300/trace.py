@@ -49,7 +49,6 @@ def summarize(trace: np.ndarray, plan: np.ndarray) -> dict:
             rec["scores_us"] = float(np.mean((w8 - f1)[sub])) / 1e3
             rec["softmax_us"] = float(np.mean((w9 - w8)[sub])) / 1e3
             rec["pv_us"] = float(np.mean((w10 - w9)[sub])) / 1e3
-            rec["signal_us"] = float(np.mean((w11 - pg)[sub])) / 1e3
         if issued.any():
             # producer: first page issued relative to the consumer reaching the
             # instruction (negative = issued ahead), and last issue relative to its end

@@ -124,11 +124,11 @@ int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, fl
 
 /* Wait for the handle's stream, then return and clear the device status of the
  * steps enqueued since the last check (LL_OK if all of them succeeded). After
- * an error the library resets its counters, so the next step starts clean. */
+ * an error the library clears its device state, so the next step starts clean. */
 int ll_synchronize(ll_handle *h);
 
-/* Upper bound, in nanoseconds, on any single device-side wait (dependency
- * counters and shared-memory page handoff). Past it the kernel records
+/* Upper bound, in nanoseconds, on any single device-side wait (for tagged
+ * activations from other SMs, and the shared-memory page handoff). Past it the kernel records
  * LL_ERR_DEP_TIMEOUT, lets its own copies land, and returns. Default 1 s. */
 int ll_set_timeout_ns(ll_handle *h, uint64_t ns);
 
@@ -160,8 +160,9 @@ int ll_query(const ll_handle *h, int what, int64_t *value);
 /* Fault injection for tests (host side only; nothing faults on the device):
  * LL_FAULT_DROP_SIGNAL removes the completion signal of every instruction of
  * kind `op` (0 QKV, 1 attention, 2 O projection, 3 gate/up, 4 down) in layer
- * `layer`, so the instruction waiting on it runs into its time limit and the
- * step returns LL_ERR_DEP_TIMEOUT. LL_FAULT_NONE restores the schedule. */
+ * `layer`: those instructions store their outputs with a tag no reader accepts,
+ * so the instruction waiting on them runs into its time limit and the step
+ * returns LL_ERR_DEP_TIMEOUT. LL_FAULT_NONE restores the schedule. */
 #define LL_FAULT_NONE 0
 #define LL_FAULT_DROP_SIGNAL 1
 int ll_debug_inject(ll_handle *h, int kind, int layer, int op);
@@ -171,8 +172,10 @@ int ll_debug_inject(ll_handle *h, int kind, int layer, int op);
  * When out is not NULL it must hold nsm*max_instr*7 int32, filled [sm][i] with
  * (op, layer, r0, r1, wait_counter, wait_count, signal_counter); op is 0 QKV,
  * 1 attention, 2 O projection, 3 gate/up, 4 down, 5 LM head, -1 an unused slot;
- * [r0, r1) is the SM's row range, or (KV head, split) for attention; counters
- * are -1 where there is none. */
+ * [r0, r1) is the SM's row range, or (KV head, split) for attention. The
+ * counter fields name the dependency: the instruction reads the outputs that
+ * wait_count instructions marked signal_counter produce (the kernel finds
+ * them ready by their tags); -1 where there is none. */
 int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr);
 
 /* Explanation of the last error on this handle (never NULL). */
