@@ -519,16 +519,29 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             xr[j * 8 + 4] = bf_lo(u.z); xr[j * 8 + 5] = bf_hi(u.z);
             xr[j * 8 + 6] = bf_lo(u.w); xr[j * 8 + 7] = bf_hi(u.w);
         } else {
+            // wide input, one 256-element group per j: the warp reads it with
+            // coalesced loads (lane l takes words 2l + 64r, r < 4) and turns it
+            // into the lane layout through its own 256 floats of s.xin
             uint64_t w[8];
-            const uint64_t *at = src + size_t(v) * 8;
+            const uint64_t *at = src + size_t(sw * 32 * VPL + j * 32) * 8;
             poll_words(p, s, w, tag, [&](uint64_t (&ww)[8]) {
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) ld_tag2(at + e, ww[e], ww[e + 1]);
-            }, [&](int i) { return at + i; });
+                for (int r = 0; r < 4; r++) ld_tag2(at + 64 * r + 2 * lane, ww[2 * r], ww[2 * r + 1]);
+            }, [&](int i) { return at + 64 * (i / 2) + 2 * lane + (i & 1); });
+            float *tw = s.xin + warp * 256;
 #pragma unroll
-            for (int e = 0; e < 8; e++) xr[j * 8 + e] = tag_val(w[e]);
+            for (int r = 0; r < 4; r++)
+                *reinterpret_cast<float2 *>(tw + 64 * r + 2 * lane) = make_float2(tag_val(w[2 * r]), tag_val(w[2 * r + 1]));
+            __syncwarp();
+            const float4 a = *reinterpret_cast<const float4 *>(tw + 8 * lane);
+            const float4 b = *reinterpret_cast<const float4 *>(tw + 8 * lane + 4);
+            xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
+            xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
+            __syncwarp();
         }
     }
+    // (wide inputs: also every warp is done with its part of s.xin, which
+    // s.acc overlaps, before any team writes row results)
     if (!staged && src && consumer_any(s.abort)) return false;
     if (!normed) {
         // s.acc shares space with s.xin: every warp holds its input before any
