@@ -307,6 +307,24 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
 
 // Tag of the words an instruction of `layer` writes in the current step (never 0
 // for a live step, so cleared memory never passes).
+//
+// Each tagged buffer is rewritten once per layer, and no untagged signal orders
+// a rewrite after the last read of the previous layer's words; the data flow
+// does. Every SM's QKV rows feed some attention item, every attention item
+// feeds every O-projection SM (the full merged vector), every O-projection SM
+// feeds every gate/up SM (the full residual), every gate/up SM feeds every
+// down SM (the full act vector), and every down SM feeds every QKV SM (the full
+// residual). So before any SM can write a buffer for layer l + 1 it has waited,
+// through this chain, on words that every reader of the layer-l words produced
+// after reading them:
+//   qkv    (QKV -> attention):  rewrite needs x_out(l) from all down SMs;
+//   part   (attention -> merge): rewrite needs qkv(l+1), i.e. x_out(l), i.e. o(l) merged;
+//   o      (merge -> O):        rewrite needs qkv(l+1), i.e. every O-projection SM done;
+//   x_mid  (O -> gate/up):      rewrite needs o(l+1), i.e. every gate/up SM done with layer l;
+//   act    (gate/up -> down):   rewrite needs x_mid(l+1), i.e. every down SM done with layer l;
+//   x_out  (down -> QKV, LM):   rewrite needs act(l+1), i.e. every QKV SM done with layer l
+// (and the LM head's read of the last layer is in the same launch, before any
+// next-step write, which belongs to the next launch).
 __device__ __forceinline__ uint32_t tag_of(const KParams &p, int layer) {
     return p.epoch * static_cast<uint32_t>(p.L + 1) + static_cast<uint32_t>(layer) + 1u;
 }
