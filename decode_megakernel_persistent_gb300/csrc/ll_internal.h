@@ -74,6 +74,7 @@ enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1 };
 struct LayerW {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
 };
+constexpr int SMEM_LAYERS = 32;  // layers whose weight pointers the megakernel keeps in shared memory
 
 // Counters, each on its own 128-byte line.
 constexpr int CTR_STRIDE = 32;  // uint32 per counter slot

@@ -218,6 +218,7 @@ struct alignas(16) Smem {
     alignas(16) uint16_t vnew[MAX_HD];
     float m_run[MAX_GQA], l_run[MAX_GQA], alpha[MAX_GQA];
     float xown[XOWN_MAX];  // this SM's rows of the residual stream (the O and down rows)
+    LayerW lw[SMEM_LAYERS];  // weight pointers of the first SMEM_LAYERS layers, copied at kernel start
     float nred[NCW];
     unsigned long long kred[NCW];
     int32_t token;
@@ -360,25 +361,18 @@ __device__ __forceinline__ bool poll_give_up(const KParams &p, Smem &s, uint32_t
 }
 
 // Load N tagged words with `load(w)` (which fills every entry; entries it does
-// not need it sets to a word with the expected tag; word i sits at addr(i))
-// until all carry `tag`. While one is stale the thread re-reads that word alone,
-// so a block waiting on a wide input puts one load per thread on L2 per round,
-// not the whole input.
-template <int N, class Load, class Addr>
-__device__ __forceinline__ void poll_words(const KParams &p, Smem &s, uint64_t (&w)[N], uint32_t tag, Load load,
-                                           Addr addr) {
+// not need it sets to a word with the expected tag) until all carry `tag`. Every
+// round reloads them all: whichever word turns current first, the thread sees
+// the rest within the same round trip.
+template <int N, class Load>
+__device__ __forceinline__ void poll_words(const KParams &p, Smem &s, uint64_t (&w)[N], uint32_t tag, Load load) {
     uint64_t t0 = 0;
-    uint32_t it = 0;
-    for (;;) {
+    for (uint32_t it = 0;; ++it) {
         load(w);
-        const uint64_t *stale = nullptr;
+        bool ok = true;
 #pragma unroll
-        for (int i = N - 1; i >= 0; i--)
-            if (!tag_ok(w[i], tag)) stale = addr(i);
-        if (!stale) return;
-        do {
-            if (poll_give_up(p, s, it++, t0)) return;
-        } while (!tag_ok(ld_tag(stale), tag));
+        for (int i = 0; i < N; i++) ok = ok && tag_ok(w[i], tag);
+        if (ok || poll_give_up(p, s, it, t0)) return;
     }
 }
 
@@ -405,8 +399,14 @@ __device__ __forceinline__ const MvShape &mv_of(const KParams &p, int op) {
     return op == OP_OPROJ ? p.mv_q : (op == OP_DOWN ? p.mv_i : p.mv_h);
 }
 
-__device__ int mv_segments(const KParams &p, const Instr &ins, Seg *seg) {
-    const LayerW *lw = ins.op == OP_LMHEAD ? nullptr : &p.layers[ins.layer];
+// A layer's weight pointers, from shared memory for the first SMEM_LAYERS layers:
+// an instruction then does not start with a dependent global load.
+__device__ __forceinline__ const LayerW &layer_w(const KParams &p, const Smem &s, int l) {
+    return l < SMEM_LAYERS ? s.lw[l] : p.layers[l];
+}
+
+__device__ int mv_segments(const KParams &p, const Smem &s, const Instr &ins, Seg *seg) {
+    const LayerW *lw = ins.op == OP_LMHEAD ? nullptr : &layer_w(p, s, ins.layer);
     const int r0 = ins.r0, r1 = ins.r1;
     int n = 0;
     switch (ins.op) {
@@ -452,10 +452,10 @@ __device__ __forceinline__ int attn_pp(const KParams &p) { return PAGE_BYTES / (
 
 // Lane-held input vector: element (sw*32*VPL + j*32 + lane)*8 + e sits in xr[j*8+e].
 // The RMSNorm gain of a normed instruction (QKV, gate/up, LM head), or null.
-__device__ __forceinline__ const uint16_t *norm_gain(const KParams &p, const Instr &ins) {
+__device__ __forceinline__ const uint16_t *norm_gain(const KParams &p, const Smem &s, const Instr &ins) {
     switch (ins.op) {
-        case OP_QKV: return p.layers[ins.layer].attn_norm;
-        case OP_GATEUP: return p.layers[ins.layer].mlp_norm;
+        case OP_QKV: return layer_w(p, s, ins.layer).attn_norm;
+        case OP_GATEUP: return layer_w(p, s, ins.layer).mlp_norm;
         case OP_LMHEAD: return p.final_norm;
         default: return nullptr;
     }
@@ -463,8 +463,8 @@ __device__ __forceinline__ const uint16_t *norm_gain(const KParams &p, const Ins
 
 // Gains are weights: a lane's slice is fetched before the dependency wait.
 template <int VPL>
-__device__ __forceinline__ void load_gain(const KParams &p, const Instr &ins, const MvShape &mv, uint4 (&gv)[VPL]) {
-    const uint16_t *gain = norm_gain(p, ins);
+__device__ __forceinline__ void load_gain(const KParams &p, const Smem &s, const Instr &ins, const MvShape &mv, uint4 (&gv)[VPL]) {
+    const uint16_t *gain = norm_gain(p, s, ins);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sw = (warp % (NCW / mv.teams)) % mv.ws;
 #pragma unroll
@@ -482,7 +482,7 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
                            float (&xr)[VPL * 8], const uint4 (&gv)[VPL]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int sw = (warp % (NCW / mv.teams)) % mv.ws;
-    const bool normed = norm_gain(p, ins) != nullptr;
+    const bool normed = norm_gain(p, s, ins) != nullptr;
     const uint64_t *src = nullptr;
     uint32_t tag = 0;
     switch (ins.op) {
@@ -510,7 +510,7 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
                 if (i < K) ld_tag2(src + i, ww[2 * k], ww[2 * k + 1]);
                 else ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
             }
-        }, [&](int i) { return src + (tid + (i / 2) * NCT) * 2 + (i & 1); });
+        });
 #pragma unroll
         for (int k = 0; k < PAIRS; k++) {
             const int i = (tid + k * NCT) * 2;
@@ -545,7 +545,7 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             poll_words(p, s, w, tag, [&](uint64_t (&ww)[8]) {
 #pragma unroll
                 for (int r = 0; r < 4; r++) ld_tag2(at + 64 * r + 2 * lane, ww[2 * r], ww[2 * r + 1]);
-            }, [&](int i) { return at + 64 * (i / 2) + 2 * lane + (i & 1); });
+            });
             float *tw = s.xin + warp * 256;
 #pragma unroll
             for (int r = 0; r < 4; r++)
@@ -621,10 +621,10 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
                          float &best, int &best_idx) {
     const MvShape &mv = mv_of(p, ins.op);
     Seg seg[3];
-    const int nseg = mv_segments(p, ins, seg);
+    const int nseg = mv_segments(p, s, ins, seg);
     if (nseg == 0) return true;  // no rows here: nothing to read or wait for
     uint4 gv[VPL];
-    load_gain<VPL>(p, ins, mv, gv);
+    load_gain<VPL>(p, s, ins, mv, gv);
     float xr[VPL * 8];
     if (!load_input<VPL>(p, s, ins, mv, xr, gv)) return false;
     if (threadIdx.x == 0) trace_put(p, ii, 1);
@@ -969,9 +969,6 @@ __device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int
                         ww[3 * k] = ww[3 * k + 1] = ww[3 * k + 2] = static_cast<uint64_t>(tag) << 32;
                     }
                 }
-            }, [&](int i) {
-                const uint64_t *pc = base + size_t(cb + (i / 3) * T) * stride;
-                return i % 3 == 2 ? pc + d : pc + hd + i % 3;
             });
 #pragma unroll
             for (int k = 0; k < 4; k++) {
@@ -1032,10 +1029,6 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
             ww[2] = has_k ? ld_tag(kh + tid) : ok;
             ww[3] = has_k ? ld_tag(kh + tid + half) : ok;
             ww[4] = has_v ? ld_tag(vh + tid) : ok;
-        }, [&](int k) {
-            const uint64_t *a[5] = {qh + size_t(h) * hd + i, qh + size_t(h) * hd + i + half, kh + tid, kh + tid + half,
-                                    vh + tid};
-            return a[k];
         });
         if (has_q) {
             const float a = tag_val(w[0]), b = tag_val(w[1]);
@@ -1283,6 +1276,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         s.flag = 0;
         s.token = p.token_dev ? *p.token_dev : p.token;
         s.start_status = ld_relaxed(p.status);
+    }
+    {
+        const int nl = p.L < SMEM_LAYERS ? p.L : SMEM_LAYERS;
+        constexpr int WORDS = sizeof(LayerW) / 8;
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.layers);
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(s.lw);
+        for (int i = threadIdx.x; i < nl * WORDS; i += NTHREADS) dst[i] = __ldg(src + i);
     }
     __syncthreads();
     if (s.start_status != 0) return;  // an earlier step failed: do nothing
