@@ -315,6 +315,18 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.max_seq = c.max_seq;
     p.eps = c.rms_eps;
     p.attn_splits = h->splits;
+    {
+        // kernel variant: per-warp (flash) softmax when the longest attention item
+        // at max_seq spans at least 10 pages. Its merge of the warps costs ~1.5 us
+        // per item and its variant of the kernel runs the matrix-vector products a
+        // little slower, so it pays off only where attention dominates (measured:
+        // 1B at 32k context -10 %, 8B at 8k with 7-page items +9 %). Tuning knob
+        // LL_ATTN_FLASH = 0 / 1 overrides.
+        const int per_split = (c.max_seq + h->splits - 1) / h->splits;
+        const int pp = ll::PAGE_BYTES / (4 * c.head_dim);
+        p.attn_flash = (per_split + pp - 1) / pp >= 10 ? 1 : 0;
+        if (const char *e = std::getenv("LL_ATTN_FLASH")) p.attn_flash = std::atoi(e) ? 1 : 0;
+    }
     p.mv_h = mh;
     p.mv_q = mq;
     p.mv_i = mi;

@@ -105,6 +105,7 @@ struct KParams {
     int32_t L, H, nq, nkv, hd, I, V, max_seq;
     float eps;
     int32_t attn_splits;
+    int32_t attn_flash;       // kernel variant: per-warp softmax in attention (long items)
     MvShape mv_h, mv_q, mv_i; // input widths hidden, n_q*hd, inter
     // Activations between instructions, as tagged words: (tag << 32) | fp32 bits,
     // stored and loaded as single 8-byte accesses. A reader takes a word only

@@ -197,16 +197,23 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 // ---------------------------------------------------------------------------------
 // Shared memory
 
+// One merge slot of the attention warps (per-warp softmax): o for up to 512
+// (query head, dim) pairs (n_q / n_kv * head_dim <= 512), then m and l of up to
+// 8 heads.
+constexpr int AT_SLOT = 512 + 2 * MAX_GQA;
+
 struct alignas(16) Smem {
     union {
         float xin[XIN_FLOATS];  // O-projection input: the merged attention output; also the
                                 // attention P.V partials of the P.V warps
         float acc[ACC_FLOATS];  // the SM's row results of the current matrix-vector instruction
-        struct {
+        struct {                                // attention, block-wide softmax per page:
             float ared_lo[ATT_WARPS * 4 * 64];  // P.V partials of four heads of 64 dims
-            float sc[MAX_GQA][132];             // attention scores of up to 129 positions
+            float sc[MAX_GQA][132];             // scores of up to 129 positions
             float pt[132][MAX_GQA];             // their probabilities, position-major
         };
+        uint32_t qf[2][MAX_HD / 16][32][2];  // attention, per-warp softmax: query MMA fragments (bf16 hi, lo)
+        float ared[NCW / 2][AT_SLOT];        // attention, per-warp softmax: (o, m, l) of warps being merged
     };
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
     uint64_t empty[NPAGES];  // page released by the consumers
@@ -1096,8 +1103,270 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     return merge_splits(p, s, g, c, G, hd, tag, wtag);
 }
 
+// Tensor-core step of the attention: D += A * B with A 16 x 16 bf16 (rows g + 8
+// of A are zero, since a KV head has at most 8 query heads), B 16 x 8 bf16, D
+// 16 x 8 fp32 (m16n8k16). Lane (g, t) = (lane / 4, lane % 4) holds A rows g at
+// columns 2t, 2t + 1 (a0) and 2t + 8, 2t + 9 (a2), B rows 2t, 2t + 1 (b0) and
+// 2t + 8, 2t + 9 (b1) of column g, and D row g at columns 2t, 2t + 1 (d0, d1).
+__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// x as the sum of two bf16 terms (hi, lo), so that a bf16 tensor-core product of
+// x with a bf16 operand keeps ~16 bits of x.
+__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
+    hi = f_to_bf16(x);
+    lo = f_to_bf16(x - bf16_to_f(hi));
+}
+
+// Attention over one page of n cached positions (K rows at kbase, V rows at vbase)
+// plus, if with_new, the new token (s.knew, s.vnew) at index n, for the group's G
+// query heads, as flash decoding within the block. The warps form HD / 64 dim
+// groups of NCW * 64 / HD warps; warp w (group dg, index tw) takes the 8-position
+// tiles tw, tw + group size, ... and keeps its own running softmax and its
+// group's 64 dims of O. Per tile: S = Q K^T on tensor cores (Q from its bf16
+// hi/lo fragments in s.qf, K straight from the page); the tile's maximum and sum
+// over the 4 lanes of each head; P = exp(S - m) split into bf16 hi/lo, which in
+// the m16n8k16 layouts is already the A fragment of the next product; O += P V
+// with V straight from the page. Lane (g, t) keeps head g's running m and l and
+// its O at dims 64 dg + 8d + 2t, +1 for d < 8.
+template <int HD>
+__device__ __forceinline__ void attn_tiles(const Smem &s, uint32_t kbase, uint32_t vbase, int n, bool with_new,
+                                           float &m_run, float &l_run, float (&o)[8][2]) {
+    constexpr int KS = HD / 16, GW = NCW * 64 / HD;  // k-steps; warps per dim group
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int dg = warp / GW, tw = warp % GW;
+    const int nt = n + (with_new ? 1 : 0);
+    const uint32_t knew = smem_addr(s.knew), vnew = smem_addr(s.vnew);
+    for (int tile = tw; tile * 8 < nt; tile += GW) {
+        // scores: column g of K^T is position tile * 8 + g (past the last one: a
+        // finite stand-in row, masked below)
+        const int jb = tile * 8 + g;
+        const uint32_t krow = jb < n ? kbase + uint32_t(jb) * (HD * 2) : knew;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t qa = smem_addr(&s.qf[0][0][lane][0]);  // (volatile loads: not kept across tiles)
+        constexpr uint32_t QHL = sizeof(s.qf[0]), QKS = sizeof(s.qf[0][0]);
+#pragma unroll
+        for (int ks = 0; ks < KS; ks++) {
+            const uint32_t b0 = lds_u32(krow + (16 * ks + 2 * t) * 2);
+            const uint32_t b1 = lds_u32(krow + (16 * ks + 2 * t + 8) * 2);
+            const uint32_t qh = qa + ks * QKS, ql = qh + QHL;
+            mma_rows8(c, lds_u32(qh), lds_u32(qh + 4), b0, b1);
+            mma_rows8(c, lds_u32(ql), lds_u32(ql + 4), b0, b1);
+        }
+        // this lane: head g at positions j0 = tile * 8 + 2t and j0 + 1
+        const int j0 = tile * 8 + 2 * t;
+        const float s0 = j0 < nt ? c[0] : -INFINITY, s1 = j0 + 1 < nt ? c[1] : -INFINITY;
+        float mt = fmaxf(s0, s1);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        const float m_new = fmaxf(m_run, mt);  // finite: position tile * 8 exists
+        const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
+        const float p0 = j0 < nt ? expf(s0 - m_new) : 0.f, p1 = j0 + 1 < nt ? expf(s1 - m_new) : 0.f;
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l_run = l_run * alpha + ps;
+        m_run = m_new;
+        uint16_t h0, l0, h1, l1;
+        split_bf16(p0, h0, l0);
+        split_bf16(p1, h1, l1);
+        const uint32_t ah = uint32_t(h0) | (uint32_t(h1) << 16), al = uint32_t(l0) | (uint32_t(l1) << 16);
+        // P.V: B rows 2t, 2t + 1 are positions j0, j0 + 1 (rows 2t + 8, 2t + 9 meet
+        // zero columns of P); column g is dim 64 dg + 8d + g
+        const uint32_t col = uint32_t(64 * dg + g) * 2;
+        const uint32_t v0 = (j0 < n ? vbase + uint32_t(j0) * (HD * 2) : vnew) + col;
+        const uint32_t v1 = (j0 + 1 < n ? vbase + uint32_t(j0 + 1) * (HD * 2) : vnew) + col;
+#pragma unroll
+        for (int d = 0; d < 8; d++) {
+            const uint32_t b0 = uint32_t(lds_u16(v0 + d * 16)) | (uint32_t(lds_u16(v1 + d * 16)) << 16);
+            float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
+            mma_rows8(acc, ah, 0u, b0, 0u);
+            mma_rows8(acc, al, 0u, b0, 0u);
+            o[d][0] = acc[0];
+            o[d][1] = acc[1];
+        }
+    }
+}
+
+template <int DL>
+__device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
+    const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
+    constexpr int hd = DL * 32, half = hd / 2;
+    const int G = p.nq / p.nkv, tid = threadIdx.x;
+    const int qd = p.nq * hd, kd = p.nkv * hd;
+    const bool owner = c == S - 1;  // this split owns position pos
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    const float2 *cs = p.rope_cs + size_t(p.pos) * half;
+    const uint32_t tag = tag_of(p, l);
+    // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
+    // 1/sqrt(hd); the owner also rotates the new key and takes the new value
+    {
+        const uint64_t *qh = p.t_qkv + size_t(g * G) * hd;
+        const uint64_t *kh = p.t_qkv + qd + size_t(g) * hd;
+        const uint64_t *vh = p.t_qkv + qd + kd + size_t(g) * hd;
+        const bool has_q = tid < G * hd, has_k = owner && tid < half, has_v = owner && tid < hd;
+        const int h = tid / hd, d = tid % hd, i = d < half ? d : d - half;
+        uint64_t w[5];
+        poll_words(p, s, w, tag, [&](uint64_t (&ww)[5]) {
+            const uint64_t ok = static_cast<uint64_t>(tag) << 32;
+            ww[0] = has_q ? ld_tag(qh + size_t(h) * hd + i) : ok;
+            ww[1] = has_q ? ld_tag(qh + size_t(h) * hd + i + half) : ok;
+            ww[2] = has_k ? ld_tag(kh + tid) : ok;
+            ww[3] = has_k ? ld_tag(kh + tid + half) : ok;
+            ww[4] = has_v ? ld_tag(vh + tid) : ok;
+        });
+        if (has_q) {
+            const float a = tag_val(w[0]), b = tag_val(w[1]);
+            const float2 r = cs[i];
+            s.qr[h][d] = (d < half ? a * r.x - b * r.y : a * r.y + b * r.x) * scale;
+        }
+        if (has_k) {
+            const float a = tag_val(w[2]), b = tag_val(w[3]);
+            const float2 r = cs[tid];
+            s.knew[tid] = f_to_bf16(a * r.x - b * r.y);
+            s.knew[tid + half] = f_to_bf16(a * r.y + b * r.x);
+        }
+        if (has_v) s.vnew[tid] = f_to_bf16(tag_val(w[4]));
+    }
+    if (tid < G) {
+        s.m_run[tid] = -INFINITY;
+        s.l_run[tid] = 0.f;
+    }
+    // attn_page reads s.knew / s.vnew also as a stand-in row for positions past
+    // the last one (their probabilities are zero): make them finite everywhere
+    if (!owner)
+        for (int d = tid; d < hd; d += NCT) s.knew[d] = s.vnew[d] = 0;
+    if (consumer_any(s.abort)) return false;
+    // the queries as tensor-core A fragments, bf16 hi and lo: lane (g, t) of k-step
+    // ks holds head g at dims 16ks + 2t, +1 and 16ks + 2t + 8, +9 (0 past G heads)
+    for (int i = tid; i < (hd / 16) * 32; i += NCT) {
+        const int ks = i / 32, ln = i % 32, g = ln >> 2, t = ln & 3;
+        uint16_t h[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+        if (g < G) {
+            const int d[4] = {16 * ks + 2 * t, 16 * ks + 2 * t + 1, 16 * ks + 2 * t + 8, 16 * ks + 2 * t + 9};
+#pragma unroll
+            for (int e = 0; e < 4; e++) split_bf16(s.qr[g][d[e]], h[e], lo[e]);
+        }
+        s.qf[0][ks][ln][0] = uint32_t(h[0]) | (uint32_t(h[1]) << 16);
+        s.qf[0][ks][ln][1] = uint32_t(h[2]) | (uint32_t(h[3]) << 16);
+        s.qf[1][ks][ln][0] = uint32_t(lo[0]) | (uint32_t(lo[1]) << 16);
+        s.qf[1][ks][ln][1] = uint32_t(lo[2]) | (uint32_t(lo[3]) << 16);
+    }
+    consumer_sync();
+    if (tid == 0) trace_put(p, ii, 1);
+    if (owner) {
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
+        if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
+            for (int d = tid; d < hd; d += NCT) {
+                p.k_cache[at + d] = s.knew[d];
+                p.v_cache[at + d] = s.vnew[d];
+            }
+    }
+    // this lane's share of the running softmax and output (see attn_tiles)
+    float m_run = -INFINITY, l_run = 0.f, o[8][2];
+#pragma unroll
+    for (int d = 0; d < 8; d++) o[d][0] = o[d][1] = 0.f;
+    int c0, c1;
+    attn_range(p, c, c0, c1);
+    const int PP = attn_pp(p);
+    for (int p0 = c0; p0 < c1; p0 += PP) {
+        const int n = min(PP, c1 - p0);
+        const bool with_new = owner && p0 + PP >= c1;  // fold the new token into the last page
+        const uint32_t slot = cpage % NPAGES;
+        if (consumer_any(!wait_page(p, s, cpage))) return false;
+        if (tid == 0) {
+            ptrace_put(p, cpage, 1);
+            trace_put(p, ii, 6);
+        }
+        const uint32_t pg = smem_addr(pages + size_t(slot) * PAGE_BYTES);
+        attn_tiles<hd>(s, pg, pg + PAGE_BYTES / 2, n, with_new, m_run, l_run, o);  // V at half a page
+        consumer_sync();  // every warp is done with the page
+        if (tid == 0) {
+            ptrace_put(p, cpage, 2);
+            mbar_arrive(&s.empty[slot]);
+        }
+        ++cpage;
+    }
+    if (owner && c0 == c1) {
+        attn_tiles<hd>(s, 0u, 0u, 0, true, m_run, l_run, o);
+        consumer_sync();  // s.qf is read up to here; the merge below reuses its space
+    }
+    if (tid == 0) trace_put(p, ii, 7);
+
+    // merge the warps of each dim group pairwise, halving their number each round
+    constexpr int GW = NCW * 64 / hd;
+    const int warp = tid >> 5, dg = warp / GW, tw = warp % GW, gq = (tid & 31) >> 2, tq = tid & 3;
+    for (int half = GW / 2; half >= 1; half /= 2) {
+        if (tw >= half && tw < 2 * half && gq < G) {
+            float *sl = s.ared[dg * (GW / 2) + tw - half];
+#pragma unroll
+            for (int d = 0; d < 8; d++) {
+                sl[gq * 64 + 8 * d + 2 * tq] = o[d][0];
+                sl[gq * 64 + 8 * d + 2 * tq + 1] = o[d][1];
+            }
+            if (tq == 0) {
+                sl[512 + gq] = m_run;
+                sl[512 + MAX_GQA + gq] = l_run;
+            }
+        }
+        consumer_sync();
+        if (tw < half && gq < G) {
+            const float *sl = s.ared[dg * (GW / 2) + tw];
+            const float mo = sl[512 + gq], lo = sl[512 + MAX_GQA + gq];
+            const float M = fmaxf(m_run, mo);
+            const float wa = m_run == -INFINITY ? 0.f : expf(m_run - M), wb = mo == -INFINITY ? 0.f : expf(mo - M);
+            l_run = l_run * wa + lo * wb;
+            m_run = M;
+#pragma unroll
+            for (int d = 0; d < 8; d++) {
+                o[d][0] = o[d][0] * wa + sl[gq * 64 + 8 * d + 2 * tq] * wb;
+                o[d][1] = o[d][1] * wa + sl[gq * 64 + 8 * d + 2 * tq + 1] * wb;
+            }
+        }
+        consumer_sync();
+    }
+
+    // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}], from the
+    // first warp of every dim group
+    const int stride = hd + 4;
+    const uint32_t wtag = write_tag(p, ins);
+    if (tw == 0 && gq < G) {
+        uint64_t *dst = p.t_part + (size_t(g * G + gq) * S + c) * stride;
+#pragma unroll
+        for (int d = 0; d < 8; d++) {
+            st_tag(dst + 64 * dg + 8 * d + 2 * tq, o[d][0], wtag);
+            st_tag(dst + 64 * dg + 8 * d + 2 * tq + 1, o[d][1], wtag);
+        }
+        if (dg == 0 && tq == 0) {
+            st_tag(dst + hd, m_run, wtag);
+            st_tag(dst + hd + 1, l_run, wtag);
+        }
+    }
+    if (tid == 0) trace_put(p, ii, 2);
+    return merge_splits(p, s, g, c, G, hd, tag, wtag);
+}
+
+// FLASH: the kernel variant for long attention items (see attn_tiles); the other
+// variant keeps a block-wide softmax per page, cheaper when an item spans a page
+// or two. The host picks the variant by the longest item at max_seq.
+template <bool FLASH>
 __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
-    return p.hd == 64 ? attn_item<2>(p, s, pages, ins, ii, cpage) : attn_item<4>(p, s, pages, ins, ii, cpage);
+    if constexpr (FLASH)
+        return p.hd == 64 ? attn_item_flash<2>(p, s, pages, ins, ii, cpage)
+                          : attn_item_flash<4>(p, s, pages, ins, ii, cpage);
+    else
+        return p.hd == 64 ? attn_item<2>(p, s, pages, ins, ii, cpage) : attn_item<4>(p, s, pages, ins, ii, cpage);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1229,6 +1498,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     }
 }
 
+template <bool FLASH>
 __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
     const int n = p.n_instr[blockIdx.x];
@@ -1240,7 +1510,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
         if (threadIdx.x == 0) trace_put(p, i, 0);
         bool ok;
         if (ins.op == OP_ATTN) {
-            ok = attn_instr(p, s, pages, ins, i, cpage);
+            ok = attn_instr<FLASH>(p, s, pages, ins, i, cpage);
         } else {
             const MvShape &mv = mv_of(p, ins.op);
             switch (mv.vpl * 16 + mv.rw) {
@@ -1260,6 +1530,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     }
 }
 
+template <bool FLASH>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *pages = smem;
@@ -1293,26 +1564,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) producer(p, s, pages);
     } else {
-        consumer(p, s, pages);
+        consumer<FLASH>(p, s, pages);
     }
 }
 
 int megakernel_smem_bytes() { return SMEM_BYTES; }
 
 int megakernel_prepare(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes);
-    if (e != cudaSuccess) return LL_ERR_CUDA;
-    int blocks = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_megakernel, NTHREADS, smem_bytes);
-    if (e != cudaSuccess) return LL_ERR_CUDA;
-    return blocks >= 1 ? LL_OK : LL_ERR_DEVICE;
+    const void *fns[2] = {reinterpret_cast<const void *>(decode_megakernel<false>),
+                          reinterpret_cast<const void *>(decode_megakernel<true>)};
+    for (const void *fn : fns) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return LL_ERR_CUDA;
+        int blocks = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, NTHREADS, smem_bytes);
+        if (e != cudaSuccess) return LL_ERR_CUDA;
+        if (blocks < 1) return LL_ERR_DEVICE;
+    }
+    return LL_OK;
 }
 
 int launch_megakernel(const KParams &p, void *stream, int smem_bytes) {
     void *args[] = {const_cast<KParams *>(&p)};
-    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(decode_megakernel),
-                                                dim3(p.nsm), dim3(NTHREADS), args, size_t(smem_bytes),
+    const void *fn = p.attn_flash ? reinterpret_cast<const void *>(decode_megakernel<true>)
+                                  : reinterpret_cast<const void *>(decode_megakernel<false>);
+    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(p.nsm), dim3(NTHREADS), args, size_t(smem_bytes),
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }

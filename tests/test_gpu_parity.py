@@ -80,6 +80,25 @@ def test_head_layouts(shape, backend):
     pr.close()
 
 
+@pytest.mark.parametrize("shape", GQA_SHAPES + [synth.TINY], ids=lambda s: s.name)
+def test_per_warp_softmax_variant(shape, monkeypatch):
+    # the kernel variant that long attention items use (picked at init by the
+    # longest item), forced here on short ones: several pages per item, the new
+    # token folded in, and items with no cached positions (pos 0)
+    monkeypatch.setenv("LL_ATTN_FLASH", "1")
+    monkeypatch.setenv("LL_ATTN_SPLIT_POS", "256")
+    max_seq = 400
+    pr = Pair(shape, max_seq, ll.LL_BACKEND_MEGAKERNEL, kv_fill=390, gain_jitter=0.25)
+    tok = 3
+    for pos in (390, 391):
+        _, tok, _ = pr.step(tok, pos, what=f"{shape.name} pos {pos}")
+    pr.kv_close(slice(390, 392))
+    pr.close()
+    pr = Pair(shape, 8, ll.LL_BACKEND_MEGAKERNEL)
+    pr.step(5, 0, what=f"{shape.name} pos 0")
+    pr.close()
+
+
 def _full_size(key, backend, steps=2):
     wl = synth.WORKLOADS[key]
     shape, ctx = wl.shape, wl.context
