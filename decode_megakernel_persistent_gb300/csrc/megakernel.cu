@@ -1131,10 +1131,9 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
 
 // Attention over one page of n cached positions (K rows at kbase, V rows at vbase)
 // plus, if with_new, the new token (s.knew, s.vnew) at index n, for the group's G
-// query heads, as flash decoding within the block. The warps form HD / 64 dim
-// groups of NCW * 64 / HD warps; warp w (group dg, index tw) takes the 8-position
-// tiles tw, tw + group size, ... and keeps its own running softmax and its
-// group's 64 dims of O. Per tile: S = Q K^T on tensor cores (Q from its bf16
+// query heads, as flash decoding: the calling warp takes the 8-position tiles
+// tile0, tile0 + tstride, ... for the 64 dims of its dim group dg, keeping its
+// own running softmax across tiles and pages. Per tile: S = Q K^T on tensor cores (Q from its bf16
 // hi/lo fragments in s.qf, K straight from the page); the tile's maximum and sum
 // over the 4 lanes of each head; P = exp(S - m) split into bf16 hi/lo, which in
 // the m16n8k16 layouts is already the A fragment of the next product; O += P V
@@ -1142,13 +1141,13 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
 // its O at dims 64 dg + 8d + 2t, +1 for d < 8.
 template <int HD>
 __device__ __forceinline__ void attn_tiles(const Smem &s, uint32_t kbase, uint32_t vbase, int n, bool with_new,
-                                           float &m_run, float &l_run, float (&o)[8][2]) {
-    constexpr int KS = HD / 16, GW = NCW * 64 / HD;  // k-steps; warps per dim group
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int dg = warp / GW, tw = warp % GW;
+                                           float &m_run, float &l_run, float (&o)[8][2], int dg, int tile0,
+                                           int tstride) {
+    constexpr int KS = HD / 16;  // k-steps
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int nt = n + (with_new ? 1 : 0);
     const uint32_t knew = smem_addr(s.knew), vnew = smem_addr(s.vnew);
-    for (int tile = tw; tile * 8 < nt; tile += GW) {
+    for (int tile = tile0; tile * 8 < nt; tile += tstride) {
         // scores: column g of K^T is position tile * 8 + g (past the last one: a
         // finite stand-in row, masked below)
         const int jb = tile * 8 + g;
@@ -1280,28 +1279,43 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     int c0, c1;
     attn_range(p, c, c0, c1);
     const int PP = attn_pp(p);
-    for (int p0 = c0; p0 < c1; p0 += PP) {
+    // The warps form DG dim groups (64 dims each); within a dim group, NGR page
+    // groups of W warps each take every NGR-th page of the item, W warps sharing a
+    // page's tiles. So NGR pages are worked on at once and a warp's chain of tiles
+    // per page stays short; the last of a page's DG * W warps releases it.
+    constexpr int DG = hd / 64, GWD = NCW / DG, NGR = 4, W = GWD / NGR;
+    const int warp_i = tid >> 5, lane_i = tid & 31;
+    const int dgi = warp_i / GWD, pgq = (warp_i % GWD) / W, wi = warp_i % W;
+    bool bad = false;
+    int npg = 0;
+    for (int p0 = c0; p0 < c1; p0 += PP, npg++) {
+        const uint32_t page = cpage + uint32_t(npg), slot = page % NPAGES;
+        if (npg % NGR != pgq) continue;
         const int n = min(PP, c1 - p0);
         const bool with_new = owner && p0 + PP >= c1;  // fold the new token into the last page
-        const uint32_t slot = cpage % NPAGES;
-        if (consumer_any(!wait_page(p, s, cpage))) return false;
-        if (tid == 0) {
-            ptrace_put(p, cpage, 1);
-            trace_put(p, ii, 6);
+        bool okp = !bad;
+        if (lane_i == 0 && okp) okp = wait_page(p, s, page);
+        okp = __shfl_sync(0xffffffffu, okp, 0);
+        if (!okp) {
+            bad = true;
+            continue;
         }
         const uint32_t pg = smem_addr(pages + size_t(slot) * PAGE_BYTES);
-        attn_tiles<hd>(s, pg, pg + PAGE_BYTES / 2, n, with_new, m_run, l_run, o);  // V at half a page
-        consumer_sync();  // every warp is done with the page
-        if (tid == 0) {
-            ptrace_put(p, cpage, 2);
-            mbar_arrive(&s.empty[slot]);
+        attn_tiles<hd>(s, pg, pg + PAGE_BYTES / 2, n, with_new, m_run, l_run, o, dgi, wi, W);  // V at half a page
+        __syncwarp();
+        if (lane_i == 0) {
+            __threadfence_block();
+            if (atomicAdd(&s.pcnt[slot], 1) == DG * W - 1) {
+                s.pcnt[slot] = 0;
+                ptrace_put(p, page, 2);
+                mbar_arrive(&s.empty[slot]);
+            }
         }
-        ++cpage;
     }
-    if (owner && c0 == c1) {
-        attn_tiles<hd>(s, 0u, 0u, 0, true, m_run, l_run, o);
-        consumer_sync();  // s.qf is read up to here; the merge below reuses its space
-    }
+    cpage += uint32_t(npg);
+    if (consumer_any(bad)) return false;
+    if (owner && c0 == c1 && pgq == 0) attn_tiles<hd>(s, 0u, 0u, 0, true, m_run, l_run, o, dgi, wi, W);
+    consumer_sync();  // s.qf is read up to here; the merge below reuses its space
     if (tid == 0) trace_put(p, ii, 7);
 
     // merge the warps of each dim group pairwise, halving their number each round
