@@ -1,6 +1,7 @@
 // api.cpp -- the C ABI of libll.so (declared in include/ll.h): argument and
 // shape checks, library memory, the RoPE table, schedule upload, launches and
 // status handling.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder itself is fetched from the driver)
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -67,6 +68,42 @@ int upload_schedule(ll_handle *h) {
 
 // KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
 // longest context, at most one attention item per SM.
+// The KV tensor maps of the per-warp attention variant (ll::TM_*): each cache as
+// a 2-D bf16 tensor of head_dim columns and L * n_kv * max_seq rows, boxes of 64
+// columns (128 bytes, the widest the 128-byte swizzle takes) by a page of rows or
+// by one 16-row tile. False if the driver has no encoder or the rows do not fit
+// the 32-bit signed coordinates of a copy.
+bool encode_kv_maps(const ll_config &c, uint16_t *k_cache, uint16_t *v_cache, ll::TensorMap (&out)[ll::TM_COUNT]) {
+    using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static_assert(sizeof(CUtensorMap) == sizeof(ll::TensorMap), "tensor map size");
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    const auto encode = reinterpret_cast<EncodeTiled>(fn);
+    const uint64_t rows = uint64_t(c.n_layers) * uint64_t(c.n_kv_heads) * uint64_t(c.max_seq);
+    if (rows + ll::PAGE_BYTES >= (1ull << 31)) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(c.head_dim), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(c.head_dim) * 2};
+    const cuuint32_t page_rows = ll::PAGE_BYTES / (4 * c.head_dim), estr[2] = {1, 1};
+    for (int i = 0; i < ll::TM_COUNT; i++) {
+        const bool tile = i == ll::TM_K_TILE || i == ll::TM_V_TILE;
+        const cuuint32_t box[2] = {64, tile ? cuuint32_t(ll::ATT_TILE) : page_rows};
+        CUtensorMap m;
+        if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i < ll::TM_V_PAGE ? k_cache : v_cache, dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+        std::memcpy(&out[i], &m, sizeof m);
+    }
+    return true;
+}
+
 int attn_splits(const ll_config &c, int nsm) {
     int per = ll::ATTN_SPLIT_POS;  // tuning knob (environment), read at init
     if (const char *e = std::getenv("LL_ATTN_SPLIT_POS")) per = std::max(1, std::atoi(e));
@@ -316,16 +353,19 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.eps = c.rms_eps;
     p.attn_splits = h->splits;
     {
-        // kernel variant: per-warp (flash) softmax when the longest attention item
-        // at max_seq spans at least 10 pages. Its merge of the warps costs ~1.5 us
-        // per item and its variant of the kernel runs the matrix-vector products a
-        // little slower, so it pays off only where attention dominates (measured:
-        // 1B at 32k context -10 %, 8B at 8k with 7-page items +9 %). Tuning knob
-        // LL_ATTN_FLASH = 0 / 1 overrides.
+        // kernel variant: per-warp (flash) softmax on tensor cores when the longest
+        // attention item at max_seq spans at least 4 pages. Its merge of the warps
+        // costs ~1.5 us per item, so on items of one or two pages the block-wide
+        // pass is faster (measured: 1B at 1k context, 1-page items: 656 against
+        // 683 us; 3B at 2k, 2-page items: 1631 against 1652 us; 8B at 8k, 7-page
+        // items: 3224 against 3433 us; 1B at 32k, 14-page items: 869 against
+        // 1148 us). Tuning knob LL_ATTN_FLASH = 0 / 1 overrides.
         const int per_split = (c.max_seq + h->splits - 1) / h->splits;
         const int pp = ll::PAGE_BYTES / (4 * c.head_dim);
-        p.attn_flash = (per_split + pp - 1) / pp >= 10 ? 1 : 0;
+        p.attn_flash = (per_split + pp - 1) / pp >= 4 ? 1 : 0;
         if (const char *e = std::getenv("LL_ATTN_FLASH")) p.attn_flash = std::atoi(e) ? 1 : 0;
+        // its KV pages come through TMA tensor maps; without them, the block variant
+        if (!encode_kv_maps(c, k_cache, v_cache, p.kv_maps)) p.attn_flash = 0;
     }
     p.mv_h = mh;
     p.mv_q = mq;

@@ -71,6 +71,17 @@ struct PDesc {
 };
 enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1 };
 
+// A TMA tensor map (CUtensorMap: 128 opaque bytes, 64-byte aligned), kept as
+// bytes here so that this header needs no driver API types.
+struct alignas(64) TensorMap {
+    unsigned char bytes[128];
+};
+// KV tensor maps of the per-warp attention variant: the K or V cache as a 2-D
+// tensor (head_dim, L * n_kv * max_seq rows), 64-dim boxes with the 128-byte
+// swizzle; box height a whole page of positions or one 16-position tile.
+enum : int { TM_K_PAGE = 0, TM_K_TILE = 1, TM_V_PAGE = 2, TM_V_TILE = 3, TM_COUNT = 4 };
+constexpr int ATT_TILE = 16;  // positions per tensor-core attention tile
+
 struct LayerW {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
 };
@@ -90,6 +101,7 @@ struct CtrLayout {
 };
 
 struct KParams {
+    TensorMap kv_maps[TM_COUNT];  // (TM_*) used by the per-warp attention variant
     // schedule
     const Instr *instrs;      // [nsm][max_instr]
     const int32_t *n_instr;   // [nsm]

@@ -212,7 +212,7 @@ struct alignas(16) Smem {
             float sc[MAX_GQA][132];             // scores of up to 129 positions
             float pt[132][MAX_GQA];             // their probabilities, position-major
         };
-        uint32_t qf[2][MAX_HD / 16][32][2];  // attention, per-warp softmax: query MMA fragments (bf16 hi, lo)
+        uint4 qf[MAX_HD / 16][32];           // attention, per-warp softmax: query MMA A fragments (hi, lo rows)
         float ared[NCW / 2][AT_SLOT];        // attention, per-warp softmax: (o, m, l) of warps being merged
     };
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
@@ -223,6 +223,7 @@ struct alignas(16) Smem {
     float qr[MAX_GQA][MAX_HD];  // the attention item's rotated, scaled query heads
     alignas(16) uint16_t knew[MAX_HD];
     alignas(16) uint16_t vnew[MAX_HD];
+    alignas(16) uint16_t zrow[64];  // zeros: the K / V row read for positions past a page's end
     float m_run[MAX_GQA], l_run[MAX_GQA], alpha[MAX_GQA];
     float xown[XOWN_MAX];  // this SM's rows of the residual stream (the O and down rows)
     LayerW lw[SMEM_LAYERS];  // weight pointers of the first SMEM_LAYERS layers, copied at kernel start
@@ -1116,6 +1117,37 @@ __device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
+// D += A * B, m16n8k16, all four A registers: a0 = (row g, cols 2t, 2t + 1),
+// a1 = (row g + 8, same cols), a2 = (row g, cols 2t + 8, 2t + 9), a3 = (row g + 8,
+// those cols); D: d0, d1 = row g, d2, d3 = row g + 8, at cols 2t, 2t + 1.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 bf16 matrices from shared memory: lanes 8i .. 8i + 7 give the row
+// addresses of matrix i; lane (g, t) receives row g, elements 2t, 2t + 1 of each
+// (trans: element rows 2t, 2t + 1 of column g).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -1129,71 +1161,111 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
     lo = f_to_bf16(x - bf16_to_f(hi));
 }
 
-// Attention over one page of n cached positions (K rows at kbase, V rows at vbase)
-// plus, if with_new, the new token (s.knew, s.vnew) at index n, for the group's G
-// query heads, as flash decoding: the calling warp takes the 8-position tiles
-// tile0, tile0 + tstride, ... for the 64 dims of its dim group dg, keeping its
-// own running softmax across tiles and pages. Per tile: S = Q K^T on tensor cores (Q from its bf16
-// hi/lo fragments in s.qf, K straight from the page); the tile's maximum and sum
-// over the 4 lanes of each head; P = exp(S - m) split into bf16 hi/lo, which in
-// the m16n8k16 layouts is already the A fragment of the next product; O += P V
-// with V straight from the page. Lane (g, t) keeps head g's running m and l and
-// its O at dims 64 dg + 8d + 2t, +1 for d < 8.
+// Attention over one page of n cached positions plus, if with_new, the new token
+// (s.knew, s.vnew) at index n, for the group's G query heads, as flash decoding:
+// the calling warp takes the 16-position tiles tile0, tile0 + tstride, ... for the
+// 64 dims of its dim group dg, keeping its own running softmax across tiles and
+// pages. The page holds K at kbase and V at vbase, each as [dim half][position]
+// [64 dims] with PP positions per half and 128-byte rows in the TMA 128-byte
+// swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), so that the eight rows
+// of an ldmatrix fall in eight different bank groups.
+//
+// The query heads' fp32 values enter as two bf16 terms, hi in rows 0..7 of the
+// A operand and lo in rows 8..15 (a KV head has at most 8 query heads), so one
+// m16n8k16 product yields both and their sum is exact to ~16 bits. Per tile:
+// S = Q K^T (K^T as B, 8 positions per product, two products per k-step); the
+// tile's maximum and sum over the 4 lanes of each head; P = exp(S - m), split the
+// same way into hi (rows g) and lo (rows g + 8), which in the m16n8k16 layouts
+// is already the A fragment of O += P V (V as B, 16 positions by 8 dims per
+// product). Positions past the page's end read s.zrow (zero K and V), the new
+// token's position reads s.knew / s.vnew. Lane (g, t) keeps head g's running m
+// and l and its O at dims 64 dg + 8d + 2t, +1 for d < 8.
 template <int HD>
 __device__ __forceinline__ void attn_tiles(const Smem &s, uint32_t kbase, uint32_t vbase, int n, bool with_new,
                                            float &m_run, float &l_run, float (&o)[8][2], int dg, int tile0,
-                                           int tstride) {
+                                           int tstride, int PP) {
     constexpr int KS = HD / 16;  // k-steps
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int lane = threadIdx.x & 31, t = lane & 3, mi = lane >> 3, r = lane & 7;
     const int nt = n + (with_new ? 1 : 0);
-    const uint32_t knew = smem_addr(s.knew), vnew = smem_addr(s.vnew);
-    for (int tile = tile0; tile * 8 < nt; tile += tstride) {
-        // scores: column g of K^T is position tile * 8 + g (past the last one: a
-        // finite stand-in row, masked below)
-        const int jb = tile * 8 + g;
-        const uint32_t krow = jb < n ? kbase + uint32_t(jb) * (HD * 2) : knew;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t qa = smem_addr(&s.qf[0][0][lane][0]);  // (volatile loads: not kept across tiles)
-        constexpr uint32_t QHL = sizeof(s.qf[0]), QKS = sizeof(s.qf[0][0]);
+    const uint32_t half_bytes = uint32_t(PP) * 128u;
+    for (int tile = tile0; tile * ATT_TILE < nt; tile += tstride) {
+        const int j0 = tile * ATT_TILE;
+        // this lane's ldmatrix row for K: position jk, 16-byte chunk 2 (ks % 4) + (mi & 1)
+        // of dim half ks / 4; for V: position jv, chunk 2 dd + (mi >> 1) of half dg
+        uint32_t krow, kh, kx, vrow, vx;
+        {
+            const int jk = j0 + 8 * (mi >> 1) + r;
+            if (jk < n) {
+                krow = kbase + uint32_t(jk) * 128u, kh = half_bytes, kx = uint32_t(jk & 7);
+            } else if (with_new && jk == n) {
+                krow = smem_addr(s.knew), kh = 128u, kx = 0u;
+            } else {
+                krow = smem_addr(s.zrow), kh = 0u, kx = 0u;
+            }
+            const int jv = j0 + 8 * (mi & 1) + r;
+            if (jv < n) {
+                vrow = vbase + uint32_t(dg) * half_bytes + uint32_t(jv) * 128u, vx = uint32_t(jv & 7);
+            } else if (with_new && jv == n) {
+                vrow = smem_addr(s.vnew) + uint32_t(dg) * 128u, vx = 0u;
+            } else {
+                vrow = smem_addr(s.zrow), vx = 0u;
+            }
+        }
+        // scores: c[nb] covers positions j0 + 8 nb .. + 7 (columns), hi / lo rows
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const uint4 *qa = &s.qf[0][lane];
 #pragma unroll
         for (int ks = 0; ks < KS; ks++) {
-            const uint32_t b0 = lds_u32(krow + (16 * ks + 2 * t) * 2);
-            const uint32_t b1 = lds_u32(krow + (16 * ks + 2 * t + 8) * 2);
-            const uint32_t qh = qa + ks * QKS, ql = qh + QHL;
-            mma_rows8(c, lds_u32(qh), lds_u32(qh + 4), b0, b1);
-            mma_rows8(c, lds_u32(ql), lds_u32(ql + 4), b0, b1);
+            uint32_t b[4];
+            const uint32_t ch = uint32_t(2 * (ks & 3) + (mi & 1));
+            ldsm_x4(krow + uint32_t(ks >> 2) * kh + ((ch ^ kx) << 4), b);
+            const uint4 a = lds_v4(smem_addr(qa + ks * 32));  // (volatile: not kept across tiles)
+            mma_16816(c[0], a, b[0], b[1]);
+            mma_16816(c[1], a, b[2], b[3]);
         }
-        // this lane: head g at positions j0 = tile * 8 + 2t and j0 + 1
-        const int j0 = tile * 8 + 2 * t;
-        const float s0 = j0 < nt ? c[0] : -INFINITY, s1 = j0 + 1 < nt ? c[1] : -INFINITY;
-        float mt = fmaxf(s0, s1);
+        // this lane: head g at positions j0 + 2t, +1 (c[0]) and j0 + 8 + 2t, +1 (c[1])
+        float sc[4];
+#pragma unroll
+        for (int nb = 0; nb < 2; nb++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int j = j0 + 8 * nb + 2 * t + e;
+                sc[2 * nb + e] = j < nt ? c[nb][e] + c[nb][e + 2] : -INFINITY;
+            }
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-        const float m_new = fmaxf(m_run, mt);  // finite: position tile * 8 exists
+        const float m_new = fmaxf(m_run, mt);  // finite: position j0 exists
         const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
-        const float p0 = j0 < nt ? expf(s0 - m_new) : 0.f, p1 = j0 + 1 < nt ? expf(s1 - m_new) : 0.f;
-        float ps = p0 + p1;
+        float pr[4], ps = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
+            ps += pr[e];
+        }
         ps += __shfl_xor_sync(0xffffffffu, ps, 1);
         ps += __shfl_xor_sync(0xffffffffu, ps, 2);
         l_run = l_run * alpha + ps;
         m_run = m_new;
-        uint16_t h0, l0, h1, l1;
-        split_bf16(p0, h0, l0);
-        split_bf16(p1, h1, l1);
-        const uint32_t ah = uint32_t(h0) | (uint32_t(h1) << 16), al = uint32_t(l0) | (uint32_t(l1) << 16);
-        // P.V: B rows 2t, 2t + 1 are positions j0, j0 + 1 (rows 2t + 8, 2t + 9 meet
-        // zero columns of P); column g is dim 64 dg + 8d + g
-        const uint32_t col = uint32_t(64 * dg + g) * 2;
-        const uint32_t v0 = (j0 < n ? vbase + uint32_t(j0) * (HD * 2) : vnew) + col;
-        const uint32_t v1 = (j0 + 1 < n ? vbase + uint32_t(j0 + 1) * (HD * 2) : vnew) + col;
+        uint16_t h[4], lo[4];
 #pragma unroll
-        for (int d = 0; d < 8; d++) {
-            const uint32_t b0 = uint32_t(lds_u16(v0 + d * 16)) | (uint32_t(lds_u16(v1 + d * 16)) << 16);
-            float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
-            mma_rows8(acc, ah, 0u, b0, 0u);
-            mma_rows8(acc, al, 0u, b0, 0u);
-            o[d][0] = acc[0];
-            o[d][1] = acc[1];
+        for (int e = 0; e < 4; e++) split_bf16(pr[e], h[e], lo[e]);
+        const uint4 pa = make_uint4(uint32_t(h[0]) | (uint32_t(h[1]) << 16), uint32_t(lo[0]) | (uint32_t(lo[1]) << 16),
+                                    uint32_t(h[2]) | (uint32_t(h[3]) << 16), uint32_t(lo[2]) | (uint32_t(lo[3]) << 16));
+        // P.V: 8 dims per product, two products per ldmatrix
+#pragma unroll
+        for (int dd = 0; dd < 4; dd++) {
+            uint32_t b[4];
+            const uint32_t ch = uint32_t(2 * dd + (mi >> 1));
+            ldsm_x4_t(vrow + ((ch ^ vx) << 4), b);
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int d = 2 * dd + u;
+                float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
+                mma_16816(acc, pa, b[2 * u], b[2 * u + 1]);
+                o[d][0] = acc[0] + acc[2];
+                o[d][1] = acc[1] + acc[3];
+            }
         }
     }
 }
@@ -1242,13 +1314,10 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
         s.m_run[tid] = -INFINITY;
         s.l_run[tid] = 0.f;
     }
-    // attn_page reads s.knew / s.vnew also as a stand-in row for positions past
-    // the last one (their probabilities are zero): make them finite everywhere
-    if (!owner)
-        for (int d = tid; d < hd; d += NCT) s.knew[d] = s.vnew[d] = 0;
     if (consumer_any(s.abort)) return false;
-    // the queries as tensor-core A fragments, bf16 hi and lo: lane (g, t) of k-step
-    // ks holds head g at dims 16ks + 2t, +1 and 16ks + 2t + 8, +9 (0 past G heads)
+    // the queries as tensor-core A fragments: lane (g, t) of k-step ks holds head g
+    // at dims 16ks + 2t, +1 (x: bf16 hi, y: lo) and 16ks + 2t + 8, +9 (z: hi, w: lo),
+    // zero past G heads
     for (int i = tid; i < (hd / 16) * 32; i += NCT) {
         const int ks = i / 32, ln = i % 32, g = ln >> 2, t = ln & 3;
         uint16_t h[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
@@ -1257,10 +1326,8 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
 #pragma unroll
             for (int e = 0; e < 4; e++) split_bf16(s.qr[g][d[e]], h[e], lo[e]);
         }
-        s.qf[0][ks][ln][0] = uint32_t(h[0]) | (uint32_t(h[1]) << 16);
-        s.qf[0][ks][ln][1] = uint32_t(h[2]) | (uint32_t(h[3]) << 16);
-        s.qf[1][ks][ln][0] = uint32_t(lo[0]) | (uint32_t(lo[1]) << 16);
-        s.qf[1][ks][ln][1] = uint32_t(lo[2]) | (uint32_t(lo[3]) << 16);
+        s.qf[ks][ln] = make_uint4(uint32_t(h[0]) | (uint32_t(h[1]) << 16), uint32_t(lo[0]) | (uint32_t(lo[1]) << 16),
+                                  uint32_t(h[2]) | (uint32_t(h[3]) << 16), uint32_t(lo[2]) | (uint32_t(lo[3]) << 16));
     }
     consumer_sync();
     if (tid == 0) trace_put(p, ii, 1);
@@ -1301,7 +1368,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
             continue;
         }
         const uint32_t pg = smem_addr(pages + size_t(slot) * PAGE_BYTES);
-        attn_tiles<hd>(s, pg, pg + PAGE_BYTES / 2, n, with_new, m_run, l_run, o, dgi, wi, W);  // V at half a page
+        attn_tiles<hd>(s, pg, pg + PAGE_BYTES / 2, n, with_new, m_run, l_run, o, dgi, wi, W, PP);  // V at half a page
         __syncwarp();
         if (lane_i == 0) {
             __threadfence_block();
@@ -1314,7 +1381,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     }
     cpage += uint32_t(npg);
     if (consumer_any(bad)) return false;
-    if (owner && c0 == c1 && pgq == 0) attn_tiles<hd>(s, 0u, 0u, 0, true, m_run, l_run, o, dgi, wi, W);
+    if (owner && c0 == c1 && pgq == 0) attn_tiles<hd>(s, 0u, 0u, 0, true, m_run, l_run, o, dgi, wi, W, PP);
     consumer_sync();  // s.qf is read up to here; the merge below reuses its space
     if (tid == 0) trace_put(p, ii, 7);
 
@@ -1403,10 +1470,21 @@ __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint3
         : "memory");
 }
 
+// TMA tensor copy of one box of a 2-D tensor map (coordinates: x the inner
+// element index, a multiple of 64 here; y the row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst, const TensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // The producer thread walks its SM's host-built page list (weight pages with
 // their addresses, attention items expanded from pos here), so that issuing a
 // page costs it only a few instructions: it shares its scheduler with consumer
 // warps and gets a small share of the issue slots.
+template <bool FLASH>
 __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     const PDesc *dl = p.pdesc + p.pdesc_off[blockIdx.x];
     const int nd = p.pdesc_off[blockIdx.x + 1] - p.pdesc_off[blockIdx.x];
@@ -1421,26 +1499,35 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     const uint32_t lim = p.max_inflight >= 1 && p.max_inflight < NPAGES ? p.max_inflight : NPAGES;
     for (int di = 0; di < nd && ok; di++) {
         const PDesc e = dl[di];
-        int a_c0 = 0, a_c1 = 1, a_p0 = 0;
-        size_t head_base = 0;
+        int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
+        size_t head_row = 0;
         if (e.kind == PD_ATTN) {
             const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
             attn_range(p, c, a_c0, a_c1);
             a_p0 = a_c0;
-            head_base = (size_t(layer) * p.nkv + g) * size_t(p.max_seq) * p.hd;
+            head_row = (size_t(layer) * p.nkv + g) * size_t(p.max_seq);
             if (a_c0 >= a_c1) continue;  // empty split: no pages
         }
         // weight entries are one page; attention entries one page per PP positions
         while (ok) {
             const void *src0, *src1 = nullptr;
             uint32_t b0, b1 = 0;
+            int a_row = 0;
             if (e.kind == PD_ATTN) {
                 if (a_p0 >= a_c1) break;
-                const int n = min(PP, a_c1 - a_p0);
-                b0 = b1 = uint32_t(n) * p.hd * 2;
-                src0 = p.k_cache + head_base + size_t(a_p0) * p.hd;
-                src1 = p.v_cache + head_base + size_t(a_p0) * p.hd;
-                a_p0 += n;
+                a_n = min(PP, a_c1 - a_p0);
+                a_row = int(head_row) + a_p0;
+                if (FLASH) {
+                    // K and V through the tensor maps: whole page, or 16-row tiles
+                    const uint32_t tiles = uint32_t(a_n + ATT_TILE - 1) / ATT_TILE;
+                    b0 = b1 = a_n == PP ? uint32_t(PAGE_BYTES / 2) : tiles * uint32_t(p.hd / 64) * ATT_TILE * 128u;
+                    src0 = src1 = nullptr;
+                } else {
+                    b0 = b1 = uint32_t(a_n) * p.hd * 2;
+                    src0 = p.k_cache + (head_row + size_t(a_p0)) * p.hd;
+                    src1 = p.v_cache + (head_row + size_t(a_p0)) * p.hd;
+                }
+                a_p0 += a_n;
             } else {
                 src0 = reinterpret_cast<const void *>(e.src);
                 b0 = e.bytes;
@@ -1483,9 +1570,25 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
             ptrace_put(p, ppage, 0);
             s.slot_page[slot] = ppage;
             mbar_expect_tx(&s.full[slot], b0 + b1);
-            if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
-            else bulk_load(dst, src0, b0, &s.full[slot]);
-            if (b1) bulk_load(dst + PAGE_BYTES / 2, src1, b1, &s.full[slot]);
+            if (FLASH && e.kind == PD_ATTN) {
+                // [K | V] x [dim half] x [positions] x 64 dims, swizzled (see attn_tiles)
+                const int dh = p.hd / 64;
+                for (int kv = 0; kv < 2; kv++)
+                    for (int h = 0; h < dh; h++) {
+                        uint8_t *d = dst + kv * (PAGE_BYTES / 2) + h * PP * 128;
+                        if (a_n == PP) {
+                            tma_load_2d(d, &p.kv_maps[kv ? TM_V_PAGE : TM_K_PAGE], 64 * h, a_row, &s.full[slot]);
+                        } else {
+                            for (int j = 0; j < a_n; j += ATT_TILE)
+                                tma_load_2d(d + j * 128, &p.kv_maps[kv ? TM_V_TILE : TM_K_TILE], 64 * h, a_row + j,
+                                            &s.full[slot]);
+                        }
+                    }
+            } else {
+                if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
+                else bulk_load(dst, src0, b0, &s.full[slot]);
+                if (b1) bulk_load(dst + PAGE_BYTES / 2, src1, b1, &s.full[slot]);
+            }
             if (int(e.instr) != last_instr) {
                 trace_put(p, e.instr, 4);
                 last_instr = e.instr;
@@ -1561,7 +1664,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         s.flag = 0;
         s.token = p.token_dev ? *p.token_dev : p.token;
         s.start_status = ld_relaxed(p.status);
+        // the swizzled KV pages of the per-warp attention need 1024-byte aligned slots
+        if (FLASH && (smem_addr(pages) & 1023u) != 0) {
+            atomicCAS(p.status, 0, LL_ERR_DEVICE);
+            s.start_status = LL_ERR_DEVICE;
+        }
     }
+    if (threadIdx.x < 32) reinterpret_cast<uint32_t *>(s.zrow)[threadIdx.x] = 0u;
     {
         const int nl = p.L < SMEM_LAYERS ? p.L : SMEM_LAYERS;
         constexpr int WORDS = sizeof(LayerW) / 8;
@@ -1576,7 +1685,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         return;
     }
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) producer(p, s, pages);
+        if (threadIdx.x == NCT) producer<FLASH>(p, s, pages);
     } else {
         consumer<FLASH>(p, s, pages);
     }
