@@ -194,7 +194,14 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         return bad(LL_ERR_ARG, "unknown backend");
     if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return bad(LL_ERR_ARG, "rms_eps/rope_theta invalid");
     ll::MvShape mh{}, mq{}, mi{};
-    if (!ll::mv_shape(c.hidden, mh) || !ll::mv_shape(c.n_q_heads * c.head_dim, mq) || !ll::mv_shape(c.inter, mi))
+    // Input floats a lane may hold per team copy of a matvec input (tuning knob
+    // LL_MV_LANE_FLOATS, 16 or 32). 32 allows more teams, so more pages in
+    // progress at once: measured 1B 673 -> 656 us, 3B 1715 -> 1630 us, 8B 3270 ->
+    // 3225 us, 1B at 32k 891 -> 872 us (same box, back to back).
+    int lane_floats = 32;
+    if (const char *e = std::getenv("LL_MV_LANE_FLOATS")) lane_floats = std::atoi(e) == 16 ? 16 : 32;
+    if (!ll::mv_shape(c.hidden, mh, lane_floats) || !ll::mv_shape(c.n_q_heads * c.head_dim, mq, lane_floats) ||
+        !ll::mv_shape(c.inter, mi, lane_floats))
         return bad(LL_ERR_SHAPE, "hidden, n_q_heads*head_dim and inter must be multiples of 256, at most 16384");
     // ---- pointer checks
     if (!aligned16(k_cache) || !aligned16(v_cache)) return bad(LL_ERR_ARG, "KV caches must be 16-byte aligned");

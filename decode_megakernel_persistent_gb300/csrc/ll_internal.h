@@ -172,7 +172,9 @@ int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
 // Host-side schedule construction (schedule.cpp).
 void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm, int splits,
                     std::vector<std::vector<Instr>> &lists);
-bool mv_shape(int K, MvShape &m);
+// lane_floats: the most input floats a lane may hold per team copy of the
+// input (16 or 32); more allows more teams (pages in progress at once).
+bool mv_shape(int K, MvShape &m, int lane_floats = 16);
 void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector<LayerW> &layers,
                  const uint16_t *lm_head, int H, int qd, int kd, int I, const MvShape &mh, const MvShape &mq,
                  const MvShape &mi, std::vector<PDesc> &out, std::vector<int32_t> &off);

@@ -83,12 +83,12 @@ static bool mv_combo_ok(int vpl, int rw) {
     return false;
 }
 
-bool mv_shape(int K, MvShape &m) {
+bool mv_shape(int K, MvShape &m, int lane_floats) {
     if (K <= 0 || K % 256 != 0 || K > 16384) return false;
     const int rows_fit = PAGE_BYTES / (2 * K);
     if (rows_fit < 1) return false;
     int teams = 1;
-    while (teams < 4 && K * teams * 2 <= 32 * 32 * NCW) teams *= 2;
+    while (teams < 4 && K * teams * 2 <= lane_floats * 32 * NCW) teams *= 2;
     const int W = NCW / teams;
     int best_active = 0, best_rpp = 0;
     for (int vpl = 1; vpl <= MAX_VPL; vpl++) {
