@@ -52,10 +52,11 @@ struct Instr {
 // Matrix-vector geometry for one input width K. The consumer warps form `teams`
 // teams of NCW / teams warps; page number p of the SM goes to team p % teams, so
 // several pages are worked on at once. A page holds rpp whole rows. Within a
-// team the row is cut into ws k-slices of 256*vpl elements; team warp w works on
-// slice w % ws of rows w / ws + q * rg (q < rw) of each of its pages, so ws * rg
-// warps of the team are active and each lane keeps vpl 16-byte vectors of the
-// input in registers.
+// team the row is cut into ws k-slices of vpl groups of 256 elements, the groups
+// of the slices interleaved (slice sw has groups sw, sw + ws, ...); team warp w
+// works on slice w % ws of rows w / ws + q * rg (q < rw) of each of its pages,
+// so ws * rg warps of the team are active and each lane keeps vpl 16-byte
+// vectors of the input in registers.
 struct MvShape {
     int32_t K, ws, vpl, rpp, rg, rw, teams;
 };
