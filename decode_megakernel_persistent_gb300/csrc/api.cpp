@@ -133,9 +133,12 @@ int reset_device_state(ll_handle *h) {
 }
 
 int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, float *logits,
-            int32_t *next_token_dev) {
+            int32_t *next_token_dev, int32_t n_steps = 1, int32_t *tokens_dev = nullptr) {
     if (pos < 0 || pos >= h->cfg.max_seq)
         return fail(h, LL_ERR_ARG, "pos " + std::to_string(pos) + " outside [0, max_seq)");
+    if (n_steps < 1 || int64_t(pos) + n_steps > h->cfg.max_seq)
+        return fail(h, LL_ERR_ARG, "steps " + std::to_string(pos) + ".." + std::to_string(int64_t(pos) + n_steps - 1) +
+                                       " outside [0, max_seq)");
     if (logits && !aligned16(logits)) return fail(h, LL_ERR_ARG, "logits buffer not 16-byte aligned");
     KParams p = h->kp;
     p.token = token;
@@ -143,10 +146,30 @@ int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, 
     p.pos = pos;
     p.logits = logits;
     p.next_token_dev = next_token_dev;
-    p.epoch = ++h->epoch;
+    p.n_steps = n_steps;
+    p.tokens_dev = tokens_dev;
+    p.epoch = h->epoch + 1;
+    h->epoch += static_cast<uint32_t>(n_steps);
     int rc;
-    if (h->cfg.backend == LL_BACKEND_CHAIN) rc = ll::launch_chain_step(p, h->cb, h->stream);
-    else rc = ll::launch_megakernel(p, h->stream, h->smem_bytes);
+    if (h->cfg.backend == LL_BACKEND_CHAIN) {
+        // one launch sequence per step: step i reads step i - 1's token from tokens_dev
+        rc = LL_OK;
+        for (int32_t i = 0; i < n_steps && rc == LL_OK; i++) {
+            KParams q = p;
+            q.n_steps = 1;
+            q.tokens_dev = nullptr;
+            q.pos = pos + i;
+            q.epoch = p.epoch + static_cast<uint32_t>(i);
+            if (tokens_dev) {
+                q.token_dev = i == 0 ? token_dev : tokens_dev + (i - 1);
+                q.next_token_dev = tokens_dev + i;
+            }
+            if (logits) q.logits = logits + size_t(i) * size_t(h->cfg.vocab);
+            rc = ll::launch_chain_step(q, h->cb, h->stream);
+        }
+    } else {
+        rc = ll::launch_megakernel(p, h->stream, h->smem_bytes);
+    }
     if (rc != LL_OK) {
         cudaError_t e = cudaGetLastError();
         return fail(h, rc, std::string("kernel launch failed: ") + cudaGetErrorString(e));
@@ -274,7 +297,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     int32_t *status = nullptr, *tok = nullptr;
     long long *dbg = nullptr;
     uint64_t *t_qkv = nullptr, *t_part = nullptr, *t_o = nullptr, *t_xmid = nullptr, *t_act = nullptr,
-             *t_xout = nullptr;
+             *t_xout = nullptr, *t_token = nullptr;
     const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 4);
     Piece pieces[] = {
         {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
@@ -304,6 +327,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&t_xmid), size_t(c.hidden) * 8},
         {reinterpret_cast<void **>(&t_act), size_t(c.inter) * 8},
         {reinterpret_cast<void **>(&t_xout), size_t(c.hidden) * 8},
+        {reinterpret_cast<void **>(&t_token), 8},
     };
     size_t total = 0;
     for (auto &pc : pieces) total += round_up(pc.bytes, 256);
@@ -384,7 +408,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.t_act = t_act;
     p.t_xout = t_xout;
     h->tagged = reinterpret_cast<uint8_t *>(t_qkv);
-    h->tagged_bytes = static_cast<size_t>(reinterpret_cast<uint8_t *>(t_xout) + round_up(size_t(c.hidden) * 8, 256) -
+    p.t_token = t_token;
+    h->tagged_bytes = static_cast<size_t>(reinterpret_cast<uint8_t *>(t_token) + round_up(8, 256) -
                                           reinterpret_cast<uint8_t *>(t_qkv));
     p.lm_keys = keys;
     p.ctr = ctr;
@@ -467,6 +492,13 @@ int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev, 
     }
     if (next_token_host) *next_token_host = h->pinned[0];
     return LL_OK;
+}
+
+int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t n_steps, float *logits_dev,
+                    int32_t *tokens_dev) {
+    if (!h) return LL_ERR_ARG;
+    if (!token_dev || !tokens_dev) return fail(h, LL_ERR_ARG, "token_dev or tokens_dev is NULL");
+    return enqueue(h, 0, token_dev, pos, logits_dev, nullptr, n_steps, tokens_dev);
 }
 
 int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,

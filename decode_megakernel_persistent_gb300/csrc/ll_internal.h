@@ -134,12 +134,16 @@ struct KParams {
     uint32_t *ctr;            // counters, CTR_STRIDE apart
     int32_t *status;          // sticky status word
     int32_t *token_out;       // [1] library copy of the last next token
+    uint64_t *t_token;        // each step's next token as a tagged word (tag = the step's epoch), read by the
+                              // next step of the same launch
     // step
     int32_t token;            // used when token_dev is null
     const int32_t *token_dev;
-    int32_t pos;
-    uint32_t epoch;           // 1-based step count since the last reset of counters and tagged words
-    float *logits;            // [V] or null
+    int32_t pos;              // position of the launch's first step (step i decodes at pos + i)
+    uint32_t epoch;           // 1-based step count since the last reset, of the launch's first step
+    int32_t n_steps;          // greedy steps in this launch, each fed the previous one's token
+    int32_t *tokens_dev;      // [n_steps] every step's next token (multi-step launches), or null
+    float *logits;            // [n_steps][V] or null
     int32_t *next_token_dev;  // or null
     unsigned long long timeout_ns;
     uint32_t l2_prefetch;     // pages the producer may prefetch into L2 beyond its ring

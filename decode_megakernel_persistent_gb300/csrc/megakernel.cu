@@ -230,6 +230,11 @@ struct alignas(16) Smem {
     float nred[NCW];
     unsigned long long kred[NCW];
     int32_t token;
+    // the consumers' current step of a multi-step launch
+    uint32_t c_epoch;          // its epoch (tags)
+    int32_t c_pos;             // its position
+    float *c_logits;           // where its logits go, or null
+    volatile int32_t tok_step; // steps whose input token the consumers hold (the producer's gate)
     int32_t start_status;
     volatile int32_t flag;
     volatile int32_t abort;
@@ -334,14 +339,14 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
 //   x_out  (down -> QKV, LM):   rewrite needs act(l+1), i.e. every QKV SM done with layer l
 // (and the LM head's read of the last layer is in the same launch, before any
 // next-step write, which belongs to the next launch).
-__device__ __forceinline__ uint32_t tag_of(const KParams &p, int layer) {
-    return p.epoch * static_cast<uint32_t>(p.L + 1) + static_cast<uint32_t>(layer) + 1u;
+__device__ __forceinline__ uint32_t tag_of(const KParams &p, const Smem &s, int layer) {
+    return s.c_epoch * static_cast<uint32_t>(p.L + 1) + static_cast<uint32_t>(layer) + 1u;
 }
 
 // The tag an instruction writes: its layer's, or 0 when its completion has been
 // removed from the schedule (fault injection), so that its readers time out.
-__device__ __forceinline__ uint32_t write_tag(const KParams &p, const Instr &ins) {
-    return ins.sig_ctr >= 0 ? tag_of(p, ins.layer) : 0u;
+__device__ __forceinline__ uint32_t write_tag(const KParams &p, const Smem &s, const Instr &ins) {
+    return ins.sig_ctr >= 0 ? tag_of(p, s, ins.layer) : 0u;
 }
 
 // Bounded polling of tagged words: called after a round of loads found a stale
@@ -450,10 +455,10 @@ __device__ int mv_segments(const KParams &p, const Smem &s, const Instr &ins, Se
 }
 
 // Attention: cached positions [c0, c1) of split c, PP of them per page (K then V).
-__device__ __forceinline__ void attn_range(const KParams &p, int c, int &c0, int &c1) {
+__device__ __forceinline__ void attn_range(const KParams &p, int pos, int c, int &c0, int &c1) {
     const long long S = p.attn_splits;
-    c0 = static_cast<int>((static_cast<long long>(c) * p.pos) / S);
-    c1 = static_cast<int>((static_cast<long long>(c + 1) * p.pos) / S);
+    c0 = static_cast<int>((static_cast<long long>(c) * pos) / S);
+    c1 = static_cast<int>((static_cast<long long>(c + 1) * pos) / S);
 }
 
 __device__ __forceinline__ int attn_pp(const KParams &p) { return PAGE_BYTES / (4 * p.hd); }
@@ -499,13 +504,13 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
         case OP_QKV:
             if (ins.layer > 0) {
                 src = p.t_xout;
-                tag = tag_of(p, ins.layer - 1);
+                tag = tag_of(p, s, ins.layer - 1);
             }
             break;
-        case OP_GATEUP: src = p.t_xmid; tag = tag_of(p, ins.layer); break;
-        case OP_LMHEAD: src = p.t_xout; tag = tag_of(p, p.L - 1); break;
-        case OP_DOWN: src = p.t_act; tag = tag_of(p, ins.layer); break;
-        case OP_OPROJ: src = p.t_o; tag = tag_of(p, ins.layer); break;
+        case OP_GATEUP: src = p.t_xmid; tag = tag_of(p, s, ins.layer); break;
+        case OP_LMHEAD: src = p.t_xout; tag = tag_of(p, s, p.L - 1); break;
+        case OP_DOWN: src = p.t_act; tag = tag_of(p, s, ins.layer); break;
+        case OP_OPROJ: src = p.t_o; tag = tag_of(p, s, ins.layer); break;
         default: break;
     }
     const bool staged = src && mv.K <= XIN_FLOATS;
@@ -733,7 +738,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     if (tid == 0) trace_put(p, ii, 7);
     if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
     const int r0 = ins.r0;
-    const uint32_t wtag = write_tag(p, ins);
+    const uint32_t wtag = write_tag(p, s, ins);
     switch (ins.op) {
         case OP_QKV:
             for (int t = tid; t < nrows; t += NCT)
@@ -765,7 +770,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
         default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
             for (int t = tid; t < nrows; t += NCT) {
                 const float y = s.acc[t];
-                if (p.logits && LL_OK_IDX(10, r0 + t, p.V)) p.logits[r0 + t] = y;
+                if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[r0 + t] = y;
                 if (y > best) {
                     best = y;
                     best_idx = r0 + t;
@@ -791,7 +796,7 @@ __device__ void lm_finish(const KParams &p, Smem &s, float best, int best_idx) {
         p.lm_keys[blockIdx.x] = k;
         __threadfence();
         const uint32_t old = atomicAdd(p.ctr + size_t(CtrLayout::lm_ticket(p.L)) * CTR_STRIDE, 1u);
-        s.flag = (old + 1u == p.epoch * static_cast<uint32_t>(p.nsm)) ? 1 : 0;
+        s.flag = (old + 1u == s.c_epoch * static_cast<uint32_t>(p.nsm)) ? 1 : 0;
         __threadfence();
     }
     consumer_sync();
@@ -809,7 +814,14 @@ __device__ void lm_finish(const KParams &p, Smem &s, float best, int best_idx) {
         for (int w = 0; w < NCW; w++) m = s.kred[w] > m ? s.kred[w] : m;
         const int32_t tok = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(m & 0xffffffffu));
         p.token_out[0] = tok;
-        if (p.next_token_dev) *p.next_token_dev = tok;
+        if (p.tokens_dev) p.tokens_dev[s.c_epoch - p.epoch] = tok;
+        else if (p.next_token_dev) *p.next_token_dev = tok;
+        if (p.n_steps > 1) {
+            // the next step of this launch waits for this word (its tag is this step's epoch)
+            __threadfence();
+            const uint64_t w = (static_cast<uint64_t>(s.c_epoch) << 32) | static_cast<uint32_t>(tok);
+            asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p.t_token), "l"(w) : "memory");
+        }
     }
 }
 
@@ -1022,8 +1034,8 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     const int qd = p.nq * hd, kd = p.nkv * hd;
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
-    const float2 *cs = p.rope_cs + size_t(p.pos) * half;
-    const uint32_t tag = tag_of(p, l);
+    const float2 *cs = p.rope_cs + size_t(s.c_pos) * half;
+    const uint32_t tag = tag_of(p, s, l);
     // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
     // 1/sqrt(hd); the owner also rotates the new key and takes the new value
     {
@@ -1061,7 +1073,7 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     if (consumer_any(s.abort)) return false;
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
-        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + s.c_pos) * hd;
         if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
             for (int d = tid; d < hd; d += NCT) {
                 p.k_cache[at + d] = s.knew[d];
@@ -1070,7 +1082,7 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     }
     float oacc = 0.f;
     int c0, c1;
-    attn_range(p, c, c0, c1);
+    attn_range(p, s.c_pos, c, c0, c1);
     const int PP = attn_pp(p);
     for (int p0 = c0; p0 < c1; p0 += PP) {
         const int n = min(PP, c1 - p0);
@@ -1094,7 +1106,7 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
 
     // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}]
     const int stride = hd + 4;
-    const uint32_t wtag = write_tag(p, ins);
+    const uint32_t wtag = write_tag(p, s, ins);
     if (tid < G * hd) {
         const int h = tid / hd, d = tid % hd;
         st_tag(p.t_part + (size_t(g * G + h) * S + c) * stride + d, oacc, wtag);
@@ -1281,8 +1293,8 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     const int qd = p.nq * hd, kd = p.nkv * hd;
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
-    const float2 *cs = p.rope_cs + size_t(p.pos) * half;
-    const uint32_t tag = tag_of(p, l);
+    const float2 *cs = p.rope_cs + size_t(s.c_pos) * half;
+    const uint32_t tag = tag_of(p, s, l);
     // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
     // 1/sqrt(hd); the owner also rotates the new key and takes the new value
     {
@@ -1335,7 +1347,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     consumer_sync();
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
-        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + p.pos) * hd;
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + s.c_pos) * hd;
         if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
             for (int d = tid; d < hd; d += NCT) {
                 p.k_cache[at + d] = s.knew[d];
@@ -1347,7 +1359,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
 #pragma unroll
     for (int d = 0; d < 8; d++) o[d][0] = o[d][1] = 0.f;
     int c0, c1;
-    attn_range(p, c, c0, c1);
+    attn_range(p, s.c_pos, c, c0, c1);
     const int PP = attn_pp(p);
     // The warps form DG dim groups (64 dims each); within a dim group, NGR page
     // groups of W warps each take every NGR-th page of the item, W warps sharing a
@@ -1424,7 +1436,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}], from the
     // first warp of every dim group
     const int stride = hd + 4;
-    const uint32_t wtag = write_tag(p, ins);
+    const uint32_t wtag = write_tag(p, s, ins);
     if (tw == 0 && gq < G) {
         uint64_t *dst = p.t_part + (size_t(g * G + gq) * S + c) * stride;
 #pragma unroll
@@ -1500,13 +1512,38 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     const int PP = attn_pp(p);
     const uint32_t l2_ahead = p.l2_prefetch;
     const uint32_t lim = p.max_inflight >= 1 && p.max_inflight < NPAGES ? p.max_inflight : NPAGES;
-    for (int di = 0; di < nd && ok; di++) {
-        const PDesc e = dl[di];
+    // the list once per step of the launch: weight pages run ahead into the next
+    // step freely, K/V pages of a later step wait until the consumers hold that
+    // step's input token (everything the previous steps wrote is then visible)
+    const int ntot = nd * p.n_steps;
+    int gate = 0;  // steps whose K/V pages may be fetched
+    for (int di = 0; di < ntot && ok; di++) {
+        const int st = di / nd, pos = p.pos + st;
+        const PDesc e = dl[di % nd];
         int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
         size_t head_row = 0;
+        if (e.kind == PD_ATTN && st > gate) {
+            const uint64_t t0 = gtimer();
+            for (uint32_t it = 1; s.tok_step < st; ++it) {
+                if ((it & 15u) == 0) {
+                    if (s.abort) { ok = false; break; }
+                    if (gtimer() - t0 > p.timeout_ns) {
+                        raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) break;
+            // acquire what the consumers acquired, and order it before this
+            // thread's bulk-copy (async proxy) reads of the cache
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            gate = st;
+        }
         if (e.kind == PD_ATTN) {
             const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
-            attn_range(p, c, a_c0, a_c1);
+            attn_range(p, pos, c, a_c0, a_c1);
             a_p0 = a_c0;
             head_row = (size_t(layer) * p.nkv + g) * size_t(p.max_seq);
             if (a_c0 >= a_c1) continue;  // empty split: no pages
@@ -1552,8 +1589,8 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                 for (uint32_t it = 1;; ++it) {
                     if (can_issue()) break;
                     // while held up, pull the weight pages that come next into L2
-                    if (pfi < nd && uint32_t(pfi - di) < l2_ahead) {
-                        const PDesc f = dl[pfi++];
+                    if (pfi < ntot && uint32_t(pfi - di) < l2_ahead) {
+                        const PDesc f = dl[(pfi++) % nd];
                         if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
                         continue;
                     }
@@ -1618,11 +1655,33 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     }
 }
 
+// The step the consumers start: its epoch, position and logits, and for every
+// step after the first of a launch the token the previous step chose, read from
+// its tagged word with acquire order, so that everything the previous step wrote
+// (the K/V rows of its position among them) is visible here. The producer may
+// only fetch this step's K/V pages after that (s.tok_step).
+__device__ bool consumer_step_begin(const KParams &p, Smem &s, int st) {
+    if (threadIdx.x == 0) {
+        s.c_epoch = p.epoch + static_cast<uint32_t>(st);
+        s.c_pos = p.pos + st;
+        s.c_logits = p.logits ? p.logits + size_t(st) * size_t(p.V) : nullptr;
+        if (st > 0) {
+            const uint32_t prev = p.epoch + static_cast<uint32_t>(st - 1);
+            uint64_t w = 0, t0 = 0;
+            for (uint32_t it = 0;; ++it) {
+                w = ld_tag(p.t_token);
+                if (tag_ok(w, prev) || poll_give_up(p, s, it, t0)) break;
+            }
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            s.token = static_cast<int32_t>(static_cast<uint32_t>(w));
+            s.tok_step = st;
+        }
+    }
+    return !consumer_any(s.abort);
+}
+
 template <bool FLASH>
-__device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
-    const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
-    const int n = p.n_instr[blockIdx.x];
-    uint32_t cpage = 0;
+__device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const Instr *list, int n, uint32_t &cpage) {
     float best = -INFINITY;
     int best_idx = -1;
     for (int i = 0; i < n; i++) {
@@ -1645,10 +1704,23 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
             if (ok && ins.op == OP_LMHEAD) lm_finish(p, s, best, best_idx);
         }
         if (ok) ok = instr_sync(s);
-        if (!ok) return;
+        if (!ok) return false;
         if (threadIdx.x == 0) trace_put(p, i, 3);
     }
+    return true;
 }
+
+template <bool FLASH>
+__device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
+    const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
+    const int n = p.n_instr[blockIdx.x];
+    uint32_t cpage = 0;
+    for (int st = 0; st < p.n_steps; st++) {
+        if (!consumer_step_begin(p, s, st)) return;
+        if (!consumer_step<FLASH>(p, s, pages, list, n, cpage)) return;
+    }
+}
+
 
 template <bool FLASH>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
@@ -1666,6 +1738,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         s.abort = 0;
         s.flag = 0;
         s.token = p.token_dev ? *p.token_dev : p.token;
+        s.tok_step = 0;
         s.start_status = ld_relaxed(p.status);
         // the swizzled KV pages of the per-warp attention need 1024-byte aligned slots
         if (FLASH && (smem_addr(pages) & 1023u) != 0) {

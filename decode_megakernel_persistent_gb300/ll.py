@@ -41,7 +41,7 @@ OP_QKV, OP_ATTN, OP_OPROJ, OP_GATEUP, OP_DOWN = range(5)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
-EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_synchronize",
+EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_decode_steps", "ll_synchronize",
            "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
            "ll_free", "ll_decode_step_static")
 
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
     L.ll_decode_step.restype = ctypes.c_int
     L.ll_decode_step_async.argtypes = [vp, vp, i32, vp, vp]
     L.ll_decode_step_async.restype = ctypes.c_int
+    L.ll_decode_steps.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.ll_decode_steps.restype = ctypes.c_int
     L.ll_synchronize.argtypes = [vp]
     L.ll_synchronize.restype = ctypes.c_int
     L.ll_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
@@ -169,6 +171,10 @@ def ll_decode_step(h, token: int, pos: int, logits=None) -> int:
     nxt = ctypes.c_int32(-1)
     _check(h, lib().ll_decode_step(h, int(token), int(pos), _ptr(logits), ctypes.byref(nxt)))
     return int(nxt.value)
+
+
+def ll_decode_steps(h, token_dev, pos: int, n_steps: int, logits, tokens_dev) -> None:
+    _check(h, lib().ll_decode_steps(h, _ptr(token_dev), int(pos), int(n_steps), _ptr(logits), _ptr(tokens_dev)))
 
 
 def ll_decode_step_async(h, token_dev, pos: int, logits, next_token_dev) -> None:
@@ -260,6 +266,9 @@ class Decoder:
 
     def step_async(self, token_dev, pos: int, logits, next_token_dev) -> None:
         ll_decode_step_async(self.handle, token_dev, pos, logits, next_token_dev)
+
+    def steps(self, token_dev, pos: int, n_steps: int, logits, tokens_dev) -> None:
+        ll_decode_steps(self.handle, token_dev, pos, n_steps, logits, tokens_dev)
 
     def synchronize(self) -> None:
         ll_synchronize(self.handle)

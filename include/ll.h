@@ -122,6 +122,24 @@ int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev,
 int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,
                          int32_t *next_token_dev);
 
+/* n_steps greedy decode steps in one launch of the persistent kernel, enqueued
+ * only (the page's interpreter keeps its per-SM schedule for every token; here
+ * it also keeps running from one token to the next, so the weight pages of a
+ * step stream in while the previous step's LM head and argmax finish). Step i
+ * decodes at position pos + i: step 0 reads its token from *token_dev, step
+ * i > 0 the token step i - 1 chose, and step i writes its next token to
+ * tokens_dev[i] and, when logits_dev is not NULL, its fp32 logits to
+ * logits_dev + i * vocab (so logits_dev holds n_steps * vocab floats).
+ * token_dev and tokens_dev are device int32 and must not be NULL; tokens_dev
+ * holds n_steps values, and token_dev may point into it (every block reads
+ * *token_dev before step 0 can finish). Requires
+ * n_steps >= 1 and pos + n_steps <= max_seq (LL_ERR_ARG otherwise). Results are
+ * bit-identical to n_steps calls of ll_decode_step_async chained on the device.
+ * Errors are sticky as for ll_decode_step_async; ll_synchronize() reports them.
+ * The per-operation backend runs the same steps as separate launches. */
+int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t n_steps, float *logits_dev,
+                    int32_t *tokens_dev);
+
 /* Wait for the handle's stream, then return and clear the device status of the
  * steps enqueued since the last check (LL_OK if all of them succeeded). After
  * an error the library clears its device state, so the next step starts clean. */
