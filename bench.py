@@ -8,8 +8,10 @@ layer, LM head and argmax, run by the persistent megakernel through the C ABI.
 
 Default workload: Llama-3.2-1B shape, bf16 weights bf16(0.02*N(0,1)) from seed
 0, a 1024-token random prompt (seed 1) prefilled through the model, then K
-greedy decode steps timed with CUDA events on the decode stream (the token is
-chained on the device, no host round trip). The weights (2.47 GB) are far larger
+greedy decode steps timed with CUDA events on the decode stream: one
+ll_decode_steps launch in which each step takes the token the previous one
+chose (no host round trip). ``single_step_launches`` times the same K positions
+again as K chained single-step launches. The weights (2.47 GB) are far larger
 than L2 (129 MB), so every step streams them from HBM. ``e2e`` repeats K steps
 through ll_decode_step with the token passed from the host and the next token
 read back to host memory every step, timed by the host clock.
@@ -290,16 +292,31 @@ def run_ours(args):
         pos0 = pos
         if clocks:
             clocks.mark()
+        # timed: K greedy steps in one launch of the persistent kernel (each step
+        # fed the previous one's token on the device), logits of every step kept
+        logits_k = torch.empty((K, shape.vocab), dtype=torch.float32, device=dev)
+        toks_k = torch.zeros(K, dtype=torch.int32, device=dev)
         e0.record(stream)
-        for _ in range(K):
-            dec.step_async(tok, pos, logits, tok)
-            pos += 1
+        dec.steps(tok, pos0, K, logits_k, toks_k)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
         dec.synchronize()
         dev_ms = e0.elapsed_time(e1)
         t_dev = max_over_ranks(dev_ms / 1e3, world, dev)
+        # the same K positions again as K single-step launches chained on the
+        # device (the cache rows they rewrite are read back the same way)
+        tok.copy_(toks_k[:1])
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(K):
+            dec.step_async(tok, pos0 + i, logits, tok)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dec.synchronize()
+        t_single = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        tok.copy_(toks_k[-1:])
+        pos = pos0 + K
 
         # end to end through the C ABI with host buffers
         host_tok = int(tok.item())
@@ -314,15 +331,17 @@ def run_ours(args):
         barrier(world)
         if clocks:
             clocks.stop()
-    launches = dec.query(ll.LL_Q_LAUNCHES_PER_STEP) * K
+    # kernels launched in the timed region: one persistent launch (the chain
+    # backend runs its per-operation kernels for every step)
+    launches = 1 if backend == ll.LL_BACKEND_MEGAKERNEL else dec.query(ll.LL_Q_LAUNCHES_PER_STEP) * K
 
     if rank != 0:
         dec.close()
         return
 
     bytes_per_step = statistics.mean(bytemodel.step_bytes(shape, p) for p in range(pos0, pos0 + K))
-    per_launch_s = t_dev / K
-    achieved = bytes_per_step / per_launch_s / 1e9
+    achieved = bytes_per_step * K / t_dev / 1e9  # the launch's algorithmic bytes over its duration
+    traffic_step = recorded_traffic(wl.name, args.backend)
     peak, peak_kind = peaks()
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -348,12 +367,17 @@ def run_ours(args):
         "config": {"workload": wl.name, "context": ctx, "decode_steps_timed": K,
                    "positions": [pos0, pos0 + K - 1], "weights": "bf16", "backend": args.backend,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2: every step streams all weights from HBM"},
+                   "l2": "inputs larger than L2: every step streams all weights from HBM",
+                   "timed": "one ll_decode_steps launch of K greedy steps" if backend == ll.LL_BACKEND_MEGAKERNEL
+                   else "ll_decode_steps: K steps of per-operation launches"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_8000": achieved / SPEC_HBM_GBS,
-                     "bytes_per_launch": bytes_per_step,
-                     "traffic": recorded_traffic(wl.name, args.backend)},
+                     "bytes_per_launch": bytes_per_step * K, "bytes_per_step": bytes_per_step,
+                     # ncu DRAM bytes of a single-step launch (same kernel sources) times the K steps
+                     "traffic": traffic_step * K if traffic_step else None},
+        "single_step_launches": {"us_per_token": 1e6 * t_single / K, "value": world * K / t_single,
+                                 "unit": "tokens/s", "launches": K},
         "e2e": {"value": world * K / t_e2e, "unit": "tokens/s", "us_per_token": 1e6 * t_e2e / K,
                 "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8},
         "gpu_launches": launches,

@@ -1515,86 +1515,17 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     // the list once per step of the launch: weight pages run ahead into the next
     // step freely, K/V pages of a later step wait until the consumers hold that
     // step's input token (everything the previous steps wrote is then visible)
-    const int ntot = nd * p.n_steps;
     int gate = 0;  // steps whose K/V pages may be fetched
-    for (int di = 0; di < ntot && ok; di++) {
-        const int st = di / nd, pos = p.pos + st;
-        const PDesc e = dl[di % nd];
-        int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
-        size_t head_row = 0;
-        if (e.kind == PD_ATTN && st > gate) {
-            const uint64_t t0 = gtimer();
-            for (uint32_t it = 1; s.tok_step < st; ++it) {
-                if ((it & 15u) == 0) {
-                    if (s.abort) { ok = false; break; }
-                    if (gtimer() - t0 > p.timeout_ns) {
-                        raise_status(p, s, LL_ERR_DEP_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            if (!ok) break;
-            // acquire what the consumers acquired, and order it before this
-            // thread's bulk-copy (async proxy) reads of the cache
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            gate = st;
-        }
-        if (e.kind == PD_ATTN) {
-            const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
-            attn_range(p, pos, c, a_c0, a_c1);
-            a_p0 = a_c0;
-            head_row = (size_t(layer) * p.nkv + g) * size_t(p.max_seq);
-            if (a_c0 >= a_c1) continue;  // empty split: no pages
-        }
-        // weight entries are one page; attention entries one page per PP positions
-        while (ok) {
-            const void *src0, *src1 = nullptr;
-            uint32_t b0, b1 = 0;
-            int a_row = 0;
-            if (e.kind == PD_ATTN) {
-                if (a_p0 >= a_c1) break;
-                a_n = min(PP, a_c1 - a_p0);
-                a_row = int(head_row) + a_p0;
-                if (FLASH) {
-                    // K and V through the tensor maps: whole page, or 16-row tiles
-                    const uint32_t tiles = uint32_t(a_n + ATT_TILE - 1) / ATT_TILE;
-                    b0 = b1 = a_n == PP ? uint32_t(PAGE_BYTES / 2) : tiles * uint32_t(p.hd / 64) * ATT_TILE * 128u;
-                    src0 = src1 = nullptr;
-                } else {
-                    b0 = b1 = uint32_t(a_n) * p.hd * 2;
-                    src0 = p.k_cache + (head_row + size_t(a_p0)) * p.hd;
-                    src1 = p.v_cache + (head_row + size_t(a_p0)) * p.hd;
-                }
-                a_p0 += a_n;
-            } else {
-                src0 = reinterpret_cast<const void *>(e.src);
-                b0 = e.bytes;
-            }
-            const uint32_t slot = ppage % NPAGES;
-            // a page goes out once its slot is free and fewer than p.max_inflight
-            // earlier pages are still landing
-            auto can_issue = [&]() -> bool {
-                if (ppage >= NPAGES && !mbar_test(&s.empty[slot], ((ppage / NPAGES) - 1u) & 1u)) return false;
-                if (ppage >= lim) {
-                    const uint32_t q = ppage - lim;
-                    if (!mbar_test(&s.full[q % NPAGES], (q / NPAGES) & 1u)) return false;
-                }
-                return true;
-            };
-            if (!can_issue()) {
-                if (pfi < di) pfi = di;  // from the page that is waiting
+    for (int st = 0; st < p.n_steps && ok; st++) {
+        const int pos = p.pos + st;
+        pfi = 0;
+        for (int di = 0; di < nd && ok; di++) {
+            const PDesc e = dl[di];
+            int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
+            size_t head_row = 0;
+            if (e.kind == PD_ATTN && st > gate) {
                 const uint64_t t0 = gtimer();
-                for (uint32_t it = 1;; ++it) {
-                    if (can_issue()) break;
-                    // while held up, pull the weight pages that come next into L2
-                    if (pfi < ntot && uint32_t(pfi - di) < l2_ahead) {
-                        const PDesc f = dl[(pfi++) % nd];
-                        if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
-                        continue;
-                    }
-                    __nanosleep(p.producer_sleep_ns);
+                for (uint32_t it = 1; s.tok_step < st; ++it) {
                     if ((it & 15u) == 0) {
                         if (s.abort) { ok = false; break; }
                         if (gtimer() - t0 > p.timeout_ns) {
@@ -1605,37 +1536,108 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                     }
                 }
                 if (!ok) break;
+                // acquire what the consumers acquired, and order it before this
+                // thread's bulk-copy (async proxy) reads of the cache
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                gate = st;
             }
-            uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
-            ptrace_put(p, ppage, 0);
-            s.slot_page[slot] = ppage;
-            mbar_expect_tx(&s.full[slot], b0 + b1);
-            if (FLASH && e.kind == PD_ATTN) {
-                // [K | V] x [dim half] x [positions] x 64 dims, swizzled (see attn_tiles)
-                const int dh = p.hd / 64;
-                for (int kv = 0; kv < 2; kv++)
-                    for (int h = 0; h < dh; h++) {
-                        uint8_t *d = dst + kv * (PAGE_BYTES / 2) + h * PP * 128;
-                        if (a_n == PP) {
-                            tma_load_2d(d, &p.kv_maps[kv ? TM_V_PAGE : TM_K_PAGE], 64 * h, a_row, &s.full[slot]);
-                        } else {
-                            for (int j = 0; j < a_n; j += ATT_TILE)
-                                tma_load_2d(d + j * 128, &p.kv_maps[kv ? TM_V_TILE : TM_K_TILE], 64 * h, a_row + j,
-                                            &s.full[slot]);
+            if (e.kind == PD_ATTN) {
+                const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
+                attn_range(p, pos, c, a_c0, a_c1);
+                a_p0 = a_c0;
+                head_row = (size_t(layer) * p.nkv + g) * size_t(p.max_seq);
+                if (a_c0 >= a_c1) continue;  // empty split: no pages
+            }
+            // weight entries are one page; attention entries one page per PP positions
+            while (ok) {
+                const void *src0, *src1 = nullptr;
+                uint32_t b0, b1 = 0;
+                int a_row = 0;
+                if (e.kind == PD_ATTN) {
+                    if (a_p0 >= a_c1) break;
+                    a_n = min(PP, a_c1 - a_p0);
+                    a_row = int(head_row) + a_p0;
+                    if (FLASH) {
+                        // K and V through the tensor maps: whole page, or 16-row tiles
+                        const uint32_t tiles = uint32_t(a_n + ATT_TILE - 1) / ATT_TILE;
+                        b0 = b1 = a_n == PP ? uint32_t(PAGE_BYTES / 2) : tiles * uint32_t(p.hd / 64) * ATT_TILE * 128u;
+                        src0 = src1 = nullptr;
+                    } else {
+                        b0 = b1 = uint32_t(a_n) * p.hd * 2;
+                        src0 = p.k_cache + (head_row + size_t(a_p0)) * p.hd;
+                        src1 = p.v_cache + (head_row + size_t(a_p0)) * p.hd;
+                    }
+                    a_p0 += a_n;
+                } else {
+                    src0 = reinterpret_cast<const void *>(e.src);
+                    b0 = e.bytes;
+                }
+                const uint32_t slot = ppage % NPAGES;
+                // a page goes out once its slot is free and fewer than p.max_inflight
+                // earlier pages are still landing
+                auto can_issue = [&]() -> bool {
+                    if (ppage >= NPAGES && !mbar_test(&s.empty[slot], ((ppage / NPAGES) - 1u) & 1u)) return false;
+                    if (ppage >= lim) {
+                        const uint32_t q = ppage - lim;
+                        if (!mbar_test(&s.full[q % NPAGES], (q / NPAGES) & 1u)) return false;
+                    }
+                    return true;
+                };
+                if (!can_issue()) {
+                    if (pfi < di) pfi = di;  // from the page that is waiting
+                    const uint64_t t0 = gtimer();
+                    for (uint32_t it = 1;; ++it) {
+                        if (can_issue()) break;
+                        // while held up, pull the weight pages that come next into L2
+                        if (pfi < nd && uint32_t(pfi - di) < l2_ahead) {
+                            const PDesc f = dl[pfi++];
+                            if (f.kind == PD_WEIGHTS) bulk_prefetch_l2(reinterpret_cast<const void *>(f.src), f.bytes);
+                            continue;
+                        }
+                        __nanosleep(p.producer_sleep_ns);
+                        if ((it & 15u) == 0) {
+                            if (s.abort) { ok = false; break; }
+                            if (gtimer() - t0 > p.timeout_ns) {
+                                raise_status(p, s, LL_ERR_DEP_TIMEOUT);
+                                ok = false;
+                                break;
+                            }
                         }
                     }
-            } else {
-                if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
-                else bulk_load(dst, src0, b0, &s.full[slot]);
-                if (b1) bulk_load(dst + PAGE_BYTES / 2, src1, b1, &s.full[slot]);
+                    if (!ok) break;
+                }
+                uint8_t *dst = pages + size_t(slot) * PAGE_BYTES;
+                ptrace_put(p, ppage, 0);
+                s.slot_page[slot] = ppage;
+                mbar_expect_tx(&s.full[slot], b0 + b1);
+                if (FLASH && e.kind == PD_ATTN) {
+                    // [K | V] x [dim half] x [positions] x 64 dims, swizzled (see attn_tiles)
+                    const int dh = p.hd / 64;
+                    for (int kv = 0; kv < 2; kv++)
+                        for (int h = 0; h < dh; h++) {
+                            uint8_t *d = dst + kv * (PAGE_BYTES / 2) + h * PP * 128;
+                            if (a_n == PP) {
+                                tma_load_2d(d, &p.kv_maps[kv ? TM_V_PAGE : TM_K_PAGE], 64 * h, a_row, &s.full[slot]);
+                            } else {
+                                for (int j = 0; j < a_n; j += ATT_TILE)
+                                    tma_load_2d(d + j * 128, &p.kv_maps[kv ? TM_V_TILE : TM_K_TILE], 64 * h, a_row + j,
+                                                &s.full[slot]);
+                            }
+                        }
+                } else {
+                    if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
+                    else bulk_load(dst, src0, b0, &s.full[slot]);
+                    if (b1) bulk_load(dst + PAGE_BYTES / 2, src1, b1, &s.full[slot]);
+                }
+                if (int(e.instr) != last_instr) {
+                    trace_put(p, e.instr, 4);
+                    last_instr = e.instr;
+                }
+                trace_put(p, e.instr, 5);
+                ++ppage;
+                if (e.kind == PD_WEIGHTS) break;
             }
-            if (int(e.instr) != last_instr) {
-                trace_put(p, e.instr, 4);
-                last_instr = e.instr;
-            }
-            trace_put(p, e.instr, 5);
-            ++ppage;
-            if (e.kind == PD_WEIGHTS) break;
         }
     }
     // Never leave with copies in flight into this block's shared memory: wait for
