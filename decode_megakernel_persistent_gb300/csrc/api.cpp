@@ -317,8 +317,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&logits), size_t(c.vocab) * 4},
         {reinterpret_cast<void **>(&keys), size_t(h->nsm) * 8},
         {reinterpret_cast<void **>(&ctr), nctr * 4},
-        {reinterpret_cast<void **>(&status), 4},
-        {reinterpret_cast<void **>(&tok), 4},
+        // the next token and the status word side by side: one 8-byte copy reads both
+        {reinterpret_cast<void **>(&tok), 8},
         {reinterpret_cast<void **>(&dbg), 64},
         // the megakernel's tagged activations (one contiguous run, cleared together)
         {reinterpret_cast<void **>(&t_qkv), size_t(qd + 2 * kd) * 8},
@@ -413,6 +413,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
                                           reinterpret_cast<uint8_t *>(t_qkv));
     p.lm_keys = keys;
     p.ctr = ctr;
+    status = tok + 1;
     p.status = status;
     p.token_out = tok;
 #ifdef LL_DEBUG_CHECKS
@@ -478,8 +479,7 @@ int ll_decode_step(ll_handle *h, int32_t token, int32_t pos, float *logits_dev, 
     if (token < 0 || token >= h->cfg.vocab) return fail(h, LL_ERR_ARG, "token " + std::to_string(token) + " outside [0, vocab)");
     int rc = enqueue(h, token, nullptr, pos, logits_dev, nullptr);
     if (rc != LL_OK) return rc;
-    if (cudaMemcpyAsync(h->pinned, h->kp.token_out, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
-        cudaMemcpyAsync(h->pinned + 1, h->kp.status, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
+    if (cudaMemcpyAsync(h->pinned, h->kp.token_out, 8, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
         cudaStreamSynchronize(h->stream) != cudaSuccess) {
         cudaError_t e = cudaGetLastError();
         return fail(h, LL_ERR_CUDA, std::string("step failed: ") + cudaGetErrorString(e));
