@@ -138,3 +138,36 @@ def test_steps_argument_checks():
     dec.steps(_i32([1]), 10, 6, None, toks)  # up to the last position
     dec.synchronize()
     dec.close()
+
+
+def test_steps_errors_are_reported_and_cleared():
+    # a dependency wait that runs out inside a multi-step launch (an instruction's
+    # completion removed from the schedule), then a first token out of range: each
+    # is reported by ll_synchronize, and the next launch decodes normally again
+    shape = synth.TINY
+    w = synth.make_weights(shape, seed=0, device="cuda")
+    ctx, n = 16, 4
+    k, v = synth.make_kv(shape, ctx + 3 * n, ctx, seed=2, device="cuda")
+    dec = ll.Decoder(shape, w, k, v, ctx + 3 * n)
+    toks = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ll.ll_set_timeout_ns(dec.handle, 20_000_000)  # 20 ms
+    ll.ll_debug_inject(dec.handle, ll.LL_FAULT_DROP_SIGNAL, 1, ll.OP_DOWN)
+    dec.steps(_i32([1]), ctx, n, None, toks)
+    with pytest.raises(ll.LLError) as e:
+        dec.synchronize()
+    assert e.value.code == ll.LL_ERR_DEP_TIMEOUT
+    ll.ll_debug_inject(dec.handle, ll.LL_FAULT_NONE)
+    ll.ll_set_timeout_ns(dec.handle, 1_000_000_000)
+    dec.steps(_i32([shape.vocab + 3]), ctx, n, None, toks)
+    with pytest.raises(ll.LLError) as e:
+        dec.synchronize()
+    assert e.value.code == ll.LL_ERR_ARG
+    logits = torch.empty((n, shape.vocab), dtype=torch.float32, device="cuda")
+    dec.steps(_i32([1]), ctx, n, logits, toks)
+    dec.synchronize()
+    got = toks.cpu().numpy()
+    dec.close()
+    # the same steps on a fresh handle and cache
+    ref = run(shape, w, ctx, n, "launch", tok0=1)
+    np.testing.assert_array_equal(got, ref[0])
+    np.testing.assert_array_equal(logits.cpu().numpy(), ref[1])
