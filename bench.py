@@ -350,6 +350,14 @@ def run_ours(args):
         cpu = {"value": n / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} full oracle decode steps (fp32, OpenMP over rows) at positions "
                          f"{ctx}..{ctx + n - 1} on a seeded KV cache, {secs:.1f} s"}
+        # the same on one thread, a smaller sample
+        import oracle
+        oracle.set_threads(1)
+        n1, secs1, _ = oracle_timing(shape, ctx, args.cpu_seconds / 2, weights_host=wh)
+        oracle.set_threads(cores)
+        cpu["single_thread"] = {"value": n1 / secs1, "unit": "tokens/s", "cores": 1,
+                                "sample": f"{n1} full oracle decode steps on one thread at positions "
+                                          f"{ctx}..{ctx + n1 - 1}, {secs1:.1f} s"}
     line = {
         "metric": METRIC,
         "value": world * K / t_dev,

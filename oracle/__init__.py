@@ -91,6 +91,8 @@ def _load():
             fn.argtypes = args
     lib.orc_num_threads.restype = ctypes.c_int
     lib.orc_num_threads.argtypes = []
+    lib.orc_set_threads.restype = None
+    lib.orc_set_threads.argtypes = [ctypes.c_int]
     _lib = lib
     return lib
 
@@ -118,6 +120,12 @@ def _p16(a: np.ndarray):
 def num_threads() -> int:
     """Threads the oracle's row-parallel matrix-vector products use."""
     return int(_load().orc_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads for the row-parallel loops from now on (timing only: each output
+    row is summed by one thread, so results do not depend on it)."""
+    _load().orc_set_threads(int(n))
 
 
 # ---- primitives (used by the pin tests) -------------------------------------

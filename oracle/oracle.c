@@ -240,4 +240,14 @@ int orc_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads for the row-parallel loops from now on (n >= 1); timing only, the
+ * results do not depend on it (each output row is one thread's sum). */
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
 #endif

@@ -65,5 +65,6 @@ ORC_DECLARE(orc32_, float)
 ORC_DECLARE(orc64_, double)
 
 int orc_num_threads(void);
+void orc_set_threads(int n);
 
 #endif

@@ -244,3 +244,25 @@ def test_bad_arguments_rejected():
         m.decode_step(cfg["vocab"], 0)
     with pytest.raises(ValueError):
         m.decode_step(0, 8)
+
+
+def test_results_do_not_depend_on_thread_count():
+    # each output row is summed by one thread, left to right, so the oracle's
+    # logits and cache are bit-identical on one thread and on several
+    shape = synth.TINY
+    w = synth.weights_to_host_bits(synth.make_weights(shape, seed=2, device="cpu"))
+    cfg = shape.as_dict()
+    toks = synth.make_tokens(shape.vocab, 6, seed=3)
+    before = oracle.num_threads()
+    out = []
+    try:
+        for n in (1, max(2, before)):
+            oracle.set_threads(n)
+            assert oracle.num_threads() == n
+            m = oracle.OracleModel(cfg, w, max_seq=8, prec=32)
+            logs = [m.decode_step(t, pos)[0].copy() for pos, t in enumerate(toks)]
+            out.append((np.stack(logs), m.k_cache.copy(), m.v_cache.copy()))
+    finally:
+        oracle.set_threads(before)
+    for a, b in zip(out[0], out[1]):
+        np.testing.assert_array_equal(a, b)
