@@ -69,6 +69,19 @@ def test_one_launch_equals_chained_steps(shape, ctx, n):
     assert_same(a, b)
 
 
+@pytest.mark.parametrize("shape,ctx,n", [(synth.LLAMA_3B, 300, 3), (synth.LLAMA_8B, 5000, 3)], ids=["3b", "8b"])
+def test_one_launch_equals_chained_steps_128_dim_heads(shape, ctx, n):
+    # 128-dim heads: the 3B shape (block attention) and the untied 8B shape, whose
+    # attention items at this context span several pages (per-warp variant)
+    w = synth.make_weights(shape, seed=0, device="cuda")
+    a = run(shape, w, ctx, n, "launch")
+    b = run(shape, w, ctx, n, "chained")
+    assert np.all(np.isfinite(a[1]))
+    assert_same(a, b)
+    del w
+    torch.cuda.empty_cache()
+
+
 def test_one_launch_equals_chained_steps_per_warp_attention():
     # the per-warp (tensor-core) attention variant, whose K/V pages come through
     # tensor maps: 1B shape at a context where each attention item spans pages
