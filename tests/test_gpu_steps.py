@@ -138,6 +138,27 @@ def test_every_step_matches_oracle():
     pr.close()
 
 
+def test_timed_configuration_matches_oracle_1b():
+    # the launch bench.py times, at its model and context: one ll_decode_steps
+    # launch at the 1B shape from a 1024-entry cache, every step against the oracle
+    shape = synth.LLAMA_1B
+    ctx, n = 1024, 3
+    pr = Pair(shape, ctx + n, kv_fill=ctx)
+    logits = torch.empty((n, shape.vocab), dtype=torch.float32, device="cuda")
+    toks = torch.zeros(n, dtype=torch.int32, device="cuda")
+    pr.dec.steps(_i32([17]), ctx, n, logits, toks)
+    pr.dec.synchronize()
+    got_t, got_l = toks.cpu().numpy(), logits.cpu().numpy()
+    tok = 17
+    for i in range(n):
+        ref, _ = pr.orc.decode_step(tok, ctx + i)
+        compare_logits(got_l[i], ref, f"step {i}")
+        check_token(int(got_t[i]), ref, f"step {i}")
+        tok = int(got_t[i])
+    pr.kv_close(slice(ctx, ctx + n))
+    pr.close()
+
+
 def test_steps_argument_checks():
     shape = synth.TINY
     w = synth.make_weights(shape, seed=0, device="cuda")
