@@ -337,8 +337,10 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
 //   x_mid  (O -> gate/up):      rewrite needs o(l+1), i.e. every gate/up SM done with layer l;
 //   act    (gate/up -> down):   rewrite needs x_mid(l+1), i.e. every down SM done with layer l;
 //   x_out  (down -> QKV, LM):   rewrite needs act(l+1), i.e. every QKV SM done with layer l
-// (and the LM head's read of the last layer is in the same launch, before any
-// next-step write, which belongs to the next launch).
+// The LM head reads the last layer's x_out before any write of the next step:
+// that step runs in a later launch, or, in a multi-step launch, only once its
+// input token is published, which the last SM does after every SM has finished
+// its LM head (and so every read of this step's words).
 __device__ __forceinline__ uint32_t tag_of(const KParams &p, const Smem &s, int layer) {
     return s.c_epoch * static_cast<uint32_t>(p.L + 1) + static_cast<uint32_t>(layer) + 1u;
 }
