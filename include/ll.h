@@ -159,7 +159,8 @@ int ll_set_timeout_ns(ll_handle *h, uint64_t ns);
  * attention the ends of the scores, softmax and P.V phases and of its signal.
  * The second part, [sm][4096][3] uint64, holds per shared-memory page (page
  * number modulo 4096): producer issue, consumer start, release. All values are
- * %globaltimer nanoseconds; each traced step overwrites them. NULL turns tracing
+ * %globaltimer nanoseconds; each traced step (every step of a multi-step
+ * launch) overwrites them. NULL turns tracing
  * off (the default). Returns LL_ERR_ARG if the buffer is too small or misaligned. */
 int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
 
@@ -170,7 +171,7 @@ int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
 #define LL_Q_NUM_PAGES 3        /* pages per SM */
 #define LL_Q_SCRATCH_BYTES 4    /* device bytes the library allocated */
 #define LL_Q_MAX_INSTRS 5       /* longest per-SM instruction list */
-#define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes */
+#define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes (ll_decode_steps: one launch for all its steps) */
 #define LL_Q_SMEM_BYTES 7       /* dynamic shared memory per block */
 #define LL_Q_TRACE_BYTES 8      /* size of the buffer ll_set_trace needs */
 int ll_query(const ll_handle *h, int what, int64_t *value);
