@@ -1,0 +1,37 @@
+"""Host-side pieces of bench.py that its JSON line depends on (no GPU):
+the hash that ties recorded ncu traffic to the library's code, and the
+lookup of that traffic."""
+import json
+import os
+
+import bench
+
+
+def test_code_hash_ignores_comments_and_layout():
+    src = "int f(int a) {\n    // doubled\n    return 2 * a; /* fast */\n}\n"
+    same = "int f(int a) { return 2 * a; }  // reformatted, comment moved\n"
+    other = "int f(int a) {\n    return 3 * a;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    multi = "/* a\n multi-line\n comment */ int x;"
+    assert bench._code_only(multi) == "int x;"
+
+
+def test_recorded_traffic_is_tied_to_the_code(tmp_path, monkeypatch):
+    sha = bench.kernel_sha()
+    assert len(sha) == 16
+    # a copy of the tree with the real sources and a traffic record of its own
+    pkg = tmp_path / "decode_megakernel_persistent_gb300"
+    pkg.mkdir()
+    os.symlink(os.path.join(bench.ROOT, "decode_megakernel_persistent_gb300", "csrc"), pkg / "csrc")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"megakernel:w": {"kernel_sha": sha, "bytes_per_launch": 123},
+           "megakernel:old": {"kernel_sha": "0" * 16, "bytes_per_launch": 456}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_sha() == sha
+    assert bench.recorded_traffic("w", "megakernel") == 123
+    assert bench.recorded_traffic("old", "megakernel") is None  # taken on other code
+    assert bench.recorded_traffic("missing", "megakernel") is None
+    assert bench.recorded_traffic("w", "chain") is None
