@@ -79,6 +79,42 @@ def page_stats(ptrace: np.ndarray, npages: int) -> dict:
     return {"issue_to_start_us": pct(lat), "start_to_release_us": pct(work), "issue_gap_us": pct(gap)}
 
 
+def issue_idle(tr: np.ndarray, pt: np.ndarray, plan: np.ndarray, bin_us: float = 0.5, idle_pages: int = 5,
+               page_bytes: int = 32768) -> dict:
+    """When the GPU as a whole issues no page loads. For each layer 1..L-2: its span
+    (from the end of the previous layer's down projection on the slowest SM to the
+    end of its own), the time in bins of bin_us in which all SMs together issued at
+    most idle_pages pages, and the issue rate in the other bins (pages counted as
+    page_bytes); means over those layers."""
+    valid = plan[:, :, 0] >= 0
+    t0 = tr[:, :, 0][valid].min()
+    iss = (pt[:, :, 0].astype(np.int64) - t0) / 1e3
+    iss = iss[pt[:, :, 0] > 0]
+    nl = int(plan[:, :, 1][valid & (plan[:, :, 0] < 5)].max()) + 1
+    spans, idle, rate = [], [], []
+    for l in range(1, nl - 1):
+        prev = valid & (plan[:, :, 1] == l - 1) & (plan[:, :, 0] == 4)
+        cur = valid & (plan[:, :, 1] == l) & (plan[:, :, 0] == 4)
+        if not prev.any() or not cur.any():
+            continue
+        b = (tr[:, :, 3][prev].max() - t0) / 1e3
+        e = (tr[:, :, 3][cur].max() - t0) / 1e3
+        nb = int((e - b) / bin_us)
+        if nb < 1:
+            continue
+        h, _ = np.histogram(iss, bins=b + bin_us * np.arange(nb + 1))
+        busy = h > idle_pages
+        spans.append(e - b)
+        idle.append(float((~busy).sum()) * bin_us)
+        if busy.any():
+            rate.append(float(h[busy].sum()) * page_bytes / (float(busy.sum()) * bin_us * 1e-6) / 1e9)
+    if not spans:
+        return {}
+    return {"layer_span_us": round(float(np.mean(spans)), 2), "idle_us": round(float(np.mean(idle)), 2),
+            "busy_issue_gbs": round(float(np.mean(rate)), 0) if rate else 0.0, "bin_us": bin_us,
+            "idle_pages": idle_pages}
+
+
 def main():
     import torch
 
@@ -87,11 +123,20 @@ def main():
     ap.add_argument("--workload", default="1b")
     ap.add_argument("--steps", type=int, default=3, help="traced steps (the last is reported)")
     ap.add_argument("--save", default=None, help="write the raw trace and plan to this .npz")
+    ap.add_argument("--load", default=None, help="summarise a trace written by --save (no GPU needed)")
     ap.add_argument("--notrace", action="store_true",
                     help="run the same steps with tracing off (a target for external profilers)")
     ap.add_argument("--l2-resident", action="store_true",
                     help="a 2-layer hidden-1024 model whose weights (~90 MB) stay in L2")
     args = ap.parse_args()
+    if args.load:
+        d = np.load(args.load)
+        tr, pt, plan = d["trace"], d["ptrace"], d["plan"]
+        res = summarize(tr, plan)
+        res["pages"] = page_stats(pt, pt.shape[1])
+        res["issue"] = issue_idle(tr, pt, plan)
+        print(json.dumps(res, indent=1))
+        return
     build.build()
     wl = synth.WORKLOADS[args.workload]
     shape, ctx = wl.shape, wl.context
@@ -124,6 +169,7 @@ def main():
     pt = flat[n_instr_words:].reshape(nsm, -1, 3)
     used = int(min(pt.shape[1], np.max(np.sum(pt[:, :, 0] > 0, axis=1))))
     res["pages"] = page_stats(pt, used)
+    res["issue"] = issue_idle(tr, pt[:, :used], plan)
     if args.save:
         np.savez_compressed(args.save, trace=tr, ptrace=pt[:, :used], plan=plan)
     print(json.dumps(res, indent=1))
