@@ -35,3 +35,41 @@ def test_recorded_traffic_is_tied_to_the_code(tmp_path, monkeypatch):
     assert bench.recorded_traffic("old", "megakernel") is None  # taken on other code
     assert bench.recorded_traffic("missing", "megakernel") is None
     assert bench.recorded_traffic("w", "chain") is None
+
+
+def test_clock_summary_reads_samples_inside_the_timed_region(monkeypatch):
+    # no nvidia-smi here: the sampler still records marks and parses what its
+    # output file holds; samples outside the marks are ignored, "Not Active"
+    # is not a throttle reason
+    import subprocess
+    import time as _time
+
+    def no_smi(*a, **k):
+        raise OSError("no nvidia-smi")
+
+    monkeypatch.setattr(subprocess, "Popen", no_smi)
+    cs = bench.ClockSampler(0)
+    assert cs.proc is None
+    t0 = _time.time()
+    cs.marks = [t0, t0 + 10.0]
+
+    def stamp(t):
+        lt = _time.localtime(t)
+        return _time.strftime("%Y/%m/%d %H:%M:%S", lt) + ".500"
+
+    rows = [
+        (t0 - 60, 900, "Active", "Not Active"),      # before the timed region: ignored
+        (t0 + 1, 2070, "Not Active", "Not Active"),
+        (t0 + 2, 2070, "Not Active", "Active"),      # power cap during the region
+        (t0 + 3, 2055, "Not Active", "Not Active"),
+        (t0 + 60, 500, "Active", "Not Active"),      # after: ignored
+    ]
+    with open(cs.out.name, "w") as f:
+        for t, mhz, hw, cap in rows:
+            f.write(f"{stamp(t)}, 0, {mhz}, 2070, 900.0, 0x0, {hw}, Not Active, Not Active, {cap}\n")
+    cs.stop()
+    r = cs.summary()
+    assert r["samples"] == 3
+    assert r["sm_mhz"] == 2070
+    assert r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"]
