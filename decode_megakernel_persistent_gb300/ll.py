@@ -248,8 +248,30 @@ def ll_free(h) -> None:
         lib().ll_free(h)
 
 
+def _need(t, name: str, dtype, min_numel: int, device, optional: bool = True) -> None:
+    """The library takes raw device pointers and cannot see a buffer's size, so
+    the buffers a step writes or reads are checked here: a CUDA tensor of the
+    right dtype on the decoder's device, contiguous, with room for min_numel
+    elements (raises LLError(LL_ERR_ARG) before anything is launched)."""
+    if t is None:
+        if optional:
+            return
+        raise LLError(LL_ERR_ARG, f"{name} is required")
+    if not getattr(t, "is_cuda", False):
+        raise LLError(LL_ERR_ARG, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise LLError(LL_ERR_ARG, f"{name} must be {dtype}, not {t.dtype}")
+    if device is not None and t.device != device:
+        raise LLError(LL_ERR_ARG, f"{name} is on {t.device}, the decoder on {device}")
+    if not t.is_contiguous():
+        raise LLError(LL_ERR_ARG, f"{name} must be contiguous")
+    if t.numel() < min_numel:
+        raise LLError(LL_ERR_ARG, f"{name} holds {t.numel()} elements, the call needs {min_numel}")
+
+
 class Decoder:
-    """Owns a handle plus references to the tensors it points into."""
+    """Owns a handle plus references to the tensors it points into. Its step
+    methods check the buffers they are given (_need) before the library call."""
 
     def __init__(self, shape, weights: dict, k_cache, v_cache, max_seq: int,
                  backend: int = LL_BACKEND_MEGAKERNEL, stream=None):
@@ -259,15 +281,28 @@ class Decoder:
         self.k_cache, self.v_cache = k_cache, v_cache
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         self.cfg = make_config(shape, max_seq, backend)
+        self.device = getattr(weights["embed"], "device", None)
         self.handle = ll_init(self.cfg, weights, k_cache, v_cache, self.stream)
 
+    def _bufs(self, token_dev, logits, n_logits: int, out, n_out: int) -> None:
+        import torch
+        V = int(self.shape.vocab)
+        if token_dev is not None:
+            _need(token_dev, "token_dev", torch.int32, 1, self.device, optional=False)
+        _need(logits, "logits", torch.float32, n_logits * V, self.device)
+        _need(out, "next-token buffer", torch.int32, n_out, self.device)
+
     def step(self, token: int, pos: int, logits=None) -> int:
+        self._bufs(None, logits, 1, None, 0)
         return ll_decode_step(self.handle, token, pos, logits)
 
     def step_async(self, token_dev, pos: int, logits, next_token_dev) -> None:
+        self._bufs(token_dev, logits, 1, next_token_dev, 1)
         ll_decode_step_async(self.handle, token_dev, pos, logits, next_token_dev)
 
     def steps(self, token_dev, pos: int, n_steps: int, logits, tokens_dev) -> None:
+        n = max(int(n_steps), 0)
+        self._bufs(token_dev, logits, n, tokens_dev, n)
         ll_decode_steps(self.handle, token_dev, pos, n_steps, logits, tokens_dev)
 
     def synchronize(self) -> None:
