@@ -269,13 +269,49 @@ def _need(t, name: str, dtype, min_numel: int, device, optional: bool = True) ->
         raise LLError(LL_ERR_ARG, f"{name} holds {t.numel()} elements, the call needs {min_numel}")
 
 
+def check_model(shape, weights: dict, k_cache, v_cache, max_seq: int) -> None:
+    """The weights and caches ll_init will read, against the shape: every tensor a
+    contiguous CUDA bf16 tensor on the embedding's device with exactly the
+    elements of its matrix or vector (per-layer lists n_layers long), and the
+    caches room for [n_layers][n_kv_heads][max_seq][head_dim] (raises
+    LLError(LL_ERR_ARG) naming the first misfit)."""
+    import torch
+    H, V, I, L = int(shape.hidden), int(shape.vocab), int(shape.inter), int(shape.n_layers)
+    q, kv = int(shape.n_q_heads) * int(shape.head_dim), int(shape.n_kv_heads) * int(shape.head_dim)
+    dev = getattr(weights.get("embed"), "device", None)
+
+    def exact(t, name, n):
+        _need(t, name, torch.bfloat16, n, dev, optional=False)
+        if t.numel() != n:
+            raise LLError(LL_ERR_ARG, f"{name} holds {t.numel()} elements, the shape has {n}")
+
+    exact(weights.get("embed"), "embed", V * H)
+    exact(weights.get("final_norm"), "final_norm", H)
+    if not shape.tied:
+        exact(weights.get("lm_head"), "lm_head", V * H)
+    per_layer = {"attn_norm": H, "wq": q * H, "wk": kv * H, "wv": kv * H, "wo": H * q,
+                 "mlp_norm": H, "wg": I * H, "wu": I * H, "wd": H * I}
+    for key, n in per_layer.items():
+        ts = weights.get(key)
+        if ts is None or len(ts) != L:
+            raise LLError(LL_ERR_ARG, f"{key} must list one tensor per layer ({L})")
+        for i, t in enumerate(ts):
+            exact(t, f"{key}[{i}]", n)
+    cache = L * kv * int(max_seq)
+    _need(k_cache, "k_cache", torch.bfloat16, cache, dev, optional=False)
+    _need(v_cache, "v_cache", torch.bfloat16, cache, dev, optional=False)
+
+
 class Decoder:
-    """Owns a handle plus references to the tensors it points into. Its step
-    methods check the buffers they are given (_need) before the library call."""
+    """Owns a handle plus references to the tensors it points into. The model's
+    tensors are checked at construction (check_model) and the buffers of every
+    step before its library call (_need)."""
 
     def __init__(self, shape, weights: dict, k_cache, v_cache, max_seq: int,
                  backend: int = LL_BACKEND_MEGAKERNEL, stream=None):
         import torch
+        self.handle = None
+        check_model(shape, weights, k_cache, v_cache, max_seq)
         self.shape = shape
         self.weights = weights
         self.k_cache, self.v_cache = k_cache, v_cache

@@ -48,3 +48,46 @@ def test_refuses_bad_buffers():
     assert "cuda:1" in refused(FakeCuda(10, device="cuda:1"))        # other device
     assert "contiguous" in refused(FakeCuda(10, contiguous=False))
     assert "needs 10" in refused(FakeCuda(9))                        # one element short
+
+
+def fake_model(shape, max_seq):
+    H, V, I, L = shape.hidden, shape.vocab, shape.inter, shape.n_layers
+    q, kv = shape.n_q_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
+    bf = torch.bfloat16
+    w = {"embed": FakeCuda(V * H, bf), "final_norm": FakeCuda(H, bf)}
+    if not shape.tied:
+        w["lm_head"] = FakeCuda(V * H, bf)
+    per = {"attn_norm": H, "wq": q * H, "wk": kv * H, "wv": kv * H, "wo": H * q,
+           "mlp_norm": H, "wg": I * H, "wu": I * H, "wd": H * I}
+    for k, n in per.items():
+        w[k] = [FakeCuda(n, bf) for _ in range(L)]
+    cache = L * kv * max_seq
+    return w, FakeCuda(cache, bf), FakeCuda(cache, bf)
+
+
+@pytest.mark.parametrize("name", ["llama-3.2-1b", "llama-3.1-8b"])
+def test_model_check_accepts_the_shapes(name):
+    from decode_megakernel_persistent_gb300 import synth
+    shape = {s.name: s for s in (synth.LLAMA_1B, synth.LLAMA_8B)}[name]
+    w, k, v = fake_model(shape, 1100)
+    ll.check_model(shape, w, k, v, 1100)
+
+
+def test_model_check_refuses_misfits():
+    from decode_megakernel_persistent_gb300 import synth
+    shape = synth.LLAMA_8B  # untied: the LM head is checked too
+
+    def refused(mutate, max_seq=64):
+        w, k, v = fake_model(shape, 64)
+        mutate(w, k, v)
+        with pytest.raises(ll.LLError) as e:
+            ll.check_model(shape, w, k, v, max_seq)
+        assert e.value.code == ll.LL_ERR_ARG
+        return str(e.value)
+
+    bf = torch.bfloat16
+    assert "wd[3]" in refused(lambda w, k, v: w["wd"].__setitem__(3, FakeCuda(shape.hidden * shape.inter - 1, bf)))
+    assert "wo[0]" in refused(lambda w, k, v: w["wo"].__setitem__(0, FakeCuda(shape.hidden * 4096, torch.float16)))
+    assert "lm_head" in refused(lambda w, k, v: w.pop("lm_head"))
+    assert "one tensor per layer" in refused(lambda w, k, v: w["wq"].pop())
+    assert "k_cache" in refused(lambda w, k, v: None, max_seq=65)  # caches sized for 64 positions
