@@ -320,13 +320,13 @@ class Decoder:
         self.device = getattr(weights["embed"], "device", None)
         self.handle = ll_init(self.cfg, weights, k_cache, v_cache, self.stream)
 
-    def _bufs(self, token_dev, logits, n_logits: int, out, n_out: int) -> None:
+    def _bufs(self, token_dev, logits, n_logits: int, out, n_out: int, out_required: bool = False) -> None:
         import torch
         V = int(self.shape.vocab)
         if token_dev is not None:
             _need(token_dev, "token_dev", torch.int32, 1, self.device, optional=False)
         _need(logits, "logits", torch.float32, n_logits * V, self.device)
-        _need(out, "next-token buffer", torch.int32, n_out, self.device)
+        _need(out, "next-token buffer", torch.int32, n_out, self.device, optional=not out_required)
 
     def step(self, token: int, pos: int, logits=None) -> int:
         self._bufs(None, logits, 1, None, 0)
@@ -338,7 +338,7 @@ class Decoder:
 
     def steps(self, token_dev, pos: int, n_steps: int, logits, tokens_dev) -> None:
         n = max(int(n_steps), 0)
-        self._bufs(token_dev, logits, n, tokens_dev, n)
+        self._bufs(token_dev, logits, n, tokens_dev, n, out_required=True)
         ll_decode_steps(self.handle, token_dev, pos, n_steps, logits, tokens_dev)
 
     def synchronize(self) -> None:
