@@ -44,7 +44,8 @@ def summarize(trace: np.ndarray, plan: np.ndarray) -> dict:
             rec["to_first_page_us"] = float(np.mean((f1 - r)[had])) / 1e3
             rec["compute_us"] = float(np.mean((cd - f1)[had])) / 1e3
             rec["after_compute_us"] = float(np.mean((pg - cd)[had])) / 1e3
-        if name == "attn":
+        if name == "attn" and (trace[:, :, 10][m] > 0).any():
+            # phase stamps of the block-softmax variant (the per-warp one leaves them 0)
             sub = trace[:, :, 10][m] > 0
             rec["scores_us"] = float(np.mean((w8 - f1)[sub])) / 1e3
             rec["softmax_us"] = float(np.mean((w9 - w8)[sub])) / 1e3
