@@ -226,6 +226,16 @@ def oracle_timing(shape, ctx: int, budget_s: float, max_steps: int | None = None
     return n, t_total, oracle.num_threads()
 
 
+def bench_config(wl, steps: int, warmup: int, world: int) -> dict:
+    """The workload both arms report under "config", key for key: the model and
+    context, the K timed greedy steps and their positions (after W warm-up steps),
+    the weight format and how ranks split the work."""
+    pos0 = wl.context + warmup
+    return {"workload": wl.name, "context": wl.context, "decode_steps_timed": steps,
+            "positions": [pos0, pos0 + steps - 1], "weights": "bf16",
+            "parallelism": f"replicas{world}" if world > 1 else "single"}
+
+
 def run_reference(args):
     from decode_megakernel_persistent_gb300 import synth
     world, rank, _ = dist_setup(args)
@@ -245,7 +255,8 @@ def run_reference(args):
         "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * secs / n,
         "us_per_token": 1e6 * secs / n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "context": wl.context, "weights": "bf16"},
+        "config": bench_config(wl, n, args.warmup, world),
+        "method": {"timed": "CPU oracle decode steps (fp32, OpenMP over rows) on a seeded KV cache"},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n} full oracle decode steps at positions {wl.context + args.warmup}.."},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -383,9 +394,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name, "context": ctx, "decode_steps_timed": K,
-                   "positions": [pos0, pos0 + K - 1], "weights": "bf16", "backend": args.backend,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
+        "config": bench_config(wl, K, W, world),
+        "method": {"backend": args.backend,
                    "l2": "inputs larger than L2: every step streams all weights from HBM",
                    "timed": "one ll_decode_steps launch of K greedy steps" if backend == ll.LL_BACKEND_MEGAKERNEL
                    else "ll_decode_steps: K steps of per-operation launches"},

@@ -66,8 +66,6 @@ int upload_schedule(ll_handle *h) {
     return LL_OK;
 }
 
-// KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
-// longest context, at most one attention item per SM.
 // The KV tensor maps of the per-warp attention variant (ll::TM_*): each cache as
 // a 2-D bf16 tensor of head_dim columns and L * n_kv * max_seq rows, boxes of 64
 // columns (128 bytes, the widest the 128-byte swizzle takes) by a page of rows or
@@ -104,12 +102,54 @@ bool encode_kv_maps(const ll_config &c, uint16_t *k_cache, uint16_t *v_cache, ll
     return true;
 }
 
-int attn_splits(const ll_config &c, int nsm) {
-    int per = ll::ATTN_SPLIT_POS;  // tuning knob (environment), read at init
-    if (const char *e = std::getenv("LL_ATTN_SPLIT_POS")) per = std::max(1, std::atoi(e));
-    const int want = (c.max_seq + per - 1) / per;
-    return std::max(1, std::min(want, nsm / c.n_kv_heads));
+// The weight tensor maps of tensor-core pages (ll::wmap_index): each matrix as a
+// 3-D bf16 tensor (64 columns, rows, K / 64 column blocks) with boxes of
+// (64, nr, K / 64) for nr = 1..TC_ROWS, in the 128-byte swizzle, so that one copy
+// brings nr whole rows in the layout the tensor-core page reads. Maps of
+// matrices whose width has no tensor-core geometry stay zero. False if the
+// driver has no encoder or refuses a map.
+bool encode_weight_maps(const ll_config &c, const std::vector<ll::LayerW> &layers, const uint16_t *lm_head,
+                        const ll::MvShape &mh, const ll::MvShape &mq, std::vector<ll::TensorMap> &out) {
+    using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    const auto encode = reinterpret_cast<EncodeTiled>(fn);
+    out.assign(size_t(c.n_layers + 1) * ll::TC_MATS_PER_LAYER * ll::TC_ROWS, ll::TensorMap{});
+    auto one = [&](const uint16_t *w, int64_t rows, int K, int l, int m) -> bool {
+        const cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(K / 64)};
+        const cuuint64_t strides[2] = {cuuint64_t(K) * 2, 128};  // bytes: next row, next 64-column block
+        const cuuint32_t estr[3] = {1, 1, 1};
+        for (int nr = 1; nr <= ll::TC_ROWS; nr++) {
+            const cuuint32_t box[3] = {64, cuuint32_t(nr), cuuint32_t(K / 64)};
+            CUtensorMap map;
+            if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(w), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+            std::memcpy(&out[ll::wmap_index(l, m, nr)], &map, sizeof map);
+        }
+        return true;
+    };
+    const int H = c.hidden, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+    for (int l = 0; l < c.n_layers; l++) {
+        const ll::LayerW &L = layers[l];
+        if (mh.tc && !(one(L.wq, qd, H, l, 0) && one(L.wk, kd, H, l, 1) && one(L.wv, kd, H, l, 2) &&
+                       one(L.wg, c.inter, H, l, 4) && one(L.wu, c.inter, H, l, 5)))
+            return false;
+        if (mq.tc && !one(L.wo, H, qd, l, 3)) return false;
+    }
+    if (mh.tc && !one(lm_head, c.vocab, H, c.n_layers, 0)) return false;
+    return true;
 }
+
+int attn_splits(const ll_config &c, int nsm) { return ll::attn_splits(c.max_seq, c.n_kv_heads, nsm); }
 
 void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::vector<Instr>> &lists) {
     ll::build_schedule(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim, c.inter,
@@ -181,11 +221,21 @@ const char *status_text(int s) {
     switch (s) {
         case LL_ERR_ARG: return "token out of range";
         case LL_ERR_DEP_TIMEOUT: return "a device-side wait ran past its time limit";
+        case LL_ERR_NUMERIC: return "the logits held no orderable value (all NaN): no greedy token";
         default: return "device error";
     }
 }
 
 }  // namespace
+
+namespace ll {
+int attn_splits(int max_seq, int n_kv_heads, int nsm) {
+    int per = ATTN_SPLIT_POS;
+    if (const char *e = std::getenv("LL_ATTN_SPLIT_POS")) per = std::max(1, std::atoi(e));
+    const int want = (max_seq + per - 1) / per;
+    return std::max(1, std::min(want, nsm / n_kv_heads));
+}
+}  // namespace ll
 
 extern "C" {
 
@@ -274,6 +324,23 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         delete h;
         return bad(rc, "cannot keep one megakernel block resident per SM");
     }
+    // Tensor-core pages for the widths that have them (tuning knob LL_MV_TC = 0
+    // keeps every matrix-vector product on the CUDA cores); without their tensor
+    // maps, the CUDA-core pages.
+    std::vector<ll::TensorMap> wmaps;
+    {
+        bool want_tc = true;
+        if (const char *e = std::getenv("LL_MV_TC")) want_tc = std::atoi(e) != 0;
+        ll::MvShape th{}, tq{};
+        const bool tc_h = want_tc && ll::mv_shape_tc(c.hidden, th), tc_q = want_tc && ll::mv_shape_tc(qd, tq);
+        ll::MvShape nh = tc_h ? th : mh, nq = tc_q ? tq : mq;
+        if ((tc_h || tc_q) && encode_weight_maps(c, layers, c.tied ? w->embed : w->lm_head, nh, nq, wmaps)) {
+            mh = nh;
+            mq = nq;
+        } else {
+            wmaps.clear();
+        }
+    }
     build_lists(h);
     for (auto &l : h->lists) h->max_instr = std::max<int>(h->max_instr, static_cast<int>(l.size()));
     std::vector<ll::PDesc> pdesc;
@@ -288,6 +355,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     int32_t *d_n_instr = nullptr;
     ll::LayerW *d_layers = nullptr;
     ll::PDesc *d_pdesc = nullptr;
+    ll::TensorMap *d_wmaps = nullptr;
     int32_t *d_pdesc_off = nullptr;
     float2 *d_rope = nullptr;
     float *x = nullptr, *qkv = nullptr, *part = nullptr, *o = nullptr, *act = nullptr;
@@ -304,6 +372,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&d_n_instr), size_t(h->nsm) * sizeof(int32_t)},
         {reinterpret_cast<void **>(&d_layers), size_t(c.n_layers) * sizeof(ll::LayerW)},
         {reinterpret_cast<void **>(&d_pdesc), pdesc.size() * sizeof(ll::PDesc)},
+        {reinterpret_cast<void **>(&d_wmaps), wmaps.size() * sizeof(ll::TensorMap)},
         {reinterpret_cast<void **>(&d_pdesc_off), pdesc_off.size() * sizeof(int32_t)},
         {reinterpret_cast<void **>(&d_rope), size_t(c.max_seq) * (c.head_dim / 2) * sizeof(float2)},
         {reinterpret_cast<void **>(&x), size_t(c.hidden) * 4},
@@ -401,6 +470,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.mv_h = mh;
     p.mv_q = mq;
     p.mv_i = mi;
+    p.wmaps = wmaps.empty() ? nullptr : d_wmaps;
     p.t_qkv = t_qkv;
     p.t_part = t_part;
     p.t_o = t_o;
@@ -444,11 +514,14 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     cb.act = act;
     cb.logits = logits;
     cb.splits = h->splits;
+    cb.rope_row = nullptr;
 
     bool ok = cudaMemcpy(d_layers, layers.data(), layers.size() * sizeof(ll::LayerW), cudaMemcpyHostToDevice) ==
                   cudaSuccess &&
               cudaMemcpy(d_pdesc, pdesc.data(), pdesc.size() * sizeof(ll::PDesc), cudaMemcpyHostToDevice) ==
                   cudaSuccess &&
+              (wmaps.empty() || cudaMemcpy(d_wmaps, wmaps.data(), wmaps.size() * sizeof(ll::TensorMap),
+                                           cudaMemcpyHostToDevice) == cudaSuccess) &&
               cudaMemcpy(d_pdesc_off, pdesc_off.data(), pdesc_off.size() * sizeof(int32_t), cudaMemcpyHostToDevice) ==
                   cudaSuccess &&
               cudaMemcpy(d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -559,6 +632,7 @@ int ll_query(const ll_handle *h, int what, int64_t *value) {
             *value = h->cfg.backend == LL_BACKEND_CHAIN ? 1 + 13 * int64_t(h->cfg.n_layers) + 3 : 1;
             break;
         case LL_Q_SMEM_BYTES: *value = h->smem_bytes; break;
+        case LL_Q_MV_TC: *value = (h->kp.mv_h.tc ? 1 : 0) | (h->kp.mv_q.tc ? 2 : 0) | (h->kp.mv_i.tc ? 4 : 0); break;
         case LL_Q_TRACE_BYTES:
             *value = (int64_t(h->nsm) * h->max_instr * ll::TRACE_WORDS + int64_t(h->nsm) * ll::PTRACE_PAGES * 3) *
                      int64_t(sizeof(uint64_t));

@@ -93,11 +93,11 @@ __global__ void k_matvec(const uint16_t *__restrict__ W, const float *__restrict
     }
 }
 
-// RoPE on q (in place) and k; k and v rounded to bf16 and stored at pos.
-__global__ void k_rope_kv(float *qkv, const float2 *cs, int pos, int nq, int nkv, int hd,
+// RoPE on q (in place) and k; k and v rounded to bf16 and stored at pos. c is
+// the (cos, sin) row of position pos, hd / 2 entries.
+__global__ void k_rope_kv(float *qkv, const float2 *c, int pos, int nq, int nkv, int hd,
                           uint16_t *kc, uint16_t *vc, size_t layer_base, int max_seq) {
     const int half = hd / 2;
-    const float2 *c = cs + size_t(pos) * half;
     const int total = (nq + nkv) * half;
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total + nkv * hd; t += gridDim.x * blockDim.x) {
         if (t < total) {
@@ -224,8 +224,9 @@ __global__ void k_silu_mul(const float *g, const float *u, float *a, int n) {
     }
 }
 
-// One block: greedy argmax, lowest index on ties.
-__global__ void k_argmax(const float *v, int n, int32_t *next_dev, int32_t *token_out) {
+// One block: greedy argmax, lowest index on ties. Logits that hold no orderable
+// value (all NaN) have no greedy token: the status word records LL_ERR_NUMERIC.
+__global__ void k_argmax(const float *v, int n, int32_t *next_dev, int32_t *token_out, int32_t *status) {
     __shared__ float bv[32];
     __shared__ int bi[32];
     float best = -INFINITY;
@@ -255,6 +256,7 @@ __global__ void k_argmax(const float *v, int n, int32_t *next_dev, int32_t *toke
                 best = bv[w];
                 idx = bi[w];
             }
+        if (idx == 0x7fffffff) atomicCAS(status, 0, LL_ERR_NUMERIC);
         token_out[0] = idx;
         if (next_dev) *next_dev = idx;
     }
@@ -271,6 +273,7 @@ int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream_) {
     cudaStream_t st = static_cast<cudaStream_t>(stream_);
     const int H = p.H, qd = p.nq * p.hd, kd = p.nkv * p.hd, I = p.I, G = p.nq / p.nkv;
     const size_t per_layer = size_t(p.nkv) * p.max_seq * p.hd;
+    const float2 *rope_row = b.rope_row ? b.rope_row : p.rope_cs + size_t(p.pos) * (p.hd / 2);
     auto mv = [&](const uint16_t *W, const float *in, int rows, int K, float *out, int acc) {
         k_matvec<<<grid_for_rows(rows, p.nsm), 256, 0, st>>>(W, in, rows, K, out, acc);
     };
@@ -283,7 +286,7 @@ int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream_) {
         mv(w.wk, b.h, kd, H, b.qkv + qd, 0);
         mv(w.wv, b.h, kd, H, b.qkv + qd + kd, 0);
         k_rope_kv<<<((p.nq + p.nkv) * p.hd / 2 + kd + 255) / 256, 256, 0, st>>>(
-            b.qkv, p.rope_cs, p.pos, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
+            b.qkv, rope_row, p.pos, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
         k_attn_partial<<<dim3(p.nkv, b.splits), 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, p.pos,
                                                              p.max_seq, G, p.hd, b.splits, b.part);
         k_attn_combine<<<(qd + 255) / 256, 256, 0, st>>>(b.part, p.nq, p.hd, b.splits, b.o);
@@ -297,7 +300,7 @@ int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream_) {
     k_rmsnorm<<<1, 1024, 0, st>>>(b.x, p.final_norm, H, p.eps, b.h);
     float *logits = p.logits ? p.logits : b.logits;
     mv(p.lm_head, b.h, p.V, H, logits, 0);
-    k_argmax<<<1, 1024, 0, st>>>(logits, p.V, p.next_token_dev, p.token_out);
+    k_argmax<<<1, 1024, 0, st>>>(logits, p.V, p.next_token_dev, p.token_out, p.status);
     return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 

@@ -1,5 +1,5 @@
 // ll_internal.h -- structures shared by the host runtime (api.cpp, schedule.cpp)
-// and the device code (megakernel.cu, chain.cu) of libll.so.
+// and the device code (megakernel.cuh and its instantiations, chain.cu) of libll.so.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -57,9 +57,15 @@ struct Instr {
 // works on slice w % ws of rows w / ws + q * rg (q < rw) of each of its pages,
 // so ws * rg warps of the team are active and each lane keeps vpl 16-byte
 // vectors of the input in registers.
+//
+// tc = 1 selects the tensor-core page instead (mv_shape_tc): a page holds up to
+// TC_ROWS whole rows, loaded by TMA in the 128-byte swizzle, and all NCW warps
+// work on every page, each on its own K / NCW columns.
 struct MvShape {
-    int32_t K, ws, vpl, rpp, rg, rw, teams;
+    int32_t K, ws, vpl, rpp, rg, rw, teams, tc;
 };
+constexpr int TC_ROWS = 8;        // rows of a tensor-core page (the MMA's n)
+constexpr int TC_MATS_PER_LAYER = 6;  // wq, wk, wv, wo, wg, wu: the matrices whose pages may be tensor-core pages
 
 // One entry of an SM's producer list, in consumption order: a weight page
 // (src, bytes), or an attention item whose K/V pages depend on pos and are
@@ -70,7 +76,15 @@ struct PDesc {
     uint16_t instr;  // index of the instruction the page belongs to
     uint16_t kind;   // PD_WEIGHTS or PD_ATTN
 };
-enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1 };
+enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1, PD_TMA_W = 2 };
+// PD_TMA_W: a tensor-core weight page, src = (tensor map index << 32) | first row.
+// Map index of matrix m (0..5: wq, wk, wv, wo, wg, wu) of layer l, or of the LM
+// head (l = L, m = 0), for a page of nr rows (1..TC_ROWS): every box height has
+// its own map, so that a page never loads rows of another SM's range.
+__host__ __device__ inline uint32_t wmap_index(int l, int m, int nr) {
+    return (uint32_t(l) * TC_MATS_PER_LAYER + uint32_t(m)) * TC_ROWS + uint32_t(nr - 1);
+}
+
 
 // A TMA tensor map (CUtensorMap: 128 opaque bytes, 64-byte aligned), kept as
 // bytes here so that this header needs no driver API types.
@@ -120,6 +134,7 @@ struct KParams {
     int32_t attn_splits;
     int32_t attn_flash;       // kernel variant: per-warp softmax in attention (long items)
     MvShape mv_h, mv_q, mv_i; // input widths hidden, n_q*hd, inter
+    const TensorMap *wmaps;   // weight tensor maps of tensor-core pages (wmap_index), global memory, or null
     // Activations between instructions, as tagged words: (tag << 32) | fp32 bits,
     // stored and loaded as single 8-byte accesses. A reader takes a word only
     // when its tag is the one of the current step and layer (tag_of), so the
@@ -171,7 +186,15 @@ struct ChainBufs {
     const LayerW *host_layers;  // [L], host memory
     float *x, *h, *qkv, *part, *o, *gate, *up, *act, *logits;
     int32_t splits;
+    // the (cos, sin) row of the step's position, or null to take row pos of the
+    // KParams table (rope_cs)
+    const float2 *rope_row;
 };
+
+// KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
+// longest context (tuning knob LL_ATTN_SPLIT_POS, read here), at most one
+// attention item per SM. Every entry point picks its splits with this.
+int attn_splits(int max_seq, int n_kv_heads, int nsm);
 int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
 
 // Host-side schedule construction (schedule.cpp).
@@ -180,6 +203,9 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
 // lane_floats: the most input floats a lane may hold per team copy of the
 // input (16 or 32); more allows more teams (pages in progress at once).
 bool mv_shape(int K, MvShape &m, int lane_floats = 16);
+// The tensor-core geometry for width K, if the kernel has it (K a multiple of 512,
+// at most 2048): pages of TC_ROWS rows, every warp on K / NCW columns of each.
+bool mv_shape_tc(int K, MvShape &m);
 void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector<LayerW> &layers,
                  const uint16_t *lm_head, int H, int qd, int kd, int I, const MvShape &mh, const MvShape &mq,
                  const MvShape &mi, std::vector<PDesc> &out, std::vector<int32_t> &off);

@@ -1,4 +1,5 @@
-// megakernel.cu -- the persistent decode megakernel for sm_103a.
+// megakernel.cuh -- the persistent decode megakernel for sm_103a (device code;
+// mk_cuda_cores.cu and mk_tensor_cores.cu instantiate its kernels).
 //
 // One decode step of a Llama-style decoder runs as one launch of this kernel,
 // one block per SM, following the page "Hazy Research Llama-3.2-1B Megakernel"
@@ -25,6 +26,7 @@
 // between them, so the O projection reads one merged vector; the greedy argmax
 // is reduced by the last SM to finish (an atomic ticket). Every wait is bounded
 // by a time limit.
+#pragma once
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -32,6 +34,8 @@
 #include "ll_internal.h"
 
 namespace ll {
+// Everything here has internal linkage: two translation units instantiate it.
+namespace {
 
 // ---------------------------------------------------------------------------------
 // PTX helpers
@@ -81,12 +85,6 @@ __device__ __forceinline__ uint64_t gtimer() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ int32_t ld_relaxed(const int32_t *p) {
     int32_t v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -133,18 +131,6 @@ __device__ __forceinline__ bool consumer_any(bool v) {
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
 }
 
@@ -633,6 +619,59 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[R]) {
     return v[0];
 }
 
+// The epilogue of a matrix-vector instruction, once every row's result is in
+// s.acc: q/k/v, the residual stream, silu(gate) * up, or the logits and each
+// thread's running argmax, stored as the instruction's outputs. Inlined: as a
+// called function it made the 1B step ~7 % slower (measured).
+__device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr &ins, int ii, float &best,
+                                         int &best_idx) {
+    const int tid = threadIdx.x;
+    const int nrows = ins.r1 - ins.r0;
+    const int r0 = ins.r0;
+    const uint32_t wtag = write_tag(p, s, ins);
+    switch (ins.op) {
+        case OP_QKV:
+            for (int t = tid; t < nrows; t += NCT)
+                if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS))
+                    st_tag(p.t_qkv + r0 + t, s.acc[t], wtag);
+            break;
+        case OP_OPROJ:
+        case OP_DOWN: {
+            // this SM owns rows [r0, r1) of the residual stream in both projections
+            // (same row split), so it keeps them in shared memory across layers
+            const bool from_embed = ins.op == OP_OPROJ && ins.layer == 0;
+            for (int t = tid; t < nrows; t += NCT) {
+                const int row = r0 + t;
+                if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) continue;
+                const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : s.xown[t];
+                const float v = base + s.acc[t];
+                s.xown[t] = v;
+                st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + row, v, wtag);
+            }
+            break;
+        }
+        case OP_GATEUP:
+            for (int t = tid; t < nrows; t += NCT) {
+                const float g = s.acc[t];
+                if (LL_OK_IDX(8, r0 + t, p.I) && LL_OK_IDX(9, nrows + t, ACC_FLOATS))
+                    st_tag(p.t_act + r0 + t, g / (1.0f + expf(-g)) * s.acc[nrows + t], wtag);
+            }
+            break;
+        default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
+            for (int t = tid; t < nrows; t += NCT) {
+                const float y = s.acc[t];
+                if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[r0 + t] = y;
+                if (y > best) {
+                    best = y;
+                    best_idx = r0 + t;
+                }
+            }
+            break;
+    }
+    if (threadIdx.x == 0) trace_put(p, ii, 2);
+}
+
+
 template <int VPL, int RW>
 __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
                          float &best, int &best_idx) {
@@ -739,48 +778,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     }
     if (tid == 0) trace_put(p, ii, 7);
     if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
-    const int r0 = ins.r0;
-    const uint32_t wtag = write_tag(p, s, ins);
-    switch (ins.op) {
-        case OP_QKV:
-            for (int t = tid; t < nrows; t += NCT)
-                if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS))
-                    st_tag(p.t_qkv + r0 + t, s.acc[t], wtag);
-            break;
-        case OP_OPROJ:
-        case OP_DOWN: {
-            // this SM owns rows [r0, r1) of the residual stream in both projections
-            // (same row split), so it keeps them in shared memory across layers
-            const bool from_embed = ins.op == OP_OPROJ && ins.layer == 0;
-            for (int t = tid; t < nrows; t += NCT) {
-                const int row = r0 + t;
-                if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) continue;
-                const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : s.xown[t];
-                const float v = base + s.acc[t];
-                s.xown[t] = v;
-                st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + row, v, wtag);
-            }
-            break;
-        }
-        case OP_GATEUP:
-            for (int t = tid; t < nrows; t += NCT) {
-                const float g = s.acc[t];
-                if (LL_OK_IDX(8, r0 + t, p.I) && LL_OK_IDX(9, nrows + t, ACC_FLOATS))
-                    st_tag(p.t_act + r0 + t, g / (1.0f + expf(-g)) * s.acc[nrows + t], wtag);
-            }
-            break;
-        default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
-            for (int t = tid; t < nrows; t += NCT) {
-                const float y = s.acc[t];
-                if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[r0 + t] = y;
-                if (y > best) {
-                    best = y;
-                    best_idx = r0 + t;
-                }
-            }
-            break;
-    }
-    if (threadIdx.x == 0) trace_put(p, ii, 2);
+    mv_store(p, s, ins, ii, best, best_idx);
     return true;
 }
 
@@ -814,6 +812,8 @@ __device__ void lm_finish(const KParams &p, Smem &s, float best, int best_idx) {
     if (tid == 0) {
         unsigned long long m = 0;
         for (int w = 0; w < NCW; w++) m = s.kred[w] > m ? s.kred[w] : m;
+        // no SM found an orderable logit (all NaN): there is no greedy token
+        if (m == 0) atomicCAS(p.status, 0, LL_ERR_NUMERIC);
         const int32_t tok = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(m & 0xffffffffu));
         p.token_out[0] = tok;
         if (p.tokens_dev) p.tokens_dev[s.c_epoch - p.epoch] = tok;
@@ -1121,19 +1121,6 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     return merge_splits(p, s, g, c, G, hd, tag, wtag);
 }
 
-// Tensor-core step of the attention: D += A * B with A 16 x 16 bf16 (rows g + 8
-// of A are zero, since a KV head has at most 8 query heads), B 16 x 8 bf16, D
-// 16 x 8 fp32 (m16n8k16). Lane (g, t) = (lane / 4, lane % 4) holds A rows g at
-// columns 2t, 2t + 1 (a0) and 2t + 8, 2t + 9 (a2), B rows 2t, 2t + 1 (b0) and
-// 2t + 8, 2t + 9 (b1) of column g, and D row g at columns 2t, 2t + 1 (d0, d1).
-__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-
 // D += A * B, m16n8k16, all four A registers: a0 = (row g, cols 2t, 2t + 1),
 // a1 = (row g + 8, same cols), a2 = (row g, cols 2t + 8, 2t + 9), a3 = (row g + 8,
 // those cols); D: d0, d1 = row g, d2, d3 = row g + 8, at cols 2t, 2t + 1.
@@ -1162,12 +1149,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
 
@@ -1455,6 +1436,209 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     return merge_splits(p, s, g, c, G, hd, tag, wtag);
 }
 
+
+// ---------------------------------------------------------------------------------
+// Tensor-core matrix-vector instructions (widths K with mv.tc: a multiple of 512,
+// at most 2048). A page holds nr <= TC_ROWS whole rows, loaded by one TMA copy of
+// a 3-D view of the matrix (64 columns, rows, K / 64 column blocks) in the
+// 128-byte swizzle: column block o of row r is the 128-byte line o * nr + r of the
+// page, its 16-byte chunk c at chunk c ^ ((o * nr + r) % 8). So the eight rows an
+// ldmatrix reads at one column block fall in eight different bank groups.
+//
+// The product is m16n8k16 with the input as the A operand and the page's rows as
+// B (n = 8 rows): A rows 0, 1, 2 hold three bf16 terms of the input, x = hi + mid
+// + lo to the 24 bits of an fp32 value (one term misses the logits' bar; with two,
+// bf16 roundings of the stored K/V flip measurably more often than with fp32
+// products), rows 3..15 zero; the three cost no more products than one. Warp w
+// takes columns [w K / NCW, (w + 1) K / NCW) of every page, KS k-steps of 16; the
+// NCW partial sums of each row meet in shared memory, and the last warp to finish
+// a page adds them up and releases it.
+
+// The instruction's input as A fragments: lane (g, t) of warp w holds, for its
+// k-step j (columns k0 = 16 (w KS + j) ...), term g (0: hi, 1: mid, 2: lo; 0 for
+// g >= 3) at k0 + 2t, +1 (a0[j]) and k0 + 2t + 8, +9 (a2[j]). The input is staged in
+// s.xin (the previous instruction's tagged words, or the token's embedding row
+// for layer 0), RMS-normed for QKV, gate/up and the LM head.
+template <int KS>
+__device__ bool load_input_tc(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv, uint32_t (&a0)[KS],
+                              uint32_t (&a2)[KS]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int K = mv.K;
+    const uint16_t *gain = norm_gain(p, s, ins);
+    const uint64_t *src = nullptr;
+    uint32_t tag = 0;
+    switch (ins.op) {
+        case OP_QKV:
+            if (ins.layer > 0) {
+                src = p.t_xout;
+                tag = tag_of(p, s, ins.layer - 1);
+            }
+            break;
+        case OP_GATEUP: src = p.t_xmid; tag = tag_of(p, s, ins.layer); break;
+        case OP_LMHEAD: src = p.t_xout; tag = tag_of(p, s, p.L - 1); break;
+        case OP_OPROJ: src = p.t_o; tag = tag_of(p, s, ins.layer); break;
+        default: break;
+    }
+    // this lane's gains, fetched before the wait (weights)
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t gw[KS][2];
+#pragma unroll
+    for (int j = 0; j < KS; j++) {
+        const int k0 = 16 * (warp * KS + j) + 2 * t;
+        gw[j][0] = gain ? __ldg(reinterpret_cast<const uint32_t *>(gain + k0)) : 0x3f803f80u;
+        gw[j][1] = gain ? __ldg(reinterpret_cast<const uint32_t *>(gain + k0 + 8)) : 0x3f803f80u;
+    }
+    if (src) {
+        constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
+        uint64_t w[2 * PAIRS];
+        poll_words(p, s, w, tag, [&](uint64_t (&ww)[2 * PAIRS]) {
+#pragma unroll
+            for (int k = 0; k < PAIRS; k++) {
+                const int i = (tid + k * NCT) * 2;
+                if (i < K) ld_tag2(src + i, ww[2 * k], ww[2 * k + 1]);
+                else ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
+            }
+        });
+#pragma unroll
+        for (int k = 0; k < PAIRS; k++) {
+            const int i = (tid + k * NCT) * 2;
+            if (i < K) {
+                s.xin[i] = tag_val(w[2 * k]);
+                s.xin[i + 1] = tag_val(w[2 * k + 1]);
+            }
+        }
+    } else {
+        const uint16_t *e = p.embed + size_t(s.token) * p.H;
+        for (int i = tid; i < K; i += NCT) s.xin[i] = bf16_to_f(e[i]);
+    }
+    if (consumer_any(s.abort)) return false;  // also publishes s.xin
+    float r = 1.0f;
+    if (gain) {
+        float ss = 0.f;
+        for (int i = tid; i < K; i += NCT) ss = fmaf(s.xin[i], s.xin[i], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) s.nred[warp] = ss;
+        consumer_sync();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; w++) tot += s.nred[w];
+        r = 1.0f / sqrtf(tot / static_cast<float>(K) + p.eps);
+    }
+#pragma unroll
+    for (int j = 0; j < KS; j++) {
+        const int k0 = 16 * (warp * KS + j) + 2 * t;
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const float2 x = *reinterpret_cast<const float2 *>(&s.xin[k0 + 8 * h]);
+            const float v0 = gain ? x.x * r * bf_lo(gw[j][h]) : x.x;
+            const float v1 = gain ? x.y * r * bf_hi(gw[j][h]) : x.y;
+            // term g of v0 and v1: the bf16 nearest to what the terms before it leave
+            float r0 = v0, r1 = v1;
+            uint16_t t0 = 0, t1 = 0;
+            for (int k = 0; k <= g && k < 3; k++) {
+                t0 = f_to_bf16(r0);
+                t1 = f_to_bf16(r1);
+                r0 -= bf16_to_f(t0);
+                r1 -= bf16_to_f(t1);
+            }
+            packed[h] = g < 3 ? (uint32_t(t0) | (uint32_t(t1) << 16)) : 0u;
+        }
+        a0[j] = packed[0];
+        a2[j] = packed[1];
+    }
+    // s.acc shares space with s.xin: every warp holds its fragments before any
+    // row result is written
+    consumer_sync();
+    return true;
+}
+
+template <int KS>
+__device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
+                            float &best, int &best_idx) {
+    static_assert(KS % 2 == 0, "an ldmatrix.x4 covers two k-steps");
+    const MvShape &mv = mv_of(p, ins.op);
+    Seg seg[3];
+    const int nseg = mv_segments(p, s, ins, seg);
+    if (nseg == 0) return true;  // no rows here: nothing to read or wait for
+    uint32_t a0[KS], a2[KS];
+    if (!load_input_tc<KS>(p, s, ins, mv, a0, a2)) return false;
+    if (threadIdx.x == 0) trace_put(p, ii, 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int nrows = ins.r1 - ins.r0;
+    const int q = lane >> 3, rr = lane & 7;  // the ldmatrix matrix and row this lane addresses
+    const uint32_t zrow = smem_addr(s.zrow);
+    bool bad = false;
+    for (int si = 0; si < nseg; si++) {
+        const Seg sg = seg[si];
+        const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
+        for (int pr = 0; pr < sg.nrows; pr += TC_ROWS) {
+            const int nr = min(TC_ROWS, sg.nrows - pr);
+            const uint32_t slot = cpage % NPAGES;
+            const uint32_t this_page = cpage++;
+            if (bad || !wait_page(p, s, this_page)) {
+                bad = true;
+                continue;
+            }
+            if (warp == 0 && lane == 0) {
+                ptrace_put(p, this_page, 1);
+                if (si == 0 && pr == 0) trace_put(p, ii, 6);
+            }
+            const uint32_t base = smem_addr(pages) + slot * PAGE_BYTES;
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < KS; j += 2) {
+                const int ks = warp * KS + j;  // k-steps ks, ks + 1: columns 16 ks .. 16 ks + 31
+                const int o = ks >> 2;         // their 64-column block
+                const int line = o * nr + rr;
+                const uint32_t chunk = uint32_t((ks & 3) * 2 + q);
+                const uint32_t at = rr < nr ? base + uint32_t(line) * 128u + ((chunk ^ uint32_t(line & 7)) << 4) : zrow;
+                uint32_t b[4] = {0u, 0u, 0u, 0u};
+                if (at == zrow || LL_OK_IDX(21, at + 16 - smem_addr(pages), NPAGES * PAGE_BYTES + 1)) ldsm_x4(at, b);
+                mma_16816(d, make_uint4(a0[j], 0u, a2[j], 0u), b[0], b[1]);
+                mma_16816(e, make_uint4(a0[j + 1], 0u, a2[j + 1], 0u), b[2], b[3]);
+            }
+            // D: lane (g, t) holds term g's sums for page rows 2t, 2t + 1; add the
+            // terms (lanes t, t + 4, t + 8; lanes t + 12 hold zeros)
+            float v0 = d[0] + e[0], v1 = d[1] + e[1];
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 4);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 4);
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 8);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 8);
+            if (lane < 4) {
+                s.part[slot][warp * TC_ROWS + 2 * lane] = v0;
+                s.part[slot][warp * TC_ROWS + 2 * lane + 1] = v1;
+            }
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&s.pcnt[slot], 1) == NCW - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {  // this warp finishes the page: the NCW partials of every row
+                __threadfence_block();
+                if (lane < nr) {
+                    float y = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NCW; w++) y += s.part[slot][w * TC_ROWS + lane];
+                    if (LL_OK_IDX(4, acc0 + pr + lane, ACC_FLOATS)) s.acc[acc0 + pr + lane] = y;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    s.pcnt[slot] = 0;
+                    ptrace_put(p, this_page, 2);
+                    mbar_arrive(&s.empty[slot]);
+                }
+            }
+        }
+    }
+    if (tid == 0) trace_put(p, ii, 7);
+    if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
+    mv_store(p, s, ins, ii, best, best_idx);
+    return true;
+}
+
 // FLASH: the kernel variant for long attention items (see attn_tiles); the other
 // variant keeps a block-wide softmax per page, cheaper when an item spans a page
 // or two. The host picks the variant by the longest item at max_seq.
@@ -1497,11 +1681,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const TensorMap *map, int
         : "memory");
 }
 
+// TMA tensor copy of one box of a 3-D tensor map (x, y, z coordinates) into
+// shared memory, with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const TensorMap *map, int x, int y, int z, uint64_t *bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // The producer thread walks its SM's host-built page list (weight pages with
 // their addresses, attention items expanded from pos here), so that issuing a
 // page costs it only a few instructions: it shares its scheduler with consumer
 // warps and gets a small share of the issue slots.
-template <bool FLASH>
+template <bool FLASH, bool TC>
 __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
     const PDesc *dl = p.pdesc + p.pdesc_off[blockIdx.x];
     const int nd = p.pdesc_off[blockIdx.x + 1] - p.pdesc_off[blockIdx.x];
@@ -1571,6 +1766,9 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                         src1 = p.v_cache + (head_row + size_t(a_p0)) * p.hd;
                     }
                     a_p0 += a_n;
+                } else if (TC && e.kind == PD_TMA_W) {
+                    src0 = nullptr;  // the tensor map and row are in e.src
+                    b0 = e.bytes;
                 } else {
                     src0 = reinterpret_cast<const void *>(e.src);
                     b0 = e.bytes;
@@ -1627,6 +1825,11 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                                                 &s.full[slot]);
                             }
                         }
+                } else if (TC && e.kind == PD_TMA_W) {
+                    // a tensor-core page: rows [row, row + nr) of a matrix, swizzled (see mv_instr_tc)
+                    const TensorMap *map = p.wmaps + (e.src >> 32);
+                    const int row = int(uint32_t(e.src & 0xffffffffu));
+                    tma_load_3d_hint(dst, map, 0, row, 0, &s.full[slot], evict_first);
                 } else {
                     if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
                     else bulk_load(dst, src0, b0, &s.full[slot]);
@@ -1638,7 +1841,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                 }
                 trace_put(p, e.instr, 5);
                 ++ppage;
-                if (e.kind == PD_WEIGHTS) break;
+                if (e.kind != PD_ATTN) break;
             }
         }
     }
@@ -1658,6 +1861,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
         }
     }
 }
+
 
 // The step the consumers start: its epoch, position and logits, and for every
 // step after the first of a launch the token the previous step chose, read from
@@ -1684,7 +1888,7 @@ __device__ bool consumer_step_begin(const KParams &p, Smem &s, int st) {
     return !consumer_any(s.abort);
 }
 
-template <bool FLASH>
+template <bool FLASH, bool TC>
 __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const Instr *list, int n, uint32_t &cpage) {
     float best = -INFINITY;
     int best_idx = -1;
@@ -1694,6 +1898,14 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
         bool ok;
         if (ins.op == OP_ATTN) {
             ok = attn_instr<FLASH>(p, s, pages, ins, i, cpage);
+        } else if (TC && mv_of(p, ins.op).tc) {
+            switch (mv_of(p, ins.op).K) {
+                case 512: ok = mv_instr_tc<2>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                case 1024: ok = mv_instr_tc<4>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                case 2048: ok = mv_instr_tc<8>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
+            }
+            if (ok && ins.op == OP_LMHEAD) lm_finish(p, s, best, best_idx);
         } else {
             const MvShape &mv = mv_of(p, ins.op);
             switch (mv.vpl * 16 + mv.rw) {
@@ -1714,19 +1926,23 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
     return true;
 }
 
-template <bool FLASH>
+template <bool FLASH, bool TC>
 __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
     const int n = p.n_instr[blockIdx.x];
     uint32_t cpage = 0;
     for (int st = 0; st < p.n_steps; st++) {
         if (!consumer_step_begin(p, s, st)) return;
-        if (!consumer_step<FLASH>(p, s, pages, list, n, cpage)) return;
+        if (!consumer_step<FLASH, TC>(p, s, pages, list, n, cpage)) return;
     }
 }
 
-
-template <bool FLASH>
+// FLASH: the attention variant (see attn_instr). TC: the kernel takes the widths
+// whose mv.tc is set on tensor-core pages; without it those widths never reach
+// it (the host launches the TC kernel exactly when a width has mv.tc), so the
+// CUDA-core kernel carries none of that code: its size matters, the step being
+// sensitive to instruction-cache misses when the instruction kind changes.
+template <bool FLASH, bool TC>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *pages = smem;
@@ -1744,8 +1960,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         s.token = p.token_dev ? *p.token_dev : p.token;
         s.tok_step = 0;
         s.start_status = ld_relaxed(p.status);
-        // the swizzled KV pages of the per-warp attention need 1024-byte aligned slots
-        if (FLASH && (smem_addr(pages) & 1023u) != 0) {
+        // swizzled pages (the per-warp attention's KV, tensor-core weight pages) need
+        // 1024-byte aligned slots
+        if ((FLASH || p.wmaps) && (smem_addr(pages) & 1023u) != 0) {
             atomicCAS(p.status, 0, LL_ERR_DEVICE);
             s.start_status = LL_ERR_DEVICE;
         }
@@ -1765,35 +1982,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         return;
     }
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) producer<FLASH>(p, s, pages);
+        if (threadIdx.x == NCT) producer<FLASH, TC>(p, s, pages);
     } else {
-        consumer<FLASH>(p, s, pages);
+        consumer<FLASH, TC>(p, s, pages);
     }
 }
 
-int megakernel_smem_bytes() { return SMEM_BYTES; }
-
-int megakernel_prepare(int smem_bytes) {
-    const void *fns[2] = {reinterpret_cast<const void *>(decode_megakernel<false>),
-                          reinterpret_cast<const void *>(decode_megakernel<true>)};
-    for (const void *fn : fns) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (e != cudaSuccess) return LL_ERR_CUDA;
-        int blocks = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, NTHREADS, smem_bytes);
-        if (e != cudaSuccess) return LL_ERR_CUDA;
-        if (blocks < 1) return LL_ERR_DEVICE;
-    }
-    return LL_OK;
-}
-
-int launch_megakernel(const KParams &p, void *stream, int smem_bytes) {
-    void *args[] = {const_cast<KParams *>(&p)};
-    const void *fn = p.attn_flash ? reinterpret_cast<const void *>(decode_megakernel<true>)
-                                  : reinterpret_cast<const void *>(decode_megakernel<false>);
-    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(p.nsm), dim3(NTHREADS), args, size_t(smem_bytes),
-                                                static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
-}
-
+}  // namespace
 }  // namespace ll

@@ -83,6 +83,12 @@ static bool mv_combo_ok(int vpl, int rw) {
     return false;
 }
 
+bool mv_shape_tc(int K, MvShape &m) {
+    if (K <= 0 || K % (32 * NCW) != 0 || K > 2048) return false;
+    m = MvShape{K, NCW, 0, TC_ROWS, 1, TC_ROWS, 1, 1};
+    return true;
+}
+
 bool mv_shape(int K, MvShape &m, int lane_floats) {
     if (K <= 0 || K % 256 != 0 || K > 16384) return false;
     const int rows_fit = PAGE_BYTES / (2 * K);
@@ -105,7 +111,7 @@ bool mv_shape(int K, MvShape &m, int lane_floats) {
         if (active > best_active || (active == best_active && rpp > best_rpp)) {
             best_active = active;
             best_rpp = rpp;
-            m = MvShape{K, ws, vpl, rpp, rg, rw, teams};
+            m = MvShape{K, ws, vpl, rpp, rg, rw, teams, 0};
         }
     }
     return best_active > 0;
@@ -118,14 +124,21 @@ void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector
                  const MvShape &mi, std::vector<PDesc> &out, std::vector<int32_t> &off) {
     out.clear();
     off.assign(lists.size() + 1, 0);
-    auto pages = [&](const uint16_t *w, int row0, int nrows, const MvShape &mv, int instr) {
+    // pages of a segment: rows [row0, row0 + nrows) of matrix w; tensor-core
+    // pages name the matrix's tensor map (layer l, matrix m) instead of an address
+    auto pages = [&](const uint16_t *w, int row0, int nrows, const MvShape &mv, int instr, int l, int m) {
         for (int pr = 0; pr < nrows; pr += mv.rpp) {
             const int nr = std::min(mv.rpp, nrows - pr);
             PDesc d{};
-            d.src = reinterpret_cast<unsigned long long>(w + size_t(row0 + pr) * mv.K);
+            if (mv.tc) {
+                d.src = (static_cast<unsigned long long>(wmap_index(l, m, nr)) << 32) | uint32_t(row0 + pr);
+                d.kind = PD_TMA_W;
+            } else {
+                d.src = reinterpret_cast<unsigned long long>(w + size_t(row0 + pr) * mv.K);
+                d.kind = PD_WEIGHTS;
+            }
             d.bytes = uint32_t(nr) * uint32_t(mv.K) * 2u;
             d.instr = static_cast<uint16_t>(instr);
-            d.kind = PD_WEIGHTS;
             out.push_back(d);
         }
     };
@@ -151,17 +164,17 @@ void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector
                     const uint16_t *m[3] = {lw->wq, lw->wk, lw->wv};
                     for (int k = 0; k < 3; k++) {
                         const int a = std::max(r0, b[k]), e = std::min(r1, b[k + 1]);
-                        if (a < e) pages(m[k], a - b[k], e - a, mh, int(i));
+                        if (a < e) pages(m[k], a - b[k], e - a, mh, int(i), in.layer, k);
                     }
                     break;
                 }
-                case OP_OPROJ: pages(lw->wo, r0, r1 - r0, mq, int(i)); break;
+                case OP_OPROJ: pages(lw->wo, r0, r1 - r0, mq, int(i), in.layer, 3); break;
                 case OP_GATEUP:
-                    pages(lw->wg, r0, r1 - r0, mh, int(i));
-                    pages(lw->wu, r0, r1 - r0, mh, int(i));
+                    pages(lw->wg, r0, r1 - r0, mh, int(i), in.layer, 4);
+                    pages(lw->wu, r0, r1 - r0, mh, int(i), in.layer, 5);
                     break;
-                case OP_DOWN: pages(lw->wd, r0, r1 - r0, mi, int(i)); break;
-                default: pages(lm_head, r0, r1 - r0, mh, int(i)); break;
+                case OP_DOWN: pages(lw->wd, r0, r1 - r0, mi, int(i), in.layer, 0); break;
+                default: pages(lm_head, r0, r1 - r0, mh, int(i), int(layers.size()), 0); break;
             }
         }
     }

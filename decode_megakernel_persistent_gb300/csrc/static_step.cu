@@ -130,9 +130,8 @@ extern "C" int ll_decode_step_static(const ll_config *cfg, const ll_weights *w, 
     DeviceSetup ds;
     int rc = setup_device(dev, ds, err, err_len);
     if (rc != LL_OK) return rc;
-    // KV splits as the handle path picks them: about ATTN_SPLIT_POS positions each
-    const int splits = std::max(1, std::min((c.max_seq + ll::ATTN_SPLIT_POS - 1) / ll::ATTN_SPLIT_POS,
-                                            ds.nsm / c.n_kv_heads));
+    // KV splits as the handle path picks them
+    const int splits = ll::attn_splits(c.max_seq, c.n_kv_heads, ds.nsm);
     const size_t F = sizeof(float);
     const size_t sz[] = {
         round256(size_t(c.hidden) * F),                                           // x
@@ -172,6 +171,7 @@ extern "C" int ll_decode_step_static(const ll_config *cfg, const ll_weights *w, 
     cb.logits = reinterpret_cast<float *>(take(sz[8]));
     cb.splits = splits;
     float2 *rope_row = reinterpret_cast<float2 *>(take(sz[9]));
+    cb.rope_row = rope_row;  // the per-operation RoPE kernel reads this row as given
     int32_t *words = reinterpret_cast<int32_t *>(take(sz[10]));  // [0] status, [1] next token
 
     // RoPE (cos, sin) of position pos, in double as ll_init builds its table
@@ -189,11 +189,7 @@ extern "C" int ll_decode_step_static(const ll_config *cfg, const ll_weights *w, 
     p.final_norm = w->final_norm;
     p.k_cache = k_cache;
     p.v_cache = v_cache;
-    // The per-operation RoPE kernel reads row pos of a [max_seq][hd/2] table;
-    // only that row exists here, so the base handed over sits pos rows before it
-    // (an address computed in integers, never dereferenced outside the row).
-    p.rope_cs = reinterpret_cast<const float2 *>(reinterpret_cast<uintptr_t>(rope_row) -
-                                                 uintptr_t(pos) * uintptr_t(half) * sizeof(float2));
+    p.rope_cs = nullptr;  // no table here: cb.rope_row holds the one row the step needs
     p.L = c.n_layers;
     p.H = c.hidden;
     p.nq = c.n_q_heads;

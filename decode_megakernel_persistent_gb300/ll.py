@@ -17,6 +17,7 @@ LL_ERR_CUDA = -3
 LL_ERR_DEP_TIMEOUT = -4
 LL_ERR_OOM = -5
 LL_ERR_DEVICE = -6
+LL_ERR_NUMERIC = -7
 
 LL_BACKEND_MEGAKERNEL = 0
 LL_BACKEND_CHAIN = 1
@@ -30,6 +31,7 @@ LL_Q_MAX_INSTRS = 5
 LL_Q_LAUNCHES_PER_STEP = 6
 LL_Q_SMEM_BYTES = 7
 LL_Q_TRACE_BYTES = 8
+LL_Q_MV_TC = 9
 
 LL_STATIC_SCRATCH_BYTES = 4194304
 LL_STATIC_MAX_LAYERS = 256
@@ -225,6 +227,7 @@ def ll_decode_step_static(cfg: ll_config, weights: dict, k_cache, v_cache, token
     """One decode step without a handle and without device allocation; returns the
     greedy next token. ``stream`` is a torch.cuda.Stream or None for torch's current one."""
     import torch
+    check_static_args(cfg, weights, k_cache, v_cache, logits)
     if stream is None:
         stream = torch.cuda.current_stream()
     w, keep = _weights_struct(weights)
@@ -300,6 +303,31 @@ def check_model(shape, weights: dict, k_cache, v_cache, max_seq: int) -> None:
     cache = L * kv * int(max_seq)
     _need(k_cache, "k_cache", torch.bfloat16, cache, dev, optional=False)
     _need(v_cache, "v_cache", torch.bfloat16, cache, dev, optional=False)
+
+
+def check_static_args(cfg: ll_config, weights: dict, k_cache, v_cache, logits) -> None:
+    """What ll_decode_step_static will read and write, against cfg: one tensor per
+    layer in every per-layer list (the C side walks n_layers entries of each),
+    every weight of its exact size, caches with room for
+    [n_layers][n_kv_heads][max_seq][head_dim], logits (if given) with room for
+    vocab floats, all on one device, and that device torch's current one, which
+    the library sets up from cudaGetDevice (raises LLError(LL_ERR_ARG))."""
+    import types
+
+    import torch
+    L = int(cfg.n_layers)
+    for key in LAYER_KEYS:
+        ts = weights.get(key)
+        if ts is None or len(ts) != L:
+            raise LLError(LL_ERR_ARG, f"{key} must list one tensor per layer ({L})")
+    shape = types.SimpleNamespace(**{n: int(getattr(cfg, n)) for n in (
+        "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "inter", "vocab")}, tied=bool(cfg.tied))
+    check_model(shape, weights, k_cache, v_cache, int(cfg.max_seq))
+    dev = weights["embed"].device
+    _need(logits, "logits", torch.float32, int(cfg.vocab), dev)
+    cur = torch.device("cuda", torch.cuda.current_device())
+    if dev != cur:
+        raise LLError(LL_ERR_ARG, f"the tensors are on {dev}, torch's current device is {cur}")
 
 
 class Decoder:

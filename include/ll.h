@@ -46,6 +46,7 @@ extern "C" {
 #define LL_ERR_DEP_TIMEOUT (-4)  /* a device-side wait ran past its time limit; the step was abandoned */
 #define LL_ERR_OOM (-5)          /* library scratch could not be allocated */
 #define LL_ERR_DEVICE (-6)       /* device is not sm_103 or cannot co-schedule one block per SM */
+#define LL_ERR_NUMERIC (-7)      /* the logits held no orderable value (all NaN): no greedy token */
 
 #define LL_BACKEND_MEGAKERNEL 0  /* one persistent kernel per decode step */
 #define LL_BACKEND_CHAIN 1       /* one kernel per operation, for comparison */
@@ -174,6 +175,7 @@ int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
 #define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes (ll_decode_steps: one launch for all its steps) */
 #define LL_Q_SMEM_BYTES 7       /* dynamic shared memory per block */
 #define LL_Q_TRACE_BYTES 8      /* size of the buffer ll_set_trace needs */
+#define LL_Q_MV_TC 9            /* matrix-vector widths on tensor-core pages: bit 0 hidden, bit 1 n_q*head_dim, bit 2 inter */
 int ll_query(const ll_handle *h, int what, int64_t *value);
 
 /* Fault injection for tests (host side only; nothing faults on the device):

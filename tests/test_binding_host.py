@@ -91,3 +91,28 @@ def test_model_check_refuses_misfits():
     assert "lm_head" in refused(lambda w, k, v: w.pop("lm_head"))
     assert "one tensor per layer" in refused(lambda w, k, v: w["wq"].pop())
     assert "k_cache" in refused(lambda w, k, v: None, max_seq=65)  # caches sized for 64 positions
+
+
+def _static_refused(mutate):
+    from decode_megakernel_persistent_gb300 import synth
+    shape = synth.TINY
+    w, k, v = fake_model(shape, 16)
+    logits = FakeCuda(shape.vocab)
+    cfg = ll.make_config(shape, 16)
+    w, k, v, logits = mutate(w, k, v, logits)
+    with pytest.raises(ll.LLError) as e:
+        ll.check_static_args(cfg, w, k, v, logits)
+    assert e.value.code == ll.LL_ERR_ARG
+    return str(e.value)
+
+
+def test_static_step_args_refuse_misfits():
+    # a short per-layer list would make the C side read past its host array
+    assert "one tensor per layer" in _static_refused(lambda w, k, v, lg: (dict(w, wg=w["wg"][:1]), k, v, lg))
+    # an undersized logits buffer or cache would take out-of-bounds device writes
+    assert "logits" in _static_refused(lambda w, k, v, lg: (w, k, v, FakeCuda(4095)))
+    assert "k_cache" in _static_refused(lambda w, k, v, lg: (w, FakeCuda(k.numel() - 1, torch.bfloat16), v, lg))
+    assert "v_cache" in _static_refused(lambda w, k, v, lg: (w, k, FakeCuda(v.numel(), torch.float16), lg))
+    assert "wq[1]" in _static_refused(
+        lambda w, k, v, lg: (dict(w, wq=[w["wq"][0], FakeCuda(10, torch.bfloat16)]), k, v, lg))
+    assert "cuda:1" in _static_refused(lambda w, k, v, lg: (w, k, v, FakeCuda(4096, device="cuda:1")))

@@ -6,6 +6,8 @@ call's greedy output, at the next position).
 Collected last on purpose (file name): it must pass alone in a fresh process and
 after every other test, when the library and its module are long loaded.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -83,9 +85,20 @@ def test_static_step_rejects_oversized_scratch_and_bad_args():
     k, v = synth.make_kv(shape, 16, 0, seed=2, device="cuda")
     big = ll.make_config(shape, 16)
     big.vocab = ll.LL_STATIC_SCRATCH_BYTES // 4 + 1  # logits alone overflow the array
+    # the binding refuses weights that do not fit the configuration ...
     with pytest.raises(ll.LLError) as e:
         ll.ll_decode_step_static(big, w, k, v, 1, 0, None)
-    assert e.value.code == ll.LL_ERR_SHAPE and "LL_STATIC_SCRATCH_BYTES" in str(e.value)
+    assert e.value.code == ll.LL_ERR_ARG
+    # ... and the library itself refuses the scratch it cannot hold, before any
+    # launch (the raw C call, past the binding's checks)
+    ws, keep = ll._weights_struct(w)
+    nxt = ctypes.c_int32(-1)
+    err = ctypes.create_string_buffer(256)
+    rc = ll.lib().ll_decode_step_static(ctypes.byref(big), ctypes.byref(ws), k.data_ptr(), v.data_ptr(), 1, 0, None,
+                                        ctypes.byref(nxt), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                        err, len(err))
+    del keep
+    assert rc == ll.LL_ERR_SHAPE and b"LL_STATIC_SCRATCH_BYTES" in err.value
     cfg = ll.make_config(shape, 16)
     with pytest.raises(ll.LLError) as e:
         ll.ll_decode_step_static(cfg, w, k, v, shape.vocab, 0, None)
