@@ -324,12 +324,13 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         delete h;
         return bad(rc, "cannot keep one megakernel block resident per SM");
     }
-    // Tensor-core pages for the widths that have them (tuning knob LL_MV_TC = 0
-    // keeps every matrix-vector product on the CUDA cores); without their tensor
-    // maps, the CUDA-core pages.
+    // Tensor-core pages for the widths that have them when LL_MV_TC = 1 (tuning
+    // knob; without their tensor maps, the CUDA-core pages). Off by default: at
+    // batch 1 the CUDA-core pages measured faster (1B, ctx 1024: 641 against
+    // 865-950 us per token).
     std::vector<ll::TensorMap> wmaps;
     {
-        bool want_tc = true;
+        bool want_tc = false;
         if (const char *e = std::getenv("LL_MV_TC")) want_tc = std::atoi(e) != 0;
         ll::MvShape th{}, tq{};
         const bool tc_h = want_tc && ll::mv_shape_tc(c.hidden, th), tc_q = want_tc && ll::mv_shape_tc(qd, tq);
