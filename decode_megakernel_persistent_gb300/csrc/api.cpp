@@ -33,7 +33,9 @@ struct ll_handle {
     Instr *d_instrs = nullptr;
     int max_instr = 0;
     uint32_t epoch = 0;
-    int32_t *pinned = nullptr;  // [0] next token, [1] status
+    int nb = 1;                 // sequences decoded together (batched handles)
+    bool batch_api = false;     // made by ll_init_batch: only ll_decode_steps_batch steps it
+    int32_t *pinned = nullptr;  // [0, nb) next tokens, [nb] status
     uint8_t *tagged = nullptr;  // the megakernel's tagged activation words (cleared on reset)
     size_t tagged_bytes = 0;
     std::string err;
@@ -109,7 +111,8 @@ bool encode_kv_maps(const ll_config &c, uint16_t *k_cache, uint16_t *v_cache, ll
 // matrices whose width has no tensor-core geometry stay zero. False if the
 // driver has no encoder or refuses a map.
 bool encode_weight_maps(const ll_config &c, const std::vector<ll::LayerW> &layers, const uint16_t *lm_head,
-                        const ll::MvShape &mh, const ll::MvShape &mq, std::vector<ll::TensorMap> &out) {
+                        const ll::MvShape &mh, const ll::MvShape &mq, const ll::MvShape &mi,
+                        std::vector<ll::TensorMap> &out) {
     using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -122,12 +125,13 @@ bool encode_weight_maps(const ll_config &c, const std::vector<ll::LayerW> &layer
     }
     const auto encode = reinterpret_cast<EncodeTiled>(fn);
     out.assign(size_t(c.n_layers + 1) * ll::TC_MATS_PER_LAYER * ll::TC_ROWS, ll::TensorMap{});
-    auto one = [&](const uint16_t *w, int64_t rows, int K, int l, int m) -> bool {
+    // boxes of one column chunk (kc columns) of nr rows
+    auto one = [&](const uint16_t *w, int64_t rows, int K, int kc, int l, int m) -> bool {
         const cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(K / 64)};
         const cuuint64_t strides[2] = {cuuint64_t(K) * 2, 128};  // bytes: next row, next 64-column block
         const cuuint32_t estr[3] = {1, 1, 1};
         for (int nr = 1; nr <= ll::TC_ROWS; nr++) {
-            const cuuint32_t box[3] = {64, cuuint32_t(nr), cuuint32_t(K / 64)};
+            const cuuint32_t box[3] = {64, cuuint32_t(nr), cuuint32_t(kc / 64)};
             CUtensorMap map;
             if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(w), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -140,23 +144,31 @@ bool encode_weight_maps(const ll_config &c, const std::vector<ll::LayerW> &layer
     const int H = c.hidden, qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
     for (int l = 0; l < c.n_layers; l++) {
         const ll::LayerW &L = layers[l];
-        if (mh.tc && !(one(L.wq, qd, H, l, 0) && one(L.wk, kd, H, l, 1) && one(L.wv, kd, H, l, 2) &&
-                       one(L.wg, c.inter, H, l, 4) && one(L.wu, c.inter, H, l, 5)))
+        if (mh.tc && !(one(L.wq, qd, H, mh.kc, l, 0) && one(L.wk, kd, H, mh.kc, l, 1) && one(L.wv, kd, H, mh.kc, l, 2) &&
+                       one(L.wg, c.inter, H, mh.kc, l, 4) && one(L.wu, c.inter, H, mh.kc, l, 5)))
             return false;
-        if (mq.tc && !one(L.wo, H, qd, l, 3)) return false;
+        if (mq.tc && !one(L.wo, H, qd, mq.kc, l, 3)) return false;
+        if (mi.tc && !one(L.wd, H, c.inter, mi.kc, l, 6)) return false;
     }
-    if (mh.tc && !one(lm_head, c.vocab, H, c.n_layers, 0)) return false;
+    if (mh.tc && !one(lm_head, c.vocab, H, mh.kc, c.n_layers, 0)) return false;
     return true;
 }
 
-int attn_splits(const ll_config &c, int nsm) { return ll::attn_splits(c.max_seq, c.n_kv_heads, nsm); }
+int attn_splits(const ll_config &c, int nsm, int nb = 1) { return ll::attn_splits(c.max_seq, c.n_kv_heads, nsm, nb); }
 
-void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::vector<Instr>> &lists) {
+void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::vector<Instr>> &lists, int nb = 1,
+                     int lm_rows = 1 << 30) {
     ll::build_schedule(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim, c.inter,
-                       c.vocab, c.n_kv_heads, nsm, splits, lists);
+                       c.vocab, c.n_kv_heads, nsm, splits, lists, nb, lm_rows);
 }
 
-void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists); }
+// The tensor-core kernel holds at most BACC_FLOATS (row, sequence) results per
+// instruction, so it takes an SM's vocabulary rows in pieces of this many rows.
+int lm_rows_of(const ll_handle *h) {
+    return h->kp.mv_h.tc ? std::max(ll::TC_ROWS, ll::BACC_FLOATS / h->nb / ll::TC_ROWS * ll::TC_ROWS) : (1 << 30);
+}
+
+void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists, h->nb, lm_rows_of(h)); }
 
 // Clear counters, tagged activation words and the status word after a failed
 // step so the next starts clean (the step count restarts, so no stale tag may
@@ -172,8 +184,17 @@ int reset_device_state(ll_handle *h) {
     return LL_OK;
 }
 
+// One launch of n_steps steps. pos_b: each sequence's first position (batched
+// handles), else pos for the one sequence.
 int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, float *logits,
-            int32_t *next_token_dev, int32_t n_steps = 1, int32_t *tokens_dev = nullptr) {
+            int32_t *next_token_dev, int32_t n_steps = 1, int32_t *tokens_dev = nullptr,
+            const int32_t *pos_b = nullptr) {
+    if (!pos_b && h->batch_api) return fail(h, LL_ERR_ARG, "a batched handle steps through ll_decode_steps_batch");
+    for (int b = 0; pos_b && b < h->nb; b++)
+        if (pos_b[b] < 0 || n_steps < 1 || int64_t(pos_b[b]) + n_steps > h->cfg.max_seq)
+            return fail(h, LL_ERR_ARG, "sequence " + std::to_string(b) + ": steps " + std::to_string(pos_b[b]) + ".." +
+                                           std::to_string(int64_t(pos_b[b]) + n_steps - 1) + " outside [0, max_seq)");
+    if (pos_b) pos = pos_b[0];
     if (pos < 0 || pos >= h->cfg.max_seq)
         return fail(h, LL_ERR_ARG, "pos " + std::to_string(pos) + " outside [0, max_seq)");
     if (n_steps < 1 || int64_t(pos) + n_steps > h->cfg.max_seq)
@@ -188,6 +209,7 @@ int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, 
     p.next_token_dev = next_token_dev;
     p.n_steps = n_steps;
     p.tokens_dev = tokens_dev;
+    for (int b = 0; b < h->nb; b++) p.pos_b[b] = pos_b ? pos_b[b] : pos;
     p.epoch = h->epoch + 1;
     h->epoch += static_cast<uint32_t>(n_steps);
     int rc;
@@ -219,7 +241,7 @@ int enqueue(ll_handle *h, int32_t token, const int32_t *token_dev, int32_t pos, 
 
 const char *status_text(int s) {
     switch (s) {
-        case LL_ERR_ARG: return "token out of range";
+        case LL_ERR_ARG: return "a token out of range";
         case LL_ERR_DEP_TIMEOUT: return "a device-side wait ran past its time limit";
         case LL_ERR_NUMERIC: return "the logits held no orderable value (all NaN): no greedy token";
         default: return "device error";
@@ -229,20 +251,20 @@ const char *status_text(int s) {
 }  // namespace
 
 namespace ll {
-int attn_splits(int max_seq, int n_kv_heads, int nsm) {
+int attn_splits(int max_seq, int n_kv_heads, int nsm, int nb) {
     int per = ATTN_SPLIT_POS;
     if (const char *e = std::getenv("LL_ATTN_SPLIT_POS")) per = std::max(1, std::atoi(e));
     const int want = (max_seq + per - 1) / per;
-    return std::max(1, std::min(want, nsm / n_kv_heads));
+    return std::max(1, std::min(want, nsm / (n_kv_heads * nb)));
 }
 }  // namespace ll
 
-extern "C" {
+namespace {
 
-const char *ll_init_error(void) { return g_init_error.c_str(); }
-
-int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16_t *v_cache, void *stream,
-            ll_handle **out) {
+// ll_init (nb = 1, one cache pair) and ll_init_batch (nb sequences, batch_api):
+// one handle, one library allocation, the schedule for nb sequences.
+int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_caches, uint16_t *const *v_caches,
+                int nb, bool batch_api, void *stream, ll_handle **out) {
     g_init_error.clear();
     auto bad = [&](int code, const std::string &msg) {
         g_init_error = msg;
@@ -277,7 +299,13 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         !ll::mv_shape(c.inter, mi, lane_floats))
         return bad(LL_ERR_SHAPE, "hidden, n_q_heads*head_dim and inter must be multiples of 256, at most 16384");
     // ---- pointer checks
-    if (!aligned16(k_cache) || !aligned16(v_cache)) return bad(LL_ERR_ARG, "KV caches must be 16-byte aligned");
+    if (nb < 1 || nb > ll::MAX_B || (nb & (nb - 1)) != 0)
+        return bad(LL_ERR_ARG, "the batch must be 1, 2, 4 or 8 sequences");
+    if (!k_caches || !v_caches) return bad(LL_ERR_ARG, "KV cache arrays are NULL");
+    for (int b = 0; b < nb; b++)
+        if (!aligned16(k_caches[b]) || !aligned16(v_caches[b])) return bad(LL_ERR_ARG, "KV caches must be 16-byte aligned");
+    uint16_t *const k_cache = k_caches[0], *const v_cache = v_caches[0];
+    if (batch_api && c.backend != LL_BACKEND_MEGAKERNEL) return bad(LL_ERR_ARG, "batched decode runs on the megakernel backend");
     if (!aligned16(w->embed) || !aligned16(w->final_norm)) return bad(LL_ERR_ARG, "embed/final_norm not 16-byte aligned");
     if (!c.tied && !aligned16(w->lm_head)) return bad(LL_ERR_ARG, "lm_head not 16-byte aligned");
     const uint16_t *const *lp[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->wg, w->wu, w->wd};
@@ -306,42 +334,57 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     h->device = dev;
     h->nsm = prop.multiProcessorCount;
     h->stream = static_cast<cudaStream_t>(stream);
-    h->splits = attn_splits(c, h->nsm);
+    h->nb = nb;
+    h->batch_api = batch_api;
+    h->splits = attn_splits(c, h->nsm, nb);
     h->smem_bytes = ll::megakernel_smem_bytes();
     h->host_layers = layers;
     const int qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
-    {
-        auto per_sm = [&](int64_t rows) { return (rows + h->nsm - 1) / h->nsm; };
-        const int64_t qkv_rows = int64_t(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-        if (per_sm(qkv_rows) > ll::ACC_FLOATS || 2 * per_sm(c.inter) > ll::ACC_FLOATS ||
-            per_sm(c.hidden) > ll::XOWN_MAX || per_sm(c.vocab) > ll::ACC_FLOATS) {
-            delete h;
-            return bad(LL_ERR_SHAPE, "a projection has more rows per SM than the kernel holds");
-        }
+    auto per_sm = [&](int64_t rows) { return (rows + h->nsm - 1) / h->nsm; };
+    const int64_t qkv_rows = int64_t(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    if (per_sm(qkv_rows) > ll::ACC_FLOATS || 2 * per_sm(c.inter) > ll::ACC_FLOATS ||
+        per_sm(c.hidden) > ll::XOWN_MAX || per_sm(c.vocab) > ll::ACC_FLOATS) {
+        delete h;
+        return bad(LL_ERR_SHAPE, "a projection has more rows per SM than the kernel holds");
     }
     int rc = ll::megakernel_prepare(h->smem_bytes);
     if (rc != LL_OK) {
         delete h;
         return bad(rc, "cannot keep one megakernel block resident per SM");
     }
-    // Tensor-core pages for the widths that have them when LL_MV_TC = 1 (tuning
-    // knob; without their tensor maps, the CUDA-core pages). Off by default: at
-    // batch 1 the CUDA-core pages measured faster (1B, ctx 1024: 641 against
-    // 865-950 us per token).
+    // The tensor-core kernel (tensor-core pages for every width) for batched
+    // handles, and for single-sequence handles when LL_MV_TC = 1 (tuning knob; at
+    // batch 1 the CUDA-core pages measured faster, 1B at ctx 1024: 641 against
+    // 865-950 us per token). It needs every width a multiple of 1024 and the
+    // weight tensor maps; a single-sequence handle without them keeps the
+    // CUDA-core kernel.
     std::vector<ll::TensorMap> wmaps;
     {
-        bool want_tc = false;
-        if (const char *e = std::getenv("LL_MV_TC")) want_tc = std::atoi(e) != 0;
-        ll::MvShape th{}, tq{};
-        const bool tc_h = want_tc && ll::mv_shape_tc(c.hidden, th), tc_q = want_tc && ll::mv_shape_tc(qd, tq);
-        ll::MvShape nh = tc_h ? th : mh, nq = tc_q ? tq : mq;
-        if ((tc_h || tc_q) && encode_weight_maps(c, layers, c.tied ? w->embed : w->lm_head, nh, nq, wmaps)) {
-            mh = nh;
-            mq = nq;
+        bool want_tc = batch_api;
+        if (const char *e = std::getenv("LL_MV_TC")) want_tc = want_tc || std::atoi(e) != 0;
+        ll::MvShape th{}, tq{}, ti{};
+        const bool tc_all = ll::mv_shape_tc(c.hidden, th) && ll::mv_shape_tc(qd, tq) && ll::mv_shape_tc(c.inter, ti) &&
+                            c.backend == LL_BACKEND_MEGAKERNEL;
+        const bool fits = per_sm(qkv_rows) * nb <= ll::BACC_FLOATS && 2 * per_sm(c.inter) * nb <= ll::BACC_FLOATS &&
+                          per_sm(c.hidden) * nb <= ll::BACC_FLOATS;
+        if (want_tc && tc_all && fits && encode_weight_maps(c, layers, c.tied ? w->embed : w->lm_head, th, tq, ti, wmaps)) {
+            mh = th;
+            mq = tq;
+            mi = ti;
         } else {
             wmaps.clear();
+            if (batch_api) {
+                delete h;
+                return bad(LL_ERR_SHAPE, tc_all && fits ? "weight tensor maps could not be encoded"
+                                                       : "batched decode needs hidden, n_q_heads*head_dim and inter "
+                                                         "multiples of 1024 and rows per SM x batch within the "
+                                                         "kernel's accumulator");
+            }
         }
     }
+    h->kp.mv_h = mh;
+    h->kp.mv_q = mq;
+    h->kp.mv_i = mi;
     build_lists(h);
     for (auto &l : h->lists) h->max_instr = std::max<int>(h->max_instr, static_cast<int>(l.size()));
     std::vector<ll::PDesc> pdesc;
@@ -368,6 +411,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     uint64_t *t_qkv = nullptr, *t_part = nullptr, *t_o = nullptr, *t_xmid = nullptr, *t_act = nullptr,
              *t_xout = nullptr, *t_token = nullptr;
     const size_t part_floats = size_t(c.n_q_heads) * h->splits * (c.head_dim + 4);
+    const size_t B = size_t(nb);
     Piece pieces[] = {
         {reinterpret_cast<void **>(&d_instrs), size_t(h->nsm) * h->max_instr * sizeof(Instr)},
         {reinterpret_cast<void **>(&d_n_instr), size_t(h->nsm) * sizeof(int32_t)},
@@ -385,19 +429,19 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         {reinterpret_cast<void **>(&gate), size_t(c.inter) * 4},
         {reinterpret_cast<void **>(&up), size_t(c.inter) * 4},
         {reinterpret_cast<void **>(&logits), size_t(c.vocab) * 4},
-        {reinterpret_cast<void **>(&keys), size_t(h->nsm) * 8},
+        {reinterpret_cast<void **>(&keys), size_t(h->nsm) * 8 * B},
         {reinterpret_cast<void **>(&ctr), nctr * 4},
-        // the next token and the status word side by side: one 8-byte copy reads both
-        {reinterpret_cast<void **>(&tok), 8},
+        // the next tokens and the status word side by side: one copy reads them all
+        {reinterpret_cast<void **>(&tok), (B + 1) * 4},
         {reinterpret_cast<void **>(&dbg), 64},
         // the megakernel's tagged activations (one contiguous run, cleared together)
-        {reinterpret_cast<void **>(&t_qkv), size_t(qd + 2 * kd) * 8},
-        {reinterpret_cast<void **>(&t_part), part_floats * 8},
-        {reinterpret_cast<void **>(&t_o), size_t(qd) * 8},
-        {reinterpret_cast<void **>(&t_xmid), size_t(c.hidden) * 8},
-        {reinterpret_cast<void **>(&t_act), size_t(c.inter) * 8},
-        {reinterpret_cast<void **>(&t_xout), size_t(c.hidden) * 8},
-        {reinterpret_cast<void **>(&t_token), 8},
+        {reinterpret_cast<void **>(&t_qkv), size_t(qd + 2 * kd) * 8 * B},
+        {reinterpret_cast<void **>(&t_part), part_floats * 8 * B},
+        {reinterpret_cast<void **>(&t_o), size_t(qd) * 8 * B},
+        {reinterpret_cast<void **>(&t_xmid), size_t(c.hidden) * 8 * B},
+        {reinterpret_cast<void **>(&t_act), size_t(c.inter) * 8 * B},
+        {reinterpret_cast<void **>(&t_xout), size_t(c.hidden) * 8 * B},
+        {reinterpret_cast<void **>(&t_token), 8 * B},
     };
     size_t total = 0;
     for (auto &pc : pieces) total += round_up(pc.bytes, 256);
@@ -412,7 +456,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         *pc.dst = h->dmem + off;
         off += round_up(pc.bytes, 256);
     }
-    if (cudaMallocHost(&h->pinned, 2 * sizeof(int32_t)) != cudaSuccess) {
+    if (cudaMallocHost(&h->pinned, (B + 1) * sizeof(int32_t)) != cudaSuccess) {
         cudaFree(h->dmem);
         delete h;
         return bad(LL_ERR_OOM, "pinned host buffer allocation failed");
@@ -465,6 +509,7 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
         const int pp = ll::PAGE_BYTES / (4 * c.head_dim);
         p.attn_flash = (per_split + pp - 1) / pp >= 4 ? 1 : 0;
         if (const char *e = std::getenv("LL_ATTN_FLASH")) p.attn_flash = std::atoi(e) ? 1 : 0;
+        if (nb > 1) p.attn_flash = 0;  // the per-warp variant serves one sequence
         // its KV pages come through TMA tensor maps; without them, the block variant
         if (!encode_kv_maps(c, k_cache, v_cache, p.kv_maps)) p.attn_flash = 0;
     }
@@ -472,6 +517,12 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.mv_q = mq;
     p.mv_i = mi;
     p.wmaps = wmaps.empty() ? nullptr : d_wmaps;
+    p.nb = nb;
+    for (int b = 0; b < ll::MAX_B; b++) {
+        p.kc_b[b] = b < nb ? k_caches[b] : nullptr;
+        p.vc_b[b] = b < nb ? v_caches[b] : nullptr;
+        p.pos_b[b] = 0;
+    }
     p.t_qkv = t_qkv;
     p.t_part = t_part;
     p.t_o = t_o;
@@ -480,11 +531,11 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     p.t_xout = t_xout;
     h->tagged = reinterpret_cast<uint8_t *>(t_qkv);
     p.t_token = t_token;
-    h->tagged_bytes = static_cast<size_t>(reinterpret_cast<uint8_t *>(t_token) + round_up(8, 256) -
+    h->tagged_bytes = static_cast<size_t>(reinterpret_cast<uint8_t *>(t_token) + round_up(8 * B, 256) -
                                           reinterpret_cast<uint8_t *>(t_qkv));
     p.lm_keys = keys;
     p.ctr = ctr;
-    status = tok + 1;
+    status = tok + nb;
     p.status = status;
     p.token_out = tok;
 #ifdef LL_DEBUG_CHECKS
@@ -526,8 +577,8 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
               cudaMemcpy(d_pdesc_off, pdesc_off.data(), pdesc_off.size() * sizeof(int32_t), cudaMemcpyHostToDevice) ==
                   cudaSuccess &&
               cudaMemcpy(d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaMemset(ctr, 0, nctr * 4) == cudaSuccess && cudaMemset(status, 0, 4) == cudaSuccess &&
-              cudaMemset(tok, 0, 4) == cudaSuccess && cudaMemset(dbg, 0, 64) == cudaSuccess &&
+              cudaMemset(ctr, 0, nctr * 4) == cudaSuccess && cudaMemset(tok, 0, (B + 1) * 4) == cudaSuccess &&
+              cudaMemset(dbg, 0, 64) == cudaSuccess &&
               cudaMemset(h->tagged, 0, h->tagged_bytes) == cudaSuccess;
     if (!ok || upload_schedule(h) != LL_OK) {
         ll_free(h);
@@ -535,6 +586,22 @@ int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16
     }
     *out = h;
     return LL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ll_init_error(void) { return g_init_error.c_str(); }
+
+int ll_init(const ll_config *cfg, const ll_weights *w, uint16_t *k_cache, uint16_t *v_cache, void *stream,
+            ll_handle **out) {
+    return init_handle(cfg, w, &k_cache, &v_cache, 1, false, stream, out);
+}
+
+int ll_init_batch(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_caches, uint16_t *const *v_caches,
+                  int32_t n_seq, void *stream, ll_handle **out) {
+    return init_handle(cfg, w, k_caches, v_caches, n_seq, true, stream, out);
 }
 
 #ifdef LL_DEBUG_CHECKS
@@ -575,6 +642,14 @@ int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t
     return enqueue(h, 0, token_dev, pos, logits_dev, nullptr, n_steps, tokens_dev);
 }
 
+int ll_decode_steps_batch(ll_handle *h, const int32_t *tokens_in_dev, const int32_t *pos_host, int32_t n_steps,
+                          float *logits_dev, int32_t *tokens_dev) {
+    if (!h) return LL_ERR_ARG;
+    if (!h->batch_api) return fail(h, LL_ERR_ARG, "not a batched handle (ll_init_batch makes one)");
+    if (!tokens_in_dev || !pos_host || !tokens_dev) return fail(h, LL_ERR_ARG, "tokens_in_dev, pos or tokens_dev is NULL");
+    return enqueue(h, 0, tokens_in_dev, 0, logits_dev, nullptr, n_steps, tokens_dev, pos_host);
+}
+
 int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,
                          int32_t *next_token_dev) {
     if (!h) return LL_ERR_ARG;
@@ -589,6 +664,7 @@ int ll_synchronize(ll_handle *h) {
         cudaError_t e = cudaGetLastError();
         return fail(h, LL_ERR_CUDA, std::string("synchronize failed: ") + cudaGetErrorString(e));
     }
+    report_debug(h);
     const int32_t st = h->pinned[1];
     if (st != 0) {
         reset_device_state(h);
@@ -634,6 +710,7 @@ int ll_query(const ll_handle *h, int what, int64_t *value) {
             break;
         case LL_Q_SMEM_BYTES: *value = h->smem_bytes; break;
         case LL_Q_MV_TC: *value = (h->kp.mv_h.tc ? 1 : 0) | (h->kp.mv_q.tc ? 2 : 0) | (h->kp.mv_i.tc ? 4 : 0); break;
+        case LL_Q_BATCH: *value = h->nb; break;
         case LL_Q_TRACE_BYTES:
             *value = (int64_t(h->nsm) * h->max_instr * ll::TRACE_WORDS + int64_t(h->nsm) * ll::PTRACE_PAGES * 3) *
                      int64_t(sizeof(uint64_t));

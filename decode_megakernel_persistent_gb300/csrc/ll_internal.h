@@ -30,6 +30,8 @@ constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden 
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
 constexpr int ATT_WARPS = 8;               // warps that split an attention page's P.V
 constexpr int TRACE_WORDS = 12;            // timestamps per traced instruction
+constexpr int MAX_B = 8;                   // sequences one batched handle decodes together
+constexpr int BACC_FLOATS = 1024;          // per-SM row results x sequences of a tensor-core instruction
 constexpr int PTRACE_PAGES = 4096;         // pages per SM the page trace keeps (a ring)
 
 // Instruction kinds, in the order they appear within a layer.
@@ -38,10 +40,12 @@ enum Op : uint8_t { OP_QKV = 0, OP_ATTN = 1, OP_OPROJ = 2, OP_GATEUP = 3, OP_DOW
 // One entry of an SM's instruction list. For matrix-vector instructions
 // [r0, r1) is the SM's row range (for QKV in the stacked [q; k; v] rows, for
 // gate/up in the intermediate rows of both matrices); for attention r0 is the KV
-// head and r1 the split index.
+// head and r1 the split index. sub: the sequence of an attention item (batched
+// handles); for the LM head, 1 on the SM's last LM-head instruction (batched
+// handles cut an SM's vocabulary rows into several).
 struct Instr {
     uint8_t op;
-    uint8_t pad;
+    uint8_t sub;
     uint16_t layer;
     int32_t r0, r1;
     int32_t wait_ctr;     // counter to wait on, -1 for none
@@ -58,14 +62,15 @@ struct Instr {
 // so ws * rg warps of the team are active and each lane keeps vpl 16-byte
 // vectors of the input in registers.
 //
-// tc = 1 selects the tensor-core page instead (mv_shape_tc): a page holds up to
-// TC_ROWS whole rows, loaded by TMA in the 128-byte swizzle, and all NCW warps
-// work on every page, each on its own K / NCW columns.
+// tc = 1 selects the tensor-core page instead (mv_shape_tc): the columns are cut
+// into nch chunks of kc; a page holds up to TC_ROWS rows of one chunk, loaded by
+// TMA in the 128-byte swizzle, and all NCW warps work on every page, each on its
+// own kc / NCW columns of the chunk.
 struct MvShape {
-    int32_t K, ws, vpl, rpp, rg, rw, teams, tc;
+    int32_t K, ws, vpl, rpp, rg, rw, teams, tc, kc, nch;
 };
 constexpr int TC_ROWS = 8;        // rows of a tensor-core page (the MMA's n)
-constexpr int TC_MATS_PER_LAYER = 6;  // wq, wk, wv, wo, wg, wu: the matrices whose pages may be tensor-core pages
+constexpr int TC_MATS_PER_LAYER = 7;  // wq, wk, wv, wo, wg, wu, wd: the matrices whose pages may be tensor-core pages
 
 // One entry of an SM's producer list, in consumption order: a weight page
 // (src, bytes), or an attention item whose K/V pages depend on pos and are
@@ -77,9 +82,11 @@ struct PDesc {
     uint16_t kind;   // PD_WEIGHTS or PD_ATTN
 };
 enum : uint16_t { PD_WEIGHTS = 0, PD_ATTN = 1, PD_TMA_W = 2 };
-// PD_TMA_W: a tensor-core weight page, src = (tensor map index << 32) | first row.
-// Map index of matrix m (0..5: wq, wk, wv, wo, wg, wu) of layer l, or of the LM
-// head (l = L, m = 0), for a page of nr rows (1..TC_ROWS): every box height has
+// PD_ATTN: src = (sequence << 48) | (layer << 32) | (KV head << 16) | split.
+// PD_TMA_W: a tensor-core weight page, src = (tensor map index << 40) |
+// (64-column block of its chunk << 32) | first row.
+// Map index of matrix m (0..6: wq, wk, wv, wo, wg, wu, wd) of layer l, or of the
+// LM head (l = L, m = 0), for a page of nr rows (1..TC_ROWS): every box height has
 // its own map, so that a page never loads rows of another SM's range.
 __host__ __device__ inline uint32_t wmap_index(int l, int m, int nr) {
     return (uint32_t(l) * TC_MATS_PER_LAYER + uint32_t(m)) * TC_ROWS + uint32_t(nr - 1);
@@ -135,6 +142,12 @@ struct KParams {
     int32_t attn_flash;       // kernel variant: per-warp softmax in attention (long items)
     MvShape mv_h, mv_q, mv_i; // input widths hidden, n_q*hd, inter
     const TensorMap *wmaps;   // weight tensor maps of tensor-core pages (wmap_index), global memory, or null
+    // Batched handles (the tensor-core kernel): nb sequences, each with its own KV
+    // cache and position; tagged activations, argmax keys, tokens and logits are
+    // laid out sequence after sequence. Single-sequence handles: nb = 1 and entry 0.
+    int32_t nb;
+    int32_t pos_b[MAX_B];     // each sequence's position in the launch's first step
+    uint16_t *kc_b[MAX_B], *vc_b[MAX_B];
     // Activations between instructions, as tagged words: (tag << 32) | fp32 bits,
     // stored and loaded as single 8-byte accesses. A reader takes a word only
     // when its tag is the one of the current step and layer (tag_of), so the
@@ -194,17 +207,20 @@ struct ChainBufs {
 // KV splits per KV head: about ATTN_SPLIT_POS cached positions each at the
 // longest context (tuning knob LL_ATTN_SPLIT_POS, read here), at most one
 // attention item per SM. Every entry point picks its splits with this.
-int attn_splits(int max_seq, int n_kv_heads, int nsm);
+int attn_splits(int max_seq, int n_kv_heads, int nsm, int nb = 1);
 int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
 
-// Host-side schedule construction (schedule.cpp).
+// Host-side schedule construction (schedule.cpp). nb sequences (attention items
+// per sequence); an SM's LM-head rows in instructions of at most lm_rows rows.
 void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm, int splits,
-                    std::vector<std::vector<Instr>> &lists);
+                    std::vector<std::vector<Instr>> &lists, int nb = 1, int lm_rows = 1 << 30);
 // lane_floats: the most input floats a lane may hold per team copy of the
 // input (16 or 32); more allows more teams (pages in progress at once).
 bool mv_shape(int K, MvShape &m, int lane_floats = 16);
-// The tensor-core geometry for width K, if the kernel has it (K a multiple of 512,
-// at most 2048): pages of TC_ROWS rows, every warp on K / NCW columns of each.
+// The tensor-core geometry for width K, if the kernel has it (K a multiple of
+// 1024, at most 16384): chunks of 2048 columns (1024 when 2048 does not divide K),
+// pages of TC_ROWS rows of one chunk, every warp on a whole number of 64-column
+// blocks of each.
 bool mv_shape_tc(int K, MvShape &m);
 void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector<LayerW> &layers,
                  const uint16_t *lm_head, int H, int qd, int kd, int I, const MvShape &mh, const MvShape &mq,

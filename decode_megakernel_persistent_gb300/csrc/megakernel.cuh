@@ -224,6 +224,12 @@ struct alignas(16) Smem {
     int32_t start_status;
     volatile int32_t flag;
     volatile int32_t abort;
+    // the tensor-core kernel (batched handles; one sequence is a batch of one)
+    float bacc[BACC_FLOATS];        // row results of the current instruction, [row][sequence]
+    float bxown[MAX_B][XOWN_MAX];   // each sequence's residual rows this SM owns
+    float nredb[NCW][MAX_B];        // per warp and sequence: sum of squares of the input
+    int32_t btoken[MAX_B];          // each sequence's input token of the current step
+    int32_t bpos[MAX_B];            // and its position
 };
 
 static_assert(offsetof(Smem, xin) % 16 == 0 && offsetof(Smem, pt) % 16 == 0, "alignment");
@@ -969,7 +975,10 @@ __device__ void attn_block(const KParams &p, Smem &s, const uint16_t *K, const u
 // and stores them, tagged, to t_o. The threads of one output split the S partials
 // between them (a running maximum each), then one thread combines theirs through
 // shared memory.
-__device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int hd, uint32_t tag, uint32_t wtag) {
+// (b: the sequence of a batched handle, whose partials and outputs lie b whole
+// buffers further on)
+__device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int hd, uint32_t tag, uint32_t wtag,
+                             int b = 0) {
     const int S = p.attn_splits, GH = G * hd, stride = hd + 4, tid = threadIdx.x;
     const int v0 = static_cast<int>(static_cast<long long>(c) * GH / S);
     const int nv = static_cast<int>(static_cast<long long>(c + 1) * GH / S) - v0;
@@ -979,7 +988,7 @@ __device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int
     float M = -INFINITY, L = 0.f, O = 0.f;
     if (j < T) {
         const int h = (v0 + v) / hd, d = (v0 + v) % hd;
-        const uint64_t *base = p.t_part + size_t(g * G + h) * S * stride;
+        const uint64_t *base = p.t_part + size_t(b) * p.nq * S * stride + size_t(g * G + h) * S * stride;
         for (int cb = j; cb < S; cb += 4 * T) {
             uint64_t w[12];  // per split: m, l, o[d]
             poll_words(p, s, w, tag, [&](uint64_t (&ww)[12]) {
@@ -1023,12 +1032,14 @@ __device__ bool merge_splits(const KParams &p, Smem &s, int g, int c, int G, int
             Ls = fmaf(s.xin[(jj * nv + tid) * 3 + 1], b, Ls);
             Os = fmaf(s.xin[(jj * nv + tid) * 3 + 2], b, Os);
         }
-        st_tag(p.t_o + size_t(g) * GH + v0 + tid, Os / Ls, wtag);
+        st_tag(p.t_o + size_t(b) * p.nq * hd + size_t(g) * GH + v0 + tid, Os / Ls, wtag);
     }
     return true;
 }
 
-template <int DL>
+// BATCH: the item belongs to sequence ins.sub of a batched handle (its q/k/v,
+// position, caches, partials and output); otherwise to the one sequence.
+template <int DL, bool BATCH = false>
 __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
     constexpr int hd = DL * 32, half = hd / 2;
@@ -1036,14 +1047,17 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     const int qd = p.nq * hd, kd = p.nkv * hd;
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
-    const float2 *cs = p.rope_cs + size_t(s.c_pos) * half;
+    const int b = BATCH ? int(ins.sub) : 0;
+    const int pos = BATCH ? s.bpos[b] : s.c_pos;
+    const float2 *cs = p.rope_cs + size_t(pos) * half;
+    const uint64_t *qkv_b = p.t_qkv + size_t(b) * (qd + 2 * kd);
     const uint32_t tag = tag_of(p, s, l);
     // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
     // 1/sqrt(hd); the owner also rotates the new key and takes the new value
     {
-        const uint64_t *qh = p.t_qkv + size_t(g * G) * hd;
-        const uint64_t *kh = p.t_qkv + qd + size_t(g) * hd;
-        const uint64_t *vh = p.t_qkv + qd + kd + size_t(g) * hd;
+        const uint64_t *qh = qkv_b + size_t(g * G) * hd;
+        const uint64_t *kh = qkv_b + qd + size_t(g) * hd;
+        const uint64_t *vh = qkv_b + qd + kd + size_t(g) * hd;
         const bool has_q = tid < G * hd, has_k = owner && tid < half, has_v = owner && tid < hd;
         const int h = tid / hd, d = tid % hd, i = d < half ? d : d - half;
         uint64_t w[5];
@@ -1075,16 +1089,17 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
     if (consumer_any(s.abort)) return false;
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
-        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + s.c_pos) * hd;
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + pos) * hd;
+        uint16_t *kc = BATCH ? p.kc_b[b] : p.k_cache, *vc = BATCH ? p.vc_b[b] : p.v_cache;
         if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
             for (int d = tid; d < hd; d += NCT) {
-                p.k_cache[at + d] = s.knew[d];
-                p.v_cache[at + d] = s.vnew[d];
+                kc[at + d] = s.knew[d];
+                vc[at + d] = s.vnew[d];
             }
     }
     float oacc = 0.f;
     int c0, c1;
-    attn_range(p, s.c_pos, c, c0, c1);
+    attn_range(p, pos, c, c0, c1);
     const int PP = attn_pp(p);
     for (int p0 = c0; p0 < c1; p0 += PP) {
         const int n = min(PP, c1 - p0);
@@ -1108,17 +1123,18 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
 
     // partials: part[(qhead * S + c) * (hd + 4) + {d, hd: m, hd+1: l}]
     const int stride = hd + 4;
+    uint64_t *part_b = p.t_part + size_t(b) * p.nq * S * stride;
     const uint32_t wtag = write_tag(p, s, ins);
     if (tid < G * hd) {
         const int h = tid / hd, d = tid % hd;
-        st_tag(p.t_part + (size_t(g * G + h) * S + c) * stride + d, oacc, wtag);
+        st_tag(part_b + (size_t(g * G + h) * S + c) * stride + d, oacc, wtag);
     }
     if (tid < G && LL_OK_IDX(17, (size_t(g * G + tid) * S + c) * stride + hd + 1, size_t(p.nq) * S * stride)) {
-        st_tag(p.t_part + (size_t(g * G + tid) * S + c) * stride + hd, s.m_run[tid], wtag);
-        st_tag(p.t_part + (size_t(g * G + tid) * S + c) * stride + hd + 1, s.l_run[tid], wtag);
+        st_tag(part_b + (size_t(g * G + tid) * S + c) * stride + hd, s.m_run[tid], wtag);
+        st_tag(part_b + (size_t(g * G + tid) * S + c) * stride + hd + 1, s.l_run[tid], wtag);
     }
     if (tid == 0) trace_put(p, ii, 2);
-    return merge_splits(p, s, g, c, G, hd, tag, wtag);
+    return merge_splits(p, s, g, c, G, hd, tag, wtag, b);
 }
 
 // D += A * B, m16n8k16, all four A registers: a0 = (row g, cols 2t, 2t + 1),
@@ -1438,32 +1454,277 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
 
 
 // ---------------------------------------------------------------------------------
-// Tensor-core matrix-vector instructions (widths K with mv.tc: a multiple of 512,
-// at most 2048). A page holds nr <= TC_ROWS whole rows, loaded by one TMA copy of
-// a 3-D view of the matrix (64 columns, rows, K / 64 column blocks) in the
-// 128-byte swizzle: column block o of row r is the 128-byte line o * nr + r of the
-// page, its 16-byte chunk c at chunk c ^ ((o * nr + r) % 8). So the eight rows an
+// The tensor-core kernel: matrix-vector instructions on tensor-core pages for nb
+// sequences at once (a batched handle; a single-sequence handle is a batch of
+// one). The columns of width K are cut into nch chunks of kc (2048, or 1024); a
+// page holds nr <= TC_ROWS rows of one chunk, loaded by one TMA copy of a 3-D
+// view of the matrix (64 columns, rows, K / 64 column blocks) in the 128-byte
+// swizzle: column block o of row r is the 128-byte line o * nr + r of the page,
+// its 16-byte chunk c at chunk c ^ ((o * nr + r) % 8). So the eight rows an
 // ldmatrix reads at one column block fall in eight different bank groups.
 //
-// The product is m16n8k16 with the input as the A operand and the page's rows as
-// B (n = 8 rows): A rows 0, 1, 2 hold three bf16 terms of the input, x = hi + mid
-// + lo to the 24 bits of an fp32 value (one term misses the logits' bar; with two,
-// bf16 roundings of the stored K/V flip measurably more often than with fp32
-// products), rows 3..15 zero; the three cost no more products than one. Warp w
-// takes columns [w K / NCW, (w + 1) K / NCW) of every page, KS k-steps of 16; the
-// NCW partial sums of each row meet in shared memory, and the last warp to finish
-// a page adds them up and releases it.
+// The product is m16n8k16 with the inputs as the A operand and the page's rows
+// as B (n = 8 rows). Each sequence's input enters as T bf16 terms, x = t0 + t1
+// (+ t2): T = 3 (to the 24 bits of an fp32 value) for up to 4 sequences, T = 2 (~16
+// bits) for 5..8; one term misses the logits' bar, and with two the bf16 roundings
+// of stored K/V flip measurably more often than with fp32 products. A row r of A
+// is (sequence, term): rows 0..7 hold the first 8 / T * T of them, rows 8..15 the
+// next. All NCW warps work on every page, warp w on its own KS / 4 64-column
+// blocks of the chunk, so a page costs the same products for one sequence or
+// eight. The RMSNorm gain multiplies the input before the split and the norm's
+// 1 / rms, one number per sequence, multiplies the sums after.
+//
+// A warp's partial sums of a page go into that page's own lines of the warp's
+// columns (read by no other warp, and done with once its products are issued):
+// shared memory has no room for NCW x 8 sequences x 8 rows per ring slot. The last
+// warp to finish the page adds the NCW partials into s.bacc and releases it.
 
-// The instruction's input as A fragments: lane (g, t) of warp w holds, for its
-// k-step j (columns k0 = 16 (w KS + j) ...), term g (0: hi, 1: mid, 2: lo; 0 for
-// g >= 3) at k0 + 2t, +1 (a0[j]) and k0 + 2t + 8, +9 (a2[j]). The input is staged in
-// s.xin (the previous instruction's tagged words, or the token's embedding row
-// for layer 0), RMS-normed for QKV, gate/up and the LM head.
+// The epilogue of a tensor-core instruction, once s.bacc holds every (row,
+// sequence) sum: per sequence b, q/k/v, the residual stream, silu(gate) * up, or
+// the logits and this thread's running argmax, stored as the instruction's
+// outputs; sums of a normed input are scaled by b's 1 / rms here. Thread tid
+// handles sequence tid % nb (nb divides NCT), so its best/best_idx belong to one
+// sequence.
+__device__ __forceinline__ void mv_store_b(const KParams &p, Smem &s, const Instr &ins, int ii, bool normed,
+                                           float &best, int &best_idx) {
+    const int tid = threadIdx.x, nb = p.nb;
+    const int nrows = ins.r1 - ins.r0, r0 = ins.r0;
+    const uint32_t wtag = write_tag(p, s, ins);
+    const int b = tid % nb;
+    float rn = 1.0f;
+    if (normed) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; w++) tot += s.nredb[w][b];
+        rn = 1.0f / sqrtf(tot / static_cast<float>(mv_of(p, ins.op).K) + p.eps);
+    }
+    const int qkvd = (p.nq + 2 * p.nkv) * p.hd;
+    for (int idx = tid; idx < nrows * nb; idx += NCT) {
+        const int t = idx / nb;  // idx % nb == b
+        const float y = s.bacc[idx] * rn;
+        switch (ins.op) {
+            case OP_QKV:
+                if (LL_OK_IDX(5, r0 + t, qkvd)) st_tag(p.t_qkv + size_t(b) * qkvd + r0 + t, y, wtag);
+                break;
+            case OP_OPROJ:
+            case OP_DOWN: {
+                const int row = r0 + t;
+                if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) break;
+                const float base = ins.op == OP_OPROJ && ins.layer == 0
+                                       ? bf16_to_f(p.embed[size_t(s.btoken[b]) * p.H + row])
+                                       : s.bxown[b][t];
+                const float v = base + y;
+                s.bxown[b][t] = v;
+                st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + size_t(b) * p.H + row, v, wtag);
+                break;
+            }
+            case OP_GATEUP: {
+                const float u = s.bacc[(nrows + t) * nb + b] * rn;
+                if (LL_OK_IDX(8, r0 + t, p.I)) st_tag(p.t_act + size_t(b) * p.I + r0 + t, y / (1.0f + expf(-y)) * u, wtag);
+                break;
+            }
+            default:  // OP_LMHEAD: rows ascend per thread
+                if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[size_t(b) * p.V + r0 + t] = y;
+                if (y > best) {
+                    best = y;
+                    best_idx = r0 + t;
+                }
+                break;
+        }
+    }
+    if (threadIdx.x == 0) trace_put(p, ii, 2);
+}
+
+// Greedy argmax of every sequence across the grid (batched handles): each SM
+// publishes its best key per sequence, the last SM to arrive reduces them and
+// writes the tokens. Thread tid's best is for sequence tid % nb.
+__device__ void lm_finish_b(const KParams &p, Smem &s, float best, int best_idx) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x, nb = p.nb;
+    unsigned long long key = best_idx >= 0 ? argmax_key(best, best_idx) : 0ull;
+    for (int o = 16; o >= nb; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, key, o);
+        key = w > key ? w : key;
+    }
+    unsigned long long *kr = reinterpret_cast<unsigned long long *>(s.xin);  // [NCW][MAX_B]
+    if (lane < nb) kr[warp * MAX_B + lane] = key;
+    consumer_sync();
+    if (tid < nb) {
+        unsigned long long k = 0;
+        for (int w = 0; w < NCW; w++) k = kr[w * MAX_B + tid] > k ? kr[w * MAX_B + tid] : k;
+        p.lm_keys[size_t(blockIdx.x) * nb + tid] = k;
+        __threadfence();
+    }
+    consumer_sync();
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(p.ctr + size_t(CtrLayout::lm_ticket(p.L)) * CTR_STRIDE, 1u);
+        s.flag = (old + 1u == s.c_epoch * static_cast<uint32_t>(p.nsm)) ? 1 : 0;
+        __threadfence();
+    }
+    consumer_sync();
+    if (!s.flag || warp >= nb) return;
+    // warp b reduces sequence b
+    const int b = warp;
+    unsigned long long k = 0;
+    for (int i = lane; i < p.nsm; i += 32) {
+        const unsigned long long v = __ldcg(p.lm_keys + size_t(i) * nb + b);
+        k = v > k ? v : k;
+    }
+    k = warp_max_u64(k);
+    if (lane == 0) {
+        if (k == 0) atomicCAS(p.status, 0, LL_ERR_NUMERIC);  // every logit NaN: no greedy token
+        const int32_t tok = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffu));
+        p.token_out[b] = tok;
+        if (p.tokens_dev) p.tokens_dev[size_t(s.c_epoch - p.epoch) * nb + b] = tok;
+        else if (p.next_token_dev) p.next_token_dev[b] = tok;
+        if (p.n_steps > 1) {
+            __threadfence();
+            const uint64_t w = (static_cast<uint64_t>(s.c_epoch) << 32) | static_cast<uint32_t>(tok);
+            asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p.t_token + b), "l"(w) : "memory");
+        }
+    }
+}
+
+// The step the consumers of the tensor-core kernel start: as consumer_step_begin,
+// for each of the nb sequences (its position, and after a launch's first step the
+// token the previous step chose for it).
+__device__ bool consumer_step_begin_b(const KParams &p, Smem &s, int st) {
+    if (threadIdx.x == 0) {
+        s.c_epoch = p.epoch + static_cast<uint32_t>(st);
+        s.c_pos = p.pos_b[0] + st;
+        s.c_logits = p.logits ? p.logits + size_t(st) * size_t(p.nb) * size_t(p.V) : nullptr;
+    }
+    if (threadIdx.x < p.nb) {
+        const int b = threadIdx.x;
+        s.bpos[b] = p.pos_b[b] + st;
+        if (st > 0) {
+            const uint32_t prev = p.epoch + static_cast<uint32_t>(st - 1);
+            uint64_t w = 0, t0 = 0;
+            for (uint32_t it = 0;; ++it) {
+                w = ld_tag(p.t_token + b);
+                if (tag_ok(w, prev) || poll_give_up(p, s, it, t0)) break;
+            }
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            s.btoken[b] = static_cast<int32_t>(static_cast<uint32_t>(w));
+        }
+    }
+    if (consumer_any(s.abort)) return false;
+    if (threadIdx.x == 0) {
+        s.token = s.btoken[0];
+        if (st > 0) {
+            // what the sequences' threads acquired, released to the producer's gate
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            s.tok_step = st;
+        }
+    }
+    return !consumer_any(s.abort);
+}
+
+// Sequence and term of A row r (0..15), or -1.
+__device__ __forceinline__ int tc_seq(int r, int nb, int T, int &term) {
+    const int half = r >> 3, rr = r & 7, spb = 8 / T;
+    term = rr % T;
+    if (rr >= spb * T) return -1;
+    const int b = half * spb + rr / T;
+    return b < nb ? b : -1;
+}
+
+// The next T bf16 terms of v: term k is the bf16 nearest to what terms 0..k-1
+// leave of v.
+__device__ __forceinline__ uint16_t bf16_term(float v, int term) {
+    uint16_t h = 0;
+    for (int k = 0; k <= term; k++) {
+        h = f_to_bf16(v);
+        v -= bf16_to_f(h);
+    }
+    return h;
+}
+
+// A fragments of column chunk c for this lane's two A rows (g and g + 8):
+// a[j] = {a0, a1, a2, a3} of k-step j of the warp (rows g / g + 8 at columns 2t,
+// 2t + 1 and 2t + 8, 2t + 9 of the k-step). The inputs are staged in s.xin as
+// fp32, XIN_FLOATS / kc sequences at a time, from the previous instruction's
+// tagged words (or the tokens' embedding rows for layer 0). With count_ss, this
+// lane adds the squares of the values of its term-0 rows to ssl[h].
 template <int KS>
-__device__ bool load_input_tc(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv, uint32_t (&a0)[KS],
-                              uint32_t (&a2)[KS]) {
+__device__ bool tc_fragments(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv, int c, const uint64_t *src,
+                             uint32_t tag, const uint16_t *gain, int b_lo, int t_lo, int b_hi, int t_hi, bool count_ss,
+                             float (&ssl)[2], uint32_t (&a)[KS][4]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x, t = lane & 3;
+    const int nb = p.nb, K = mv.K, Kc = mv.kc, NSR = XIN_FLOATS / Kc;
+#pragma unroll
+    for (int j = 0; j < KS; j++) a[j][0] = a[j][1] = a[j][2] = a[j][3] = 0u;
+    for (int b0 = 0; b0 < nb; b0 += NSR) {
+        const int nsr = min(NSR, nb - b0), total = nsr * Kc;
+        consumer_sync();  // s.xin is free
+        if (src) {
+            constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
+            uint64_t w[2 * PAIRS];
+            poll_words(p, s, w, tag, [&](uint64_t (&ww)[2 * PAIRS]) {
+#pragma unroll
+                for (int k = 0; k < PAIRS; k++) {
+                    const int i = (tid + k * NCT) * 2;
+                    if (i < total) {
+                        const int sq = b0 + i / Kc, kk = i % Kc;
+                        ld_tag2(src + size_t(sq) * K + size_t(c) * Kc + kk, ww[2 * k], ww[2 * k + 1]);
+                    } else {
+                        ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
+                    }
+                }
+            });
+#pragma unroll
+            for (int k = 0; k < PAIRS; k++) {
+                const int i = (tid + k * NCT) * 2;
+                if (i < total) {
+                    s.xin[i] = tag_val(w[2 * k]);
+                    s.xin[i + 1] = tag_val(w[2 * k + 1]);
+                }
+            }
+        } else {
+            for (int i = tid; i < total; i += NCT) {
+                const int sq = b0 + i / Kc, kk = i % Kc;
+                s.xin[i] = bf16_to_f(p.embed[size_t(s.btoken[sq]) * p.H + size_t(c) * Kc + kk]);
+            }
+        }
+        if (consumer_any(s.abort)) return false;  // also publishes s.xin
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int b = h ? b_hi : b_lo, term = h ? t_hi : t_lo;
+            if (b < b0 || b >= b0 + nsr) continue;
+            const float *xs = s.xin + (b - b0) * Kc;
+#pragma unroll
+            for (int j = 0; j < KS; j++) {
+                const int k = (warp * KS + j) * 16 + 2 * t;  // within the chunk
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const float2 x = *reinterpret_cast<const float2 *>(xs + k + 8 * q);
+                    float v0 = x.x, v1 = x.y;
+                    if (count_ss && term == 0) ssl[h] = fmaf(v0, v0, fmaf(v1, v1, ssl[h]));
+                    if (gain) {
+                        const uint32_t gw = __ldg(reinterpret_cast<const uint32_t *>(gain + size_t(c) * Kc + k + 8 * q));
+                        v0 *= bf_lo(gw);
+                        v1 *= bf_hi(gw);
+                    }
+                    a[j][h + 2 * q] = uint32_t(bf16_term(v0, term)) | (uint32_t(bf16_term(v1, term)) << 16);
+                }
+            }
+        }
+    }
+    return true;
+}
+
+template <int KS>
+__device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
+                            float &best, int &best_idx) {
+    static_assert(KS == 4 || KS == 8, "a warp works on whole 64-column blocks");
+    const MvShape &mv = mv_of(p, ins.op);
+    Seg seg[3];
+    const int nseg = mv_segments(p, s, ins, seg);
+    if (nseg == 0) return true;  // no rows here: nothing to read or wait for
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int K = mv.K;
+    const int g = lane >> 2, t = lane & 3, q = lane >> 3, rr = lane & 7;
+    const int nb = p.nb, T = nb <= 4 ? 3 : 2;
+    int t_lo, t_hi;
+    const int b_lo = tc_seq(g, nb, T, t_lo), b_hi = tc_seq(g + 8, nb, T, t_hi);
     const uint16_t *gain = norm_gain(p, s, ins);
     const uint64_t *src = nullptr;
     uint32_t tag = 0;
@@ -1476,179 +1737,135 @@ __device__ bool load_input_tc(const KParams &p, Smem &s, const Instr &ins, const
             break;
         case OP_GATEUP: src = p.t_xmid; tag = tag_of(p, s, ins.layer); break;
         case OP_LMHEAD: src = p.t_xout; tag = tag_of(p, s, p.L - 1); break;
-        case OP_OPROJ: src = p.t_o; tag = tag_of(p, s, ins.layer); break;
-        default: break;
+        case OP_DOWN: src = p.t_act; tag = tag_of(p, s, ins.layer); break;
+        default: src = p.t_o; tag = tag_of(p, s, ins.layer); break;  // OP_OPROJ
     }
-    // this lane's gains, fetched before the wait (weights)
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t gw[KS][2];
-#pragma unroll
-    for (int j = 0; j < KS; j++) {
-        const int k0 = 16 * (warp * KS + j) + 2 * t;
-        gw[j][0] = gain ? __ldg(reinterpret_cast<const uint32_t *>(gain + k0)) : 0x3f803f80u;
-        gw[j][1] = gain ? __ldg(reinterpret_cast<const uint32_t *>(gain + k0 + 8)) : 0x3f803f80u;
-    }
-    if (src) {
-        constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
-        uint64_t w[2 * PAIRS];
-        poll_words(p, s, w, tag, [&](uint64_t (&ww)[2 * PAIRS]) {
-#pragma unroll
-            for (int k = 0; k < PAIRS; k++) {
-                const int i = (tid + k * NCT) * 2;
-                if (i < K) ld_tag2(src + i, ww[2 * k], ww[2 * k + 1]);
-                else ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
-            }
-        });
-#pragma unroll
-        for (int k = 0; k < PAIRS; k++) {
-            const int i = (tid + k * NCT) * 2;
-            if (i < K) {
-                s.xin[i] = tag_val(w[2 * k]);
-                s.xin[i + 1] = tag_val(w[2 * k + 1]);
-            }
-        }
-    } else {
-        const uint16_t *e = p.embed + size_t(s.token) * p.H;
-        for (int i = tid; i < K; i += NCT) s.xin[i] = bf16_to_f(e[i]);
-    }
-    if (consumer_any(s.abort)) return false;  // also publishes s.xin
-    float r = 1.0f;
-    if (gain) {
-        float ss = 0.f;
-        for (int i = tid; i < K; i += NCT) ss = fmaf(s.xin[i], s.xin[i], ss);
-        ss = warp_sum(ss);
-        if (lane == 0) s.nred[warp] = ss;
-        consumer_sync();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; w++) tot += s.nred[w];
-        r = 1.0f / sqrtf(tot / static_cast<float>(K) + p.eps);
-    }
-#pragma unroll
-    for (int j = 0; j < KS; j++) {
-        const int k0 = 16 * (warp * KS + j) + 2 * t;
-        uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            const float2 x = *reinterpret_cast<const float2 *>(&s.xin[k0 + 8 * h]);
-            const float v0 = gain ? x.x * r * bf_lo(gw[j][h]) : x.x;
-            const float v1 = gain ? x.y * r * bf_hi(gw[j][h]) : x.y;
-            // term g of v0 and v1: the bf16 nearest to what the terms before it leave
-            float r0 = v0, r1 = v1;
-            uint16_t t0 = 0, t1 = 0;
-            for (int k = 0; k <= g && k < 3; k++) {
-                t0 = f_to_bf16(r0);
-                t1 = f_to_bf16(r1);
-                r0 -= bf16_to_f(t0);
-                r1 -= bf16_to_f(t1);
-            }
-            packed[h] = g < 3 ? (uint32_t(t0) | (uint32_t(t1) << 16)) : 0u;
-        }
-        a0[j] = packed[0];
-        a2[j] = packed[1];
-    }
-    // s.acc shares space with s.xin: every warp holds its fragments before any
-    // row result is written
-    consumer_sync();
-    return true;
-}
-
-template <int KS>
-__device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
-                            float &best, int &best_idx) {
-    static_assert(KS % 2 == 0, "an ldmatrix.x4 covers two k-steps");
-    const MvShape &mv = mv_of(p, ins.op);
-    Seg seg[3];
-    const int nseg = mv_segments(p, s, ins, seg);
-    if (nseg == 0) return true;  // no rows here: nothing to read or wait for
-    uint32_t a0[KS], a2[KS];
-    if (!load_input_tc<KS>(p, s, ins, mv, a0, a2)) return false;
-    if (threadIdx.x == 0) trace_put(p, ii, 1);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int nrows = ins.r1 - ins.r0;
-    const int q = lane >> 3, rr = lane & 7;  // the ldmatrix matrix and row this lane addresses
+    const int ntot = (ins.op == OP_GATEUP ? 2 : 1) * nrows;
+    for (int i = tid; i < ntot * nb; i += NCT)
+        if (LL_OK_IDX(30, i, BACC_FLOATS)) s.bacc[i] = 0.f;
     const uint32_t zrow = smem_addr(s.zrow);
+    float ssl[2] = {0.f, 0.f};
+    uint32_t a[KS][4];
+    int have = -1;  // the chunk whose fragments a[] holds
     bool bad = false;
     for (int si = 0; si < nseg; si++) {
         const Seg sg = seg[si];
         const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
-        for (int pr = 0; pr < sg.nrows; pr += TC_ROWS) {
-            const int nr = min(TC_ROWS, sg.nrows - pr);
-            const uint32_t slot = cpage % NPAGES;
-            const uint32_t this_page = cpage++;
-            if (bad || !wait_page(p, s, this_page)) {
-                bad = true;
-                continue;
+        for (int c = 0; c < mv.nch; c++) {
+            if (c != have) {
+                if (!tc_fragments<KS>(p, s, ins, mv, c, src, tag, gain, b_lo, t_lo, b_hi, t_hi, si == 0, ssl, a))
+                    return false;
+                if (tid == 0 && si == 0 && c == 0) trace_put(p, ii, 1);
+                have = c;
             }
-            if (warp == 0 && lane == 0) {
-                ptrace_put(p, this_page, 1);
-                if (si == 0 && pr == 0) trace_put(p, ii, 6);
-            }
-            const uint32_t base = smem_addr(pages) + slot * PAGE_BYTES;
-            float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < KS; j += 2) {
-                const int ks = warp * KS + j;  // k-steps ks, ks + 1: columns 16 ks .. 16 ks + 31
-                const int o = ks >> 2;         // their 64-column block
-                const int line = o * nr + rr;
-                const uint32_t chunk = uint32_t((ks & 3) * 2 + q);
-                const uint32_t at = rr < nr ? base + uint32_t(line) * 128u + ((chunk ^ uint32_t(line & 7)) << 4) : zrow;
-                uint32_t b[4] = {0u, 0u, 0u, 0u};
-                if (at == zrow || LL_OK_IDX(21, at + 16 - smem_addr(pages), NPAGES * PAGE_BYTES + 1)) ldsm_x4(at, b);
-                mma_16816(d, make_uint4(a0[j], 0u, a2[j], 0u), b[0], b[1]);
-                mma_16816(e, make_uint4(a0[j + 1], 0u, a2[j + 1], 0u), b[2], b[3]);
-            }
-            // D: lane (g, t) holds term g's sums for page rows 2t, 2t + 1; add the
-            // terms (lanes t, t + 4, t + 8; lanes t + 12 hold zeros)
-            float v0 = d[0] + e[0], v1 = d[1] + e[1];
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 4);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 4);
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 8);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 8);
-            if (lane < 4) {
-                s.part[slot][warp * TC_ROWS + 2 * lane] = v0;
-                s.part[slot][warp * TC_ROWS + 2 * lane + 1] = v1;
-            }
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(&s.pcnt[slot], 1) == NCW - 1;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {  // this warp finishes the page: the NCW partials of every row
-                __threadfence_block();
-                if (lane < nr) {
-                    float y = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NCW; w++) y += s.part[slot][w * TC_ROWS + lane];
-                    if (LL_OK_IDX(4, acc0 + pr + lane, ACC_FLOATS)) s.acc[acc0 + pr + lane] = y;
+            for (int pr = 0; pr < sg.nrows; pr += TC_ROWS) {
+                const int nr = min(TC_ROWS, sg.nrows - pr);
+                const uint32_t slot = cpage % NPAGES;
+                const uint32_t this_page = cpage++;
+                if (bad || !wait_page(p, s, this_page)) {
+                    bad = true;
+                    continue;
                 }
+                if (warp == 0 && lane == 0) {
+                    ptrace_put(p, this_page, 1);
+                    if (si == 0 && c == 0 && pr == 0) trace_put(p, ii, 6);
+                }
+                uint8_t *pg = pages + size_t(slot) * PAGE_BYTES;
+                const uint32_t base = smem_addr(pg);
+                float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < KS; j += 2) {
+                    const int ks = warp * KS + j;  // k-steps ks, ks + 1: columns 16 ks .. 16 ks + 31 of the chunk
+                    const int line = (ks >> 2) * nr + rr;
+                    const uint32_t chunk = uint32_t((ks & 3) * 2 + q);
+                    const uint32_t at =
+                        rr < nr ? base + uint32_t(line) * 128u + ((chunk ^ uint32_t(line & 7)) << 4) : zrow;
+                    uint32_t bm[4] = {0u, 0u, 0u, 0u};
+                    if (at == zrow || LL_OK_IDX(21, at + 16 - smem_addr(pages), NPAGES * PAGE_BYTES + 1)) ldsm_x4(at, bm);
+                    mma_16816(d, make_uint4(a[j][0], a[j][1], a[j][2], a[j][3]), bm[0], bm[1]);
+                    mma_16816(e, make_uint4(a[j + 1][0], a[j + 1][1], a[j + 1][2], a[j + 1][3]), bm[2], bm[3]);
+                }
+                // D: lane (g, t) holds A rows g (d0, d1) and g + 8 (d2, d3) at page rows
+                // 2t, 2t + 1; a sequence's terms are the rows below its term 0, 4 lanes apart
+                float v[4] = {d[0] + e[0], d[1] + e[1], d[2] + e[2], d[3] + e[3]};
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float u4 = __shfl_down_sync(0xffffffffu, v[i], 4);
+                    const float u8 = __shfl_down_sync(0xffffffffu, v[i], 8);
+                    v[i] += u4 + (T == 3 ? u8 : 0.f);
+                }
+                // partials [row][sequence] into the page lines of this warp's columns
+                float *own = reinterpret_cast<float *>(pg + size_t((warp * KS) >> 2) * nr * 128);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int b = h ? b_hi : b_lo, term = h ? t_hi : t_lo;
+                    if (b < 0 || term != 0) continue;
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; e2++) {
+                        const int r = 2 * t + e2;
+                        if (r < nr && LL_OK_IDX(31, r * nb + b, nr * 32)) own[r * nb + b] = v[2 * h + e2];
+                    }
+                }
+                // these generic writes precede the producer's next TMA write of the slot
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
+                int last = 0;
                 if (lane == 0) {
-                    s.pcnt[slot] = 0;
-                    ptrace_put(p, this_page, 2);
-                    mbar_arrive(&s.empty[slot]);
+                    __threadfence_block();
+                    last = atomicAdd(&s.pcnt[slot], 1) == NCW - 1;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {  // this warp finishes the page: the NCW partials of every (row, sequence)
+                    __threadfence_block();
+                    for (int idx = lane; idx < nr * nb; idx += 32) {
+                        float y = 0.f;
+#pragma unroll
+                        for (int w = 0; w < NCW; w++)
+                            y += reinterpret_cast<const float *>(pg + size_t((w * KS) >> 2) * nr * 128)[idx];
+                        const int r = idx / nb, b = idx % nb;
+                        if (LL_OK_IDX(4, (acc0 + pr + r) * nb + b, BACC_FLOATS)) s.bacc[(acc0 + pr + r) * nb + b] += y;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        s.pcnt[slot] = 0;
+                        ptrace_put(p, this_page, 2);
+                        mbar_arrive(&s.empty[slot]);
+                    }
                 }
             }
         }
     }
     if (tid == 0) trace_put(p, ii, 7);
-    if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
-    mv_store(p, s, ins, ii, best, best_idx);
+    if (consumer_any(bad)) return false;  // else every page is reduced into s.bacc
+    // each warp's share of every sequence's sum of squares (normed inputs)
+    if (gain) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float v2 = ssl[h];
+            v2 += __shfl_xor_sync(0xffffffffu, v2, 1);
+            v2 += __shfl_xor_sync(0xffffffffu, v2, 2);
+            const int b = h ? b_hi : b_lo, term = h ? t_hi : t_lo;
+            if (t == 0 && b >= 0 && term == 0) s.nredb[warp][b] = v2;
+        }
+        consumer_sync();
+    }
+    mv_store_b(p, s, ins, ii, gain != nullptr, best, best_idx);
     return true;
 }
-
 // FLASH: the kernel variant for long attention items (see attn_tiles); the other
 // variant keeps a block-wide softmax per page, cheaper when an item spans a page
 // or two. The host picks the variant by the longest item at max_seq.
-template <bool FLASH>
+// (TC: the tensor-core kernel, whose block-softmax items carry their sequence;
+// its per-warp variant serves single-sequence handles only)
+template <bool FLASH, bool TC = false>
 __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     if constexpr (FLASH)
         return p.hd == 64 ? attn_item_flash<2>(p, s, pages, ins, ii, cpage)
                           : attn_item_flash<4>(p, s, pages, ins, ii, cpage);
     else
-        return p.hd == 64 ? attn_item<2>(p, s, pages, ins, ii, cpage) : attn_item<4>(p, s, pages, ins, ii, cpage);
+        return p.hd == 64 ? attn_item<2, TC>(p, s, pages, ins, ii, cpage) : attn_item<4, TC>(p, s, pages, ins, ii, cpage);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1720,6 +1937,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
             const PDesc e = dl[di];
             int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
             size_t head_row = 0;
+            const uint16_t *a_kc = p.k_cache, *a_vc = p.v_cache;  // the item's sequence's caches
             if (e.kind == PD_ATTN && st > gate) {
                 const uint64_t t0 = gtimer();
                 for (uint32_t it = 1; s.tok_step < st; ++it) {
@@ -1740,8 +1958,15 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                 gate = st;
             }
             if (e.kind == PD_ATTN) {
-                const int layer = int(e.src >> 32), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
-                attn_range(p, pos, c, a_c0, a_c1);
+                const int layer = int((e.src >> 32) & 0xffffu), g = int((e.src >> 16) & 0xffffu), c = int(e.src & 0xffffu);
+                int a_pos = pos;
+                if (TC) {  // batched handles: the item's sequence
+                    const int b = int(e.src >> 48);
+                    a_pos = p.pos_b[b] + st;
+                    a_kc = p.kc_b[b];
+                    a_vc = p.vc_b[b];
+                }
+                attn_range(p, a_pos, c, a_c0, a_c1);
                 a_p0 = a_c0;
                 head_row = (size_t(layer) * p.nkv + g) * size_t(p.max_seq);
                 if (a_c0 >= a_c1) continue;  // empty split: no pages
@@ -1762,8 +1987,8 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                         src0 = src1 = nullptr;
                     } else {
                         b0 = b1 = uint32_t(a_n) * p.hd * 2;
-                        src0 = p.k_cache + (head_row + size_t(a_p0)) * p.hd;
-                        src1 = p.v_cache + (head_row + size_t(a_p0)) * p.hd;
+                        src0 = a_kc + (head_row + size_t(a_p0)) * p.hd;
+                        src1 = a_vc + (head_row + size_t(a_p0)) * p.hd;
                     }
                     a_p0 += a_n;
                 } else if (TC && e.kind == PD_TMA_W) {
@@ -1826,10 +2051,11 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                             }
                         }
                 } else if (TC && e.kind == PD_TMA_W) {
-                    // a tensor-core page: rows [row, row + nr) of a matrix, swizzled (see mv_instr_tc)
-                    const TensorMap *map = p.wmaps + (e.src >> 32);
-                    const int row = int(uint32_t(e.src & 0xffffffffu));
-                    tma_load_3d_hint(dst, map, 0, row, 0, &s.full[slot], evict_first);
+                    // a tensor-core page: rows [row, row + nr) of one column chunk of a
+                    // matrix, swizzled (see mv_instr_tc)
+                    const TensorMap *map = p.wmaps + (e.src >> 40);
+                    const int z = int((e.src >> 32) & 0xffu), row = int(uint32_t(e.src & 0xffffffffu));
+                    tma_load_3d_hint(dst, map, 0, row, z, &s.full[slot], evict_first);
                 } else {
                     if (e.kind == PD_WEIGHTS && p.evict_first) bulk_load_hint(dst, src0, b0, &s.full[slot], evict_first);
                     else bulk_load(dst, src0, b0, &s.full[slot]);
@@ -1897,15 +2123,16 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
         if (threadIdx.x == 0) trace_put(p, i, 0);
         bool ok;
         if (ins.op == OP_ATTN) {
-            ok = attn_instr<FLASH>(p, s, pages, ins, i, cpage);
-        } else if (TC && mv_of(p, ins.op).tc) {
-            switch (mv_of(p, ins.op).K) {
-                case 512: ok = mv_instr_tc<2>(p, s, pages, ins, i, cpage, best, best_idx); break;
+            ok = attn_instr<FLASH, TC>(p, s, pages, ins, i, cpage);
+        } else if constexpr (TC) {
+            // every width has tensor-core geometry here (the host launches this
+            // kernel only then)
+            switch (mv_of(p, ins.op).kc) {
                 case 1024: ok = mv_instr_tc<4>(p, s, pages, ins, i, cpage, best, best_idx); break;
                 case 2048: ok = mv_instr_tc<8>(p, s, pages, ins, i, cpage, best, best_idx); break;
                 default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
             }
-            if (ok && ins.op == OP_LMHEAD) lm_finish(p, s, best, best_idx);
+            if (ok && ins.op == OP_LMHEAD && ins.sub) lm_finish_b(p, s, best, best_idx);
         } else {
             const MvShape &mv = mv_of(p, ins.op);
             switch (mv.vpl * 16 + mv.rw) {
@@ -1932,7 +2159,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     const int n = p.n_instr[blockIdx.x];
     uint32_t cpage = 0;
     for (int st = 0; st < p.n_steps; st++) {
-        if (!consumer_step_begin(p, s, st)) return;
+        if (!(TC ? consumer_step_begin_b(p, s, st) : consumer_step_begin(p, s, st))) return;
         if (!consumer_step<FLASH, TC>(p, s, pages, list, n, cpage)) return;
     }
 }
@@ -1977,6 +2204,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
     }
     __syncthreads();
     if (s.start_status != 0) return;  // an earlier step failed: do nothing
+    if (TC) {  // every sequence's first token (a batch of one: the one token)
+        if (threadIdx.x < p.nb) {
+            const int t = p.token_dev ? p.token_dev[threadIdx.x] : p.token;
+            s.btoken[threadIdx.x] = t;
+            if (t < 0 || t >= p.V) s.flag = 1;
+        }
+        __syncthreads();
+        if (s.flag) {
+            if (threadIdx.x == 0) atomicCAS(p.status, 0, LL_ERR_ARG);
+            return;
+        }
+    }
     if (s.token < 0 || s.token >= p.V) {
         if (threadIdx.x == 0) atomicCAS(p.status, 0, LL_ERR_ARG);
         return;

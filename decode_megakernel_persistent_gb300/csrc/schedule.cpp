@@ -41,7 +41,7 @@ Instr make(Op op, int layer, int32_t r0, int32_t r1, int wait_ctr, uint32_t wait
 // by the order of the page's instruction list, so every wait refers to work that
 // some SM schedules earlier; with all blocks resident at once this cannot deadlock.
 void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm, int splits,
-                    std::vector<std::vector<Instr>> &lists) {
+                    std::vector<std::vector<Instr>> &lists, int nb, int lm_rows) {
     lists.assign(nsm, {});
     const uint32_t all = static_cast<uint32_t>(nsm);
     for (int l = 0; l < L; l++) {
@@ -50,12 +50,15 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
             split_rows(qd + 2 * kd, nsm, sm, r0, r1);
             lists[sm].push_back(make(OP_QKV, l, r0, r1, l ? CtrLayout::down(l - 1) : -1, l ? all : 0,
                                      CtrLayout::qkv(l)));
-            if (sm < nkv * splits)
-                lists[sm].push_back(make(OP_ATTN, l, sm / splits, sm % splits, CtrLayout::qkv(l), all,
-                                         CtrLayout::attn(l)));
+            if (sm < nb * nkv * splits) {
+                const int item = sm % (nkv * splits);
+                Instr a = make(OP_ATTN, l, item / splits, item % splits, CtrLayout::qkv(l), all, CtrLayout::attn(l));
+                a.sub = static_cast<uint8_t>(sm / (nkv * splits));
+                lists[sm].push_back(a);
+            }
             split_rows(H, nsm, sm, r0, r1);
-            lists[sm].push_back(make(OP_OPROJ, l, r0, r1, CtrLayout::attn(l), static_cast<uint32_t>(nkv * splits),
-                                     CtrLayout::oproj(l)));
+            lists[sm].push_back(make(OP_OPROJ, l, r0, r1, CtrLayout::attn(l),
+                                     static_cast<uint32_t>(nb * nkv * splits), CtrLayout::oproj(l)));
             split_rows(I, nsm, sm, r0, r1);
             lists[sm].push_back(make(OP_GATEUP, l, r0, r1, CtrLayout::oproj(l), all, CtrLayout::gateup(l)));
             split_rows(H, nsm, sm, r0, r1);
@@ -65,7 +68,15 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
     for (int sm = 0; sm < nsm; sm++) {
         int32_t r0, r1;
         split_rows(V, nsm, sm, r0, r1);
-        lists[sm].push_back(make(OP_LMHEAD, 0, r0, r1, CtrLayout::down(L - 1), all, -1));
+        // (an SM with no vocabulary rows still gets one, empty, instruction)
+        for (int32_t a = r0;;) {
+            const int32_t e = std::min<int64_t>(r1, int64_t(a) + lm_rows);
+            Instr in = make(OP_LMHEAD, 0, a, e, CtrLayout::down(L - 1), all, -1);
+            in.sub = e >= r1 ? 1 : 0;
+            lists[sm].push_back(in);
+            if (e >= r1) break;
+            a = e;
+        }
     }
 }
 
@@ -84,8 +95,9 @@ static bool mv_combo_ok(int vpl, int rw) {
 }
 
 bool mv_shape_tc(int K, MvShape &m) {
-    if (K <= 0 || K % (32 * NCW) != 0 || K > 2048) return false;
-    m = MvShape{K, NCW, 0, TC_ROWS, 1, TC_ROWS, 1, 1};
+    if (K <= 0 || K % 1024 != 0 || K > 16384) return false;
+    const int kc = K % 2048 == 0 ? 2048 : 1024;
+    m = MvShape{K, NCW, 0, TC_ROWS, 1, TC_ROWS, 1, 1, kc, K / kc};
     return true;
 }
 
@@ -111,7 +123,7 @@ bool mv_shape(int K, MvShape &m, int lane_floats) {
         if (active > best_active || (active == best_active && rpp > best_rpp)) {
             best_active = active;
             best_rpp = rpp;
-            m = MvShape{K, ws, vpl, rpp, rg, rw, teams, 0};
+            m = MvShape{K, ws, vpl, rpp, rg, rw, teams, 0, K, 1};
         }
     }
     return best_active > 0;
@@ -125,21 +137,27 @@ void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector
     out.clear();
     off.assign(lists.size() + 1, 0);
     // pages of a segment: rows [row0, row0 + nrows) of matrix w; tensor-core
-    // pages name the matrix's tensor map (layer l, matrix m) instead of an address
+    // pages name the matrix's tensor map (layer l, matrix m) and column chunk
+    // instead of an address, chunk after chunk (the consumers build the input's
+    // fragments once per chunk)
     auto pages = [&](const uint16_t *w, int row0, int nrows, const MvShape &mv, int instr, int l, int m) {
-        for (int pr = 0; pr < nrows; pr += mv.rpp) {
-            const int nr = std::min(mv.rpp, nrows - pr);
-            PDesc d{};
-            if (mv.tc) {
-                d.src = (static_cast<unsigned long long>(wmap_index(l, m, nr)) << 32) | uint32_t(row0 + pr);
-                d.kind = PD_TMA_W;
-            } else {
-                d.src = reinterpret_cast<unsigned long long>(w + size_t(row0 + pr) * mv.K);
-                d.kind = PD_WEIGHTS;
+        for (int c = 0; c < (mv.tc ? mv.nch : 1); c++) {
+            for (int pr = 0; pr < nrows; pr += mv.rpp) {
+                const int nr = std::min(mv.rpp, nrows - pr);
+                PDesc d{};
+                if (mv.tc) {
+                    d.src = (static_cast<unsigned long long>(wmap_index(l, m, nr)) << 40) |
+                            (static_cast<unsigned long long>(c * (mv.kc / 64)) << 32) | uint32_t(row0 + pr);
+                    d.kind = PD_TMA_W;
+                    d.bytes = uint32_t(nr) * uint32_t(mv.kc) * 2u;
+                } else {
+                    d.src = reinterpret_cast<unsigned long long>(w + size_t(row0 + pr) * mv.K);
+                    d.kind = PD_WEIGHTS;
+                    d.bytes = uint32_t(nr) * uint32_t(mv.K) * 2u;
+                }
+                d.instr = static_cast<uint16_t>(instr);
+                out.push_back(d);
             }
-            d.bytes = uint32_t(nr) * uint32_t(mv.K) * 2u;
-            d.instr = static_cast<uint16_t>(instr);
-            out.push_back(d);
         }
     };
     for (size_t sm = 0; sm < lists.size(); sm++) {
@@ -149,8 +167,8 @@ void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector
             const int r0 = in.r0, r1 = in.r1;
             if (in.op == OP_ATTN) {
                 PDesc d{};
-                d.src = (static_cast<unsigned long long>(in.layer) << 32) | (static_cast<unsigned long long>(r0) << 16) |
-                        static_cast<unsigned long long>(r1);
+                d.src = (static_cast<unsigned long long>(in.sub) << 48) | (static_cast<unsigned long long>(in.layer) << 32) |
+                        (static_cast<unsigned long long>(r0) << 16) | static_cast<unsigned long long>(r1);
                 d.instr = static_cast<uint16_t>(i);
                 d.kind = PD_ATTN;
                 out.push_back(d);
@@ -173,7 +191,7 @@ void build_pdesc(const std::vector<std::vector<Instr>> &lists, const std::vector
                     pages(lw->wg, r0, r1 - r0, mh, int(i), in.layer, 4);
                     pages(lw->wu, r0, r1 - r0, mh, int(i), in.layer, 5);
                     break;
-                case OP_DOWN: pages(lw->wd, r0, r1 - r0, mi, int(i), in.layer, 0); break;
+                case OP_DOWN: pages(lw->wd, r0, r1 - r0, mi, int(i), in.layer, 6); break;
                 default: pages(lm_head, r0, r1 - r0, mh, int(i), int(layers.size()), 0); break;
             }
         }

@@ -32,6 +32,8 @@ LL_Q_LAUNCHES_PER_STEP = 6
 LL_Q_SMEM_BYTES = 7
 LL_Q_TRACE_BYTES = 8
 LL_Q_MV_TC = 9
+LL_Q_BATCH = 10
+LL_MAX_BATCH = 8
 
 LL_STATIC_SCRATCH_BYTES = 4194304
 LL_STATIC_MAX_LAYERS = 256
@@ -45,7 +47,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
 EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_decode_steps", "ll_synchronize",
            "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
-           "ll_free", "ll_decode_step_static")
+           "ll_free", "ll_decode_step_static", "ll_init_batch", "ll_decode_steps_batch")
 
 
 class LLError(RuntimeError):
@@ -113,6 +115,11 @@ def lib() -> ctypes.CDLL:
     L.ll_decode_step_static.argtypes = [ctypes.POINTER(ll_config), ctypes.POINTER(ll_weights), vp, vp, i32, i32,
                                         vp, ctypes.POINTER(i32), vp, ctypes.c_char_p, ctypes.c_size_t]
     L.ll_decode_step_static.restype = ctypes.c_int
+    L.ll_init_batch.argtypes = [ctypes.POINTER(ll_config), ctypes.POINTER(ll_weights), ctypes.POINTER(vp),
+                                ctypes.POINTER(vp), i32, vp, ctypes.POINTER(vp)]
+    L.ll_init_batch.restype = ctypes.c_int
+    L.ll_decode_steps_batch.argtypes = [vp, vp, ctypes.POINTER(i32), i32, vp, vp]
+    L.ll_decode_steps_batch.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -240,6 +247,28 @@ def ll_decode_step_static(cfg: ll_config, weights: dict, k_cache, v_cache, token
     if rc != LL_OK:
         raise LLError(rc, err.value.decode())
     return int(nxt.value)
+
+
+def ll_init_batch(cfg: ll_config, weights: dict, k_caches, v_caches, stream=None):
+    """A batched handle: one (k, v) cache pair per sequence (lists of CUDA bf16 tensors)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    w, keep = _weights_struct(weights)
+    n = len(k_caches)
+    kp = (ctypes.c_void_p * max(1, n))(*[_ptr(t) for t in k_caches])
+    vp_ = (ctypes.c_void_p * max(1, len(v_caches)))(*[_ptr(t) for t in v_caches])
+    h = ctypes.c_void_p()
+    rc = lib().ll_init_batch(ctypes.byref(cfg), ctypes.byref(w), kp, vp_, int(n), ctypes.c_void_p(stream.cuda_stream),
+                             ctypes.byref(h))
+    if rc != LL_OK:
+        raise LLError(rc, lib().ll_init_error().decode())
+    return h
+
+
+def ll_decode_steps_batch(h, tokens_in_dev, positions, n_steps: int, logits, tokens_dev) -> None:
+    pos = (ctypes.c_int32 * max(1, len(positions)))(*[int(x) for x in positions])
+    _check(h, lib().ll_decode_steps_batch(h, _ptr(tokens_in_dev), pos, int(n_steps), _ptr(logits), _ptr(tokens_dev)))
 
 
 def ll_last_error(h) -> str:
@@ -385,3 +414,40 @@ class Decoder:
             self.close()
         except Exception:
             pass
+
+
+class BatchDecoder(Decoder):
+    """A batched handle (ll_init_batch) plus references to the tensors it points
+    into: n sequences, one (k, v) cache pair each, share every pass over the
+    weights. The model's tensors and every cache are checked at construction, the
+    buffers of every launch before its library call."""
+
+    def __init__(self, shape, weights: dict, k_caches, v_caches, max_seq: int, stream=None):
+        import torch
+        self.handle = None
+        n = len(k_caches)
+        if n not in (1, 2, 4, 8) or len(v_caches) != n:
+            raise LLError(LL_ERR_ARG, "the batch must be 1, 2, 4 or 8 sequences, one (k, v) cache pair each")
+        for k, v in zip(k_caches, v_caches):
+            check_model(shape, weights, k, v, max_seq)
+        self.n = n
+        self.shape = shape
+        self.weights = weights
+        self.k_caches, self.v_caches = list(k_caches), list(v_caches)
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.cfg = make_config(shape, max_seq, LL_BACKEND_MEGAKERNEL)
+        self.device = getattr(weights["embed"], "device", None)
+        self.handle = ll_init_batch(self.cfg, weights, self.k_caches, self.v_caches, self.stream)
+
+    def steps_batch(self, tokens_in_dev, positions, n_steps: int, logits, tokens_dev) -> None:
+        """n_steps greedy steps of every sequence in one launch: tokens_in_dev [n]
+        int32, positions a host list of n first positions, logits [n_steps][n][vocab]
+        fp32 or None, tokens_dev [n_steps][n] int32."""
+        import torch
+        if len(positions) != self.n:
+            raise LLError(LL_ERR_ARG, f"{self.n} positions needed, got {len(positions)}")
+        steps = max(int(n_steps), 0)
+        _need(tokens_in_dev, "tokens_in_dev", torch.int32, self.n, self.device, optional=False)
+        _need(logits, "logits", torch.float32, steps * self.n * int(self.shape.vocab), self.device)
+        _need(tokens_dev, "tokens_dev", torch.int32, steps * self.n, self.device, optional=False)
+        ll_decode_steps_batch(self.handle, tokens_in_dev, positions, n_steps, logits, tokens_dev)

@@ -141,6 +141,36 @@ int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, fl
 int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t n_steps, float *logits_dev,
                     int32_t *tokens_dev);
 
+/* Small-batch decode: n_seq independent sequences (1, 2, 4 or 8) share every
+ * pass over the weights. The page's method is batch 1; it says a batch turns the
+ * matrix-vector products into skinny matrix products, where tensor cores pay
+ * (its paragraph on CUDA-core against tensor-core matvec), so these handles run
+ * the tensor-core kernel: each weight page is multiplied with all sequences'
+ * inputs in the same m16n8k16 products, while every sequence keeps its own KV
+ * cache, position, attention items, logits and greedy tokens.
+ *
+ * ll_init_batch: as ll_init, with k_caches / v_caches host arrays of n_seq
+ * device pointers, one cache pair per sequence, each laid out as ll_init's
+ * (caller-owned, 16-byte aligned). Needs hidden, n_q_heads*head_dim and inter
+ * multiples of 1024, the megakernel backend, and rows per SM x n_seq within the
+ * kernel's accumulator (LL_ERR_SHAPE otherwise); attention uses the block-wide
+ * softmax variant and about max_seq / 128 KV splits, at most n_sm / (n_kv *
+ * n_seq). A batched handle is stepped only by ll_decode_steps_batch (the other
+ * step calls return LL_ERR_ARG); ll_synchronize, ll_set_timeout_ns,
+ * ll_set_trace, ll_query (LL_Q_BATCH) and ll_free apply as to any handle. */
+int ll_init_batch(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_caches, uint16_t *const *v_caches,
+                  int32_t n_seq, void *stream, ll_handle **out);
+
+/* n_steps greedy steps of every sequence of a batched handle in one launch.
+ * tokens_in_dev: device [n_seq] input tokens of the first step. pos_host: host
+ * [n_seq] first positions (sequence b decodes at pos_host[b] + i in step i;
+ * every pos_host[b] + n_steps <= max_seq, LL_ERR_ARG otherwise). logits_dev:
+ * device [n_steps][n_seq][vocab] fp32, or NULL. tokens_dev: device
+ * [n_steps][n_seq] greedy tokens; step i of sequence b reads the token step i - 1
+ * chose for it. Asynchronous on the handle's stream, errors as ll_decode_steps. */
+int ll_decode_steps_batch(ll_handle *h, const int32_t *tokens_in_dev, const int32_t *pos_host, int32_t n_steps,
+                          float *logits_dev, int32_t *tokens_dev);
+
 /* Wait for the handle's stream, then return and clear the device status of the
  * steps enqueued since the last check (LL_OK if all of them succeeded). After
  * an error the library clears its device state, so the next step starts clean. */
@@ -175,6 +205,7 @@ int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
 #define LL_Q_LAUNCHES_PER_STEP 6 /* kernel launches one decode step makes (ll_decode_steps: one launch for all its steps) */
 #define LL_Q_SMEM_BYTES 7       /* dynamic shared memory per block */
 #define LL_Q_TRACE_BYTES 8      /* size of the buffer ll_set_trace needs */
+#define LL_Q_BATCH 10           /* sequences a handle decodes together */
 #define LL_Q_MV_TC 9            /* matrix-vector widths on tensor-core pages: bit 0 hidden, bit 1 n_q*head_dim, bit 2 inter */
 int ll_query(const ll_handle *h, int what, int64_t *value);
 

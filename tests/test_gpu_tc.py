@@ -1,10 +1,11 @@
 """The tensor-core matrix-vector pages (LL_MV_TC=1) against the CPU oracle, and
 against the CUDA-core pages of the same kernel design.
 
-The tensor-core pages hold up to eight whole rows of a matrix loaded by TMA in
-the 128-byte swizzle and multiply them with three bf16 terms of the input on
-mma.sync; they apply to the widths 512..2048 (the 1B shape's hidden and
-attention widths, the H=512 test shapes). The parity rule is the logits' rule.
+The tensor-core pages hold up to eight rows of one 2048- (or 1024-) column chunk
+of a matrix, loaded by TMA in the 128-byte swizzle, and multiply them with
+three bf16 terms of the input on mma.sync; the tensor-core kernel takes every
+width on them, so it needs every width a multiple of 1024 (the 1B, 3B and 8B
+shapes, the H=1024 test shape). The parity rule is the logits' rule.
 """
 import numpy as np
 import pytest
@@ -29,7 +30,7 @@ def _tc(monkeypatch):
 def test_tensor_core_pages_are_active_for_1b():
     wl = synth.WORKLOADS["1b"]
     pr = Pair(wl.shape, 8)
-    assert pr.dec.query(ll.LL_Q_MV_TC) == 3  # hidden and n_q*head_dim widths
+    assert pr.dec.query(ll.LL_Q_MV_TC) == 7  # hidden, n_q*head_dim and inter widths
     pr.close()
 
 
@@ -45,12 +46,13 @@ def test_llama1b_ctx1024_tensor_core_pages():
 
 
 @pytest.mark.parametrize("flash", ["0", "1"], ids=["block-attention", "per-warp-attention"])
-def test_head_layout_prefill_and_decode_tensor_core_pages(flash, monkeypatch):
-    # H = 512: 16 warps of 32 columns each, pages of 8 rows with a ragged last page
+def test_h1024_prefill_and_decode_tensor_core_pages(flash, monkeypatch):
+    # H = 1024: one 1024-column chunk, 16 warps of 64 columns each; inter 3072:
+    # three chunks; pages of 8 rows with ragged last pages
     monkeypatch.setenv("LL_ATTN_FLASH", flash)
-    shape = synth.ModelShape("gqa8-hd64", 2, 512, 8, 1, 64, 1024, 4096, True)
+    shape = synth.ModelShape("h1024", 2, 1024, 16, 4, 64, 3072, 4096, True)
     pr = Pair(shape, 160, gain_jitter=0.25)
-    assert pr.dec.query(ll.LL_Q_MV_TC) == 3
+    assert pr.dec.query(ll.LL_Q_MV_TC) == 7
     toks = synth.make_tokens(shape.vocab, 150, seed=1)
     tok = toks[0]
     for pos in range(150):
@@ -66,7 +68,7 @@ def test_multi_step_launch_equals_chained_steps_tensor_core_pages():
     for multi in (False, True):
         k, v = synth.make_kv(shape, ctx + n + 1, ctx, seed=2, device="cuda")
         dec = ll.Decoder(shape, w, k, v, ctx + n + 1)
-        assert dec.query(ll.LL_Q_MV_TC) == 3
+        assert dec.query(ll.LL_Q_MV_TC) == 7
         logits = torch.empty((n, shape.vocab), dtype=torch.float32, device="cuda")
         toks = torch.zeros(n, dtype=torch.int32, device="cuda")
         tok = torch.tensor([5], dtype=torch.int32, device="cuda")
@@ -94,7 +96,7 @@ def test_tensor_core_and_cuda_core_pages_agree(monkeypatch):
         monkeypatch.setenv("LL_MV_TC", tc)
         k, v = synth.make_kv(shape, ctx + 1, ctx, seed=2, device="cuda")
         dec = ll.Decoder(shape, w, k, v, ctx + 1)
-        assert dec.query(ll.LL_Q_MV_TC) == (3 if tc == "1" else 0)
+        assert dec.query(ll.LL_Q_MV_TC) == (7 if tc == "1" else 0)
         logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
         nxt = dec.step(11, ctx, logits)
         res.append((nxt, logits.cpu().numpy()))
