@@ -400,6 +400,7 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
     ll::LayerW *d_layers = nullptr;
     ll::PDesc *d_pdesc = nullptr;
     ll::TensorMap *d_wmaps = nullptr;
+    ll::TensorMap *d_kvmaps = nullptr;
     int32_t *d_pdesc_off = nullptr;
     float2 *d_rope = nullptr;
     float *x = nullptr, *qkv = nullptr, *part = nullptr, *o = nullptr, *act = nullptr;
@@ -418,6 +419,7 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
         {reinterpret_cast<void **>(&d_layers), size_t(c.n_layers) * sizeof(ll::LayerW)},
         {reinterpret_cast<void **>(&d_pdesc), pdesc.size() * sizeof(ll::PDesc)},
         {reinterpret_cast<void **>(&d_wmaps), wmaps.size() * sizeof(ll::TensorMap)},
+        {reinterpret_cast<void **>(&d_kvmaps), size_t(nb) * ll::TM_COUNT * sizeof(ll::TensorMap)},
         {reinterpret_cast<void **>(&d_pdesc_off), pdesc_off.size() * sizeof(int32_t)},
         {reinterpret_cast<void **>(&d_rope), size_t(c.max_seq) * (c.head_dim / 2) * sizeof(float2)},
         {reinterpret_cast<void **>(&x), size_t(c.hidden) * 4},
@@ -509,9 +511,21 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
         const int pp = ll::PAGE_BYTES / (4 * c.head_dim);
         p.attn_flash = (per_split + pp - 1) / pp >= 4 ? 1 : 0;
         if (const char *e = std::getenv("LL_ATTN_FLASH")) p.attn_flash = std::atoi(e) ? 1 : 0;
-        if (nb > 1) p.attn_flash = 0;  // the per-warp variant serves one sequence
-        // its KV pages come through TMA tensor maps; without them, the block variant
+        // its KV pages come through TMA tensor maps (each sequence's, for the
+        // tensor-core kernel, in library memory); without them, the block variant
         if (!encode_kv_maps(c, k_cache, v_cache, p.kv_maps)) p.attn_flash = 0;
+        std::vector<ll::TensorMap> kvm(size_t(nb) * ll::TM_COUNT);
+        for (int b = 0; b < nb && p.attn_flash; b++) {
+            ll::TensorMap one[ll::TM_COUNT];
+            if (!encode_kv_maps(c, k_caches[b], v_caches[b], one)) p.attn_flash = 0;
+            for (int i = 0; i < ll::TM_COUNT; i++) kvm[size_t(b) * ll::TM_COUNT + i] = one[i];
+        }
+        if (p.attn_flash &&
+            cudaMemcpy(d_kvmaps, kvm.data(), kvm.size() * sizeof(ll::TensorMap), cudaMemcpyHostToDevice) != cudaSuccess) {
+            ll_free(h);
+            return bad(LL_ERR_CUDA, "KV tensor map upload failed");
+        }
+        p.kvmaps_b = d_kvmaps;
     }
     p.mv_h = mh;
     p.mv_q = mq;
@@ -736,19 +750,21 @@ int ll_debug_inject(ll_handle *h, int kind, int layer, int op) {
     return upload_schedule(h);
 }
 
-int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr) {
-    if (!cfg || nsm <= 0 || cfg->n_layers < 1 || cfg->n_kv_heads <= 0 || cfg->n_q_heads % cfg->n_kv_heads != 0)
-        return LL_ERR_ARG;
-    std::vector<std::vector<Instr>> lists;
-    build_lists_for(*cfg, nsm, attn_splits(*cfg, nsm), lists);
+}  // extern "C"
+
+namespace {
+// Per-SM instruction lists as [nsm][max_instr][7] int32 records (op, layer, r0,
+// r1, wait_ctr, wait_count, sig_ctr; op -1 past a list's end).
+int dump_lists(const std::vector<std::vector<Instr>> &lists, int32_t *out, size_t out_len, int32_t *max_instr) {
     size_t mx = 0;
     for (auto &l : lists) mx = std::max(mx, l.size());
     if (max_instr) *max_instr = static_cast<int32_t>(mx);
     if (!out) return LL_OK;
-    if (out_len < size_t(nsm) * mx * 7) return LL_ERR_ARG;
-    for (int sm = 0; sm < nsm; sm++) {
+    const size_t nsm = lists.size();
+    if (out_len < nsm * mx * 7) return LL_ERR_ARG;
+    for (size_t sm = 0; sm < nsm; sm++) {
         for (size_t i = 0; i < mx; i++) {
-            int32_t *o = out + (size_t(sm) * mx + i) * 7;
+            int32_t *o = out + (sm * mx + i) * 7;
             if (i < lists[sm].size()) {
                 const Instr &in = lists[sm][i];
                 o[0] = in.op; o[1] = in.layer; o[2] = in.r0; o[3] = in.r1;
@@ -759,6 +775,22 @@ int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int
         }
     }
     return LL_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr) {
+    if (!cfg || nsm <= 0 || cfg->n_layers < 1 || cfg->n_kv_heads <= 0 || cfg->n_q_heads % cfg->n_kv_heads != 0)
+        return LL_ERR_ARG;
+    std::vector<std::vector<Instr>> lists;
+    build_lists_for(*cfg, nsm, attn_splits(*cfg, nsm), lists);
+    return dump_lists(lists, out, out_len, max_instr);
+}
+
+int ll_handle_plan(const ll_handle *h, int32_t *out, size_t out_len, int32_t *max_instr) {
+    if (!h) return LL_ERR_ARG;
+    return dump_lists(h->lists, out, out_len, max_instr);
 }
 
 const char *ll_last_error(const ll_handle *h) { return h ? h->err.c_str() : "null handle"; }

@@ -148,6 +148,7 @@ struct KParams {
     int32_t nb;
     int32_t pos_b[MAX_B];     // each sequence's position in the launch's first step
     uint16_t *kc_b[MAX_B], *vc_b[MAX_B];
+    const TensorMap *kvmaps_b; // [nb][TM_COUNT] each sequence's KV tensor maps (global memory; the per-warp attention)
     // Activations between instructions, as tagged words: (tag << 32) | fp32 bits,
     // stored and loaded as single 8-byte accesses. A reader takes a word only
     // when its tag is the one of the current step and layer (tag_of), so the

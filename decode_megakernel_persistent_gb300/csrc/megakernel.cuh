@@ -1284,7 +1284,7 @@ __device__ __forceinline__ void attn_tiles(const Smem &s, uint32_t kbase, uint32
     }
 }
 
-template <int DL>
+template <int DL, bool BATCH = false>
 __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     const int g = ins.r0, c = ins.r1, S = p.attn_splits, l = ins.layer;
     constexpr int hd = DL * 32, half = hd / 2;
@@ -1292,14 +1292,17 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     const int qd = p.nq * hd, kd = p.nkv * hd;
     const bool owner = c == S - 1;  // this split owns position pos
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
-    const float2 *cs = p.rope_cs + size_t(s.c_pos) * half;
+    const int b = BATCH ? int(ins.sub) : 0;
+    const int pos = BATCH ? s.bpos[b] : s.c_pos;
+    const float2 *cs = p.rope_cs + size_t(pos) * half;
+    const uint64_t *qkv_b = p.t_qkv + size_t(b) * (qd + 2 * kd);
     const uint32_t tag = tag_of(p, s, l);
     // the group's query heads with RoPE ("rotate half") applied, pre-scaled by
     // 1/sqrt(hd); the owner also rotates the new key and takes the new value
     {
-        const uint64_t *qh = p.t_qkv + size_t(g * G) * hd;
-        const uint64_t *kh = p.t_qkv + qd + size_t(g) * hd;
-        const uint64_t *vh = p.t_qkv + qd + kd + size_t(g) * hd;
+        const uint64_t *qh = qkv_b + size_t(g * G) * hd;
+        const uint64_t *kh = qkv_b + qd + size_t(g) * hd;
+        const uint64_t *vh = qkv_b + qd + kd + size_t(g) * hd;
         const bool has_q = tid < G * hd, has_k = owner && tid < half, has_v = owner && tid < hd;
         const int h = tid / hd, d = tid % hd, i = d < half ? d : d - half;
         uint64_t w[5];
@@ -1346,11 +1349,12 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     consumer_sync();
     if (tid == 0) trace_put(p, ii, 1);
     if (owner) {
-        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + s.c_pos) * hd;
+        const size_t at = ((size_t(l) * p.nkv + g) * size_t(p.max_seq) + pos) * hd;
+        uint16_t *kc = BATCH ? p.kc_b[b] : p.k_cache, *vc = BATCH ? p.vc_b[b] : p.v_cache;
         if (LL_OK_IDX(16, at + hd, size_t(p.L) * p.nkv * p.max_seq * hd + 1))
             for (int d = tid; d < hd; d += NCT) {
-                p.k_cache[at + d] = s.knew[d];
-                p.v_cache[at + d] = s.vnew[d];
+                kc[at + d] = s.knew[d];
+                vc[at + d] = s.vnew[d];
             }
     }
     // this lane's share of the running softmax and output (see attn_tiles)
@@ -1358,7 +1362,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
 #pragma unroll
     for (int d = 0; d < 8; d++) o[d][0] = o[d][1] = 0.f;
     int c0, c1;
-    attn_range(p, s.c_pos, c, c0, c1);
+    attn_range(p, pos, c, c0, c1);
     const int PP = attn_pp(p);
     // The warps form DG dim groups (64 dims each); within a dim group, NGR page
     // groups of W warps each take every NGR-th page of the item, W warps sharing a
@@ -1437,7 +1441,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
     const int stride = hd + 4;
     const uint32_t wtag = write_tag(p, s, ins);
     if (tw == 0 && gq < G) {
-        uint64_t *dst = p.t_part + (size_t(g * G + gq) * S + c) * stride;
+        uint64_t *dst = p.t_part + size_t(b) * p.nq * S * stride + (size_t(g * G + gq) * S + c) * stride;
 #pragma unroll
         for (int d = 0; d < 8; d++) {
             st_tag(dst + 64 * dg + 8 * d + 2 * tq, o[d][0], wtag);
@@ -1449,7 +1453,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
         }
     }
     if (tid == 0) trace_put(p, ii, 2);
-    return merge_splits(p, s, g, c, G, hd, tag, wtag);
+    return merge_splits(p, s, g, c, G, hd, tag, wtag, b);
 }
 
 
@@ -1628,15 +1632,24 @@ __device__ __forceinline__ int tc_seq(int r, int nb, int T, int &term) {
     return b < nb ? b : -1;
 }
 
-// The next T bf16 terms of v: term k is the bf16 nearest to what terms 0..k-1
-// leave of v.
-__device__ __forceinline__ uint16_t bf16_term(float v, int term) {
-    uint16_t h = 0;
-    for (int k = 0; k <= term; k++) {
-        h = f_to_bf16(v);
-        v -= bf16_to_f(h);
-    }
-    return h;
+// Term `term` (0, 1, 2) of the pair (v0, v1) as packed bf16x2: term k is the
+// bf16 nearest (round to nearest even, the cvt instruction) to what terms
+// 0..k-1 leave of each value.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_term(float v0, float v1, int term) {
+    uint32_t h = cvt_bf16x2(v0, v1);
+    if (term == 0) return h;
+    v0 -= bf_lo(h);
+    v1 -= bf_hi(h);
+    h = cvt_bf16x2(v0, v1);
+    if (term == 1) return h;
+    v0 -= bf_lo(h);
+    v1 -= bf_hi(h);
+    return cvt_bf16x2(v0, v1);
 }
 
 // A fragments of column chunk c for this lane's two A rows (g and g + 8):
@@ -1704,7 +1717,7 @@ __device__ bool tc_fragments(const KParams &p, Smem &s, const Instr &ins, const 
                         v0 *= bf_lo(gw);
                         v1 *= bf_hi(gw);
                     }
-                    a[j][h + 2 * q] = uint32_t(bf16_term(v0, term)) | (uint32_t(bf16_term(v1, term)) << 16);
+                    a[j][h + 2 * q] = bf16x2_term(v0, v1, term);
                 }
             }
         }
@@ -1789,11 +1802,16 @@ __device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Ins
                 // D: lane (g, t) holds A rows g (d0, d1) and g + 8 (d2, d3) at page rows
                 // 2t, 2t + 1; a sequence's terms are the rows below its term 0, 4 lanes apart
                 float v[4] = {d[0] + e[0], d[1] + e[1], d[2] + e[2], d[3] + e[3]};
+                if (T == 3) {
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const float u4 = __shfl_down_sync(0xffffffffu, v[i], 4);
-                    const float u8 = __shfl_down_sync(0xffffffffu, v[i], 8);
-                    v[i] += u4 + (T == 3 ? u8 : 0.f);
+                    for (int i = 0; i < 4; i++) {
+                        const float u4 = __shfl_down_sync(0xffffffffu, v[i], 4);
+                        const float u8 = __shfl_down_sync(0xffffffffu, v[i], 8);
+                        v[i] += u4 + u8;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; i++) v[i] += __shfl_down_sync(0xffffffffu, v[i], 4);
                 }
                 // partials [row][sequence] into the page lines of this warp's columns
                 float *own = reinterpret_cast<float *>(pg + size_t((warp * KS) >> 2) * nr * 128);
@@ -1857,13 +1875,12 @@ __device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Ins
 // FLASH: the kernel variant for long attention items (see attn_tiles); the other
 // variant keeps a block-wide softmax per page, cheaper when an item spans a page
 // or two. The host picks the variant by the longest item at max_seq.
-// (TC: the tensor-core kernel, whose block-softmax items carry their sequence;
-// its per-warp variant serves single-sequence handles only)
+// (TC: the tensor-core kernel, whose items carry their sequence)
 template <bool FLASH, bool TC = false>
 __device__ bool attn_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage) {
     if constexpr (FLASH)
-        return p.hd == 64 ? attn_item_flash<2>(p, s, pages, ins, ii, cpage)
-                          : attn_item_flash<4>(p, s, pages, ins, ii, cpage);
+        return p.hd == 64 ? attn_item_flash<2, TC>(p, s, pages, ins, ii, cpage)
+                          : attn_item_flash<4, TC>(p, s, pages, ins, ii, cpage);
     else
         return p.hd == 64 ? attn_item<2, TC>(p, s, pages, ins, ii, cpage) : attn_item<4, TC>(p, s, pages, ins, ii, cpage);
 }
@@ -1938,6 +1955,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
             int a_c0 = 0, a_c1 = 1, a_p0 = 0, a_n = 0;
             size_t head_row = 0;
             const uint16_t *a_kc = p.k_cache, *a_vc = p.v_cache;  // the item's sequence's caches
+            const TensorMap *a_maps = p.kv_maps;                 // and KV tensor maps
             if (e.kind == PD_ATTN && st > gate) {
                 const uint64_t t0 = gtimer();
                 for (uint32_t it = 1; s.tok_step < st; ++it) {
@@ -1965,6 +1983,7 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                     a_pos = p.pos_b[b] + st;
                     a_kc = p.kc_b[b];
                     a_vc = p.vc_b[b];
+                    a_maps = p.kvmaps_b + size_t(b) * TM_COUNT;
                 }
                 attn_range(p, a_pos, c, a_c0, a_c1);
                 a_p0 = a_c0;
@@ -2043,10 +2062,10 @@ __device__ void producer(const KParams &p, Smem &s, uint8_t *pages) {
                         for (int h = 0; h < dh; h++) {
                             uint8_t *d = dst + kv * (PAGE_BYTES / 2) + h * PP * 128;
                             if (a_n == PP) {
-                                tma_load_2d(d, &p.kv_maps[kv ? TM_V_PAGE : TM_K_PAGE], 64 * h, a_row, &s.full[slot]);
+                                tma_load_2d(d, &a_maps[kv ? TM_V_PAGE : TM_K_PAGE], 64 * h, a_row, &s.full[slot]);
                             } else {
                                 for (int j = 0; j < a_n; j += ATT_TILE)
-                                    tma_load_2d(d + j * 128, &p.kv_maps[kv ? TM_V_TILE : TM_K_TILE], 64 * h, a_row + j,
+                                    tma_load_2d(d + j * 128, &a_maps[kv ? TM_V_TILE : TM_K_TILE], 64 * h, a_row + j,
                                                 &s.full[slot]);
                             }
                         }
@@ -2170,7 +2189,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
 // CUDA-core kernel carries none of that code: its size matters, the step being
 // sensitive to instruction-cache misses when the instruction kind changes.
 template <bool FLASH, bool TC>
-__global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
+__device__ __forceinline__ void megakernel_body(const KParams &p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *pages = smem;
     Smem &s = *reinterpret_cast<Smem *>(smem + NPAGES * PAGE_BYTES);
@@ -2226,6 +2245,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
         consumer<FLASH, TC>(p, s, pages);
     }
 }
+
+// One block of NTHREADS per SM: ptxas gives each thread 96 registers (17 warps
+// on 4 schedulers: 5 warps share one scheduler's 16K registers).
+template <bool FLASH, bool TC>
+__global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
+    megakernel_body<FLASH, TC>(p);
+}
+
 
 }  // namespace
 }  // namespace ll

@@ -47,7 +47,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
 EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_decode_steps", "ll_synchronize",
            "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
-           "ll_free", "ll_decode_step_static", "ll_init_batch", "ll_decode_steps_batch")
+           "ll_free", "ll_decode_step_static", "ll_init_batch", "ll_decode_steps_batch", "ll_handle_plan")
 
 
 class LLError(RuntimeError):
@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
     L.ll_init_batch.restype = ctypes.c_int
     L.ll_decode_steps_batch.argtypes = [vp, vp, ctypes.POINTER(i32), i32, vp, vp]
     L.ll_decode_steps_batch.restype = ctypes.c_int
+    L.ll_handle_plan.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(i32)]
+    L.ll_handle_plan.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -226,6 +228,17 @@ def ll_plan(cfg: ll_config, nsm: int):
     rc = lib().ll_plan(ctypes.byref(cfg), int(nsm), out.ctypes.data, out.size, ctypes.byref(mx))
     if rc != LL_OK:
         raise LLError(rc, "ll_plan failed")
+    return out
+
+
+def ll_handle_plan(h):
+    """The handle's own schedule as an int32 numpy array [nsm, max_instr, 7]."""
+    import numpy as np
+    mx = ctypes.c_int32()
+    _check(h, lib().ll_handle_plan(h, None, 0, ctypes.byref(mx)))
+    nsm = ll_query(h, LL_Q_NUM_SMS)
+    out = np.zeros((nsm, mx.value, 7), dtype=np.int32)
+    _check(h, lib().ll_handle_plan(h, out.ctypes.data, out.size, ctypes.byref(mx)))
     return out
 
 

@@ -129,6 +129,8 @@ def main():
                     help="run the same steps with tracing off (a target for external profilers)")
     ap.add_argument("--l2-resident", action="store_true",
                     help="a 2-layer hidden-1024 model whose weights (~90 MB) stay in L2")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="trace a batched handle of this many sequences (ll_init_batch)")
     args = ap.parse_args()
     if args.load:
         d = np.load(args.load)
@@ -146,8 +148,12 @@ def main():
         ctx = 1024
     max_seq = ctx + args.steps + 1
     w = synth.make_weights(shape, seed=0, device="cuda")
-    k, v = synth.make_kv(shape, max_seq, ctx, seed=2, device="cuda")
-    dec = ll.Decoder(shape, w, k, v, max_seq)
+    if args.batch:
+        kv = [synth.make_kv(shape, max_seq, ctx, seed=2 + b, device="cuda") for b in range(args.batch)]
+        dec = ll.BatchDecoder(shape, w, [x[0] for x in kv], [x[1] for x in kv], max_seq)
+    else:
+        k, v = synth.make_kv(shape, max_seq, ctx, seed=2, device="cuda")
+        dec = ll.Decoder(shape, w, k, v, max_seq)
     nbytes = dec.query(ll.LL_Q_TRACE_BYTES)
     buf = torch.zeros(nbytes // 8, dtype=torch.int64, device="cuda")
     if not args.notrace:
@@ -155,14 +161,19 @@ def main():
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     tok = 1
     for i in range(args.steps):
-        tok = dec.step(tok, ctx + i, logits)
+        if args.batch:  # every sequence one step, one launch per step
+            toks = torch.ones((1, args.batch), dtype=torch.int32, device="cuda")
+            dec.steps_batch(toks[0], [ctx + i] * args.batch, 1, None, toks)
+            dec.synchronize()
+        else:
+            tok = dec.step(tok, ctx + i, logits)
     if args.notrace:
         torch.cuda.synchronize()
         print(json.dumps({"steps": args.steps, "workload": wl.name, "traced": False}))
         dec.close()
         return
     nsm = dec.query(ll.LL_Q_NUM_SMS)
-    plan = ll.ll_plan(dec.cfg, nsm)
+    plan = ll.ll_handle_plan(dec.handle)
     flat = buf.cpu().numpy()
     n_instr_words = nsm * plan.shape[1] * 12
     tr = flat[:n_instr_words].reshape(nsm, plan.shape[1], 12)

@@ -230,6 +230,10 @@ int ll_debug_inject(ll_handle *h, int kind, int layer, int op);
  * them ready by their tags); -1 where there is none. */
 int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int32_t *max_instr);
 
+/* The handle's own per-SM instruction lists, in ll_plan's format (for a batched
+ * handle they hold its sequences' attention items and LM-head pieces). */
+int ll_handle_plan(const ll_handle *h, int32_t *out, size_t out_len, int32_t *max_instr);
+
 /* Explanation of the last error on this handle (never NULL). */
 const char *ll_last_error(const ll_handle *h);
 

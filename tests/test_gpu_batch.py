@@ -89,6 +89,15 @@ def test_batch_small_model_every_step_matches_oracles(n):
     check_against_oracles(orcs, first, out, fills, 6, f"batch {n}")
 
 
+@pytest.mark.parametrize("n", [2, 4])
+def test_batch_per_warp_attention_variant(n, monkeypatch):
+    # the per-warp (flash) attention on each sequence's own KV tensor maps
+    monkeypatch.setenv("LL_ATTN_FLASH", "1")
+    fills = [200 + 61 * b for b in range(n)]
+    orcs, first, out = run_batch(SMALL, n, fills, 5)
+    check_against_oracles(orcs, first, out, fills, 5, f"per-warp batch {n}")
+
+
 def test_batch_from_empty_caches():
     # every sequence from position 0 (its cache written by the launch itself),
     # 20 greedy steps, every step against the oracles
