@@ -7,14 +7,17 @@ layer, LM head and argmax, run by the persistent megakernel through the C ABI.
                   [--backend megakernel|chain] [--impl ours|reference]
 
 Default workload: Llama-3.2-1B shape, bf16 weights bf16(0.02*N(0,1)) from seed
-0, a 1024-token random prompt (seed 1) prefilled through the model, then K
-greedy decode steps timed with CUDA events on the decode stream: one
-ll_decode_steps launch in which each step takes the token the previous one
-chose (no host round trip). ``single_step_launches`` times the same K positions
-again as K chained single-step launches. The weights (2.47 GB) are far larger
-than L2 (129 MB), so every step streams them from HBM. ``e2e`` repeats K steps
-through ll_decode_step with the token passed from the host and the next token
-read back to host memory every step, timed by the host clock.
+0, a 1024-token random prompt (seed 1) prefilled through the model in one
+ll_prefill call (tcgen05 GEMMs; timed on its own as ``prefill``), then K greedy
+decode steps timed with CUDA events on the decode stream: one ll_decode_steps
+launch in which each step takes the token the previous one chose (no host
+round trip). ``single_step_launches`` times the same K positions again as K
+chained single-step launches. The weights (2.47 GB) are far larger than L2 (129
+MB), so every step streams them from HBM. ``e2e`` repeats K steps through
+ll_decode_step with the token passed from the host and the next token read
+back to host memory every step, timed by the host clock. ``batch`` times
+batched handles (ll_decode_steps_batch) of 2, 4 and 8 sequences on seeded
+N(0,1) caches at the same context: tokens/s of all sequences together.
 
 ``--impl reference`` times the CPU oracle (the only reference implementation
 there is) on the host cores on the same workload. Under torchrun every rank
@@ -51,6 +54,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-batch", action="store_true", help="skip the batched-decode lines")
     return ap.parse_args()
 
 
@@ -266,6 +270,38 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------------
 
+def batch_lines(shape, w, ctx, dev, K):
+    """Decode throughput of batched handles (2, 4, 8 sequences) at context ctx on
+    seeded N(0,1) caches: one ll_decode_steps_batch launch of K steps, timed with
+    CUDA events after a warm-up launch."""
+    import torch
+
+    from decode_megakernel_persistent_gb300 import ll, synth
+    out = {}
+    for n in (2, 4, 8):
+        max_seq = ctx + K + 8
+        kv = [synth.make_kv(shape, max_seq, ctx, seed=2 + b, device=dev) for b in range(n)]
+        dec = ll.BatchDecoder(shape, w, [x[0] for x in kv], [x[1] for x in kv], max_seq)
+        toks = torch.zeros((K, n), dtype=torch.int32, device=dev)
+        first = torch.tensor(synth.make_tokens(shape.vocab, n, seed=3), dtype=torch.int32, device=dev)
+        dec.steps_batch(first, [ctx] * n, 4, None, toks[:4])
+        dec.synchronize()
+        s = torch.cuda.current_stream(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        dec.steps_batch(first, [ctx + 4] * n, K, None, toks)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        dec.synchronize()
+        secs = e0.elapsed_time(e1) / 1e3
+        out[str(n)] = {"tokens_per_s": n * K / secs, "us_per_step": 1e6 * secs / K,
+                       "kv_splits": dec.query(ll.LL_Q_ATTN_SPLITS)}
+        dec.close()
+        del kv
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -290,11 +326,30 @@ def run_ours(args):
     logits = torch.empty(shape.vocab, dtype=torch.float32, device=dev)
     tok = torch.zeros(1, dtype=torch.int32, device=dev)
     prompt = synth.make_tokens(shape.vocab, max(ctx, 1), seed=1 + rank)
+    prefill = None
     with torch.cuda.stream(stream):
         if wl.kv_fill == "prefill":
             prompt_dev = torch.tensor(prompt, dtype=torch.int32, device=dev)
-            for pos in range(ctx):
-                dec.step_async(prompt_dev[pos:pos + 1], pos, logits, tok)
+            if backend == ll.LL_BACKEND_MEGAKERNEL:
+                # the prompt in one pass (tcgen05 GEMMs); once untimed (the first
+                # call makes its buffers), then timed
+                dec.prefill(prompt_dev, 0, logits, tok)
+                dec.synchronize()
+                p0 = torch.cuda.Event(enable_timing=True)
+                p1 = torch.cuda.Event(enable_timing=True)
+                p0.record(stream)
+                dec.prefill(prompt_dev, 0, logits, tok)
+                p1.record(stream)
+                torch.cuda.synchronize(dev)
+                secs = p0.elapsed_time(p1) / 1e3
+                flops = 2.0 * ctx * bytemodel.layer_weight_elements(shape)
+                prefill = {"tokens": ctx, "ms": 1e3 * secs, "tokens_per_s": ctx / secs,
+                           "tflops_algorithmic": flops / secs / 1e12,
+                           "tflops_tensor": 3 * flops / secs / 1e12,
+                           "call": "ll_prefill: every projection a tcgen05 GEMM, activations as 3 bf16 terms"}
+            else:
+                for pos in range(ctx):
+                    dec.step_async(prompt_dev[pos:pos + 1], pos, logits, tok)
         else:
             tok.fill_(prompt[0])
         dec.synchronize()
@@ -380,6 +435,9 @@ def run_ours(args):
         cpu["single_thread"] = {"value": n1 / secs1, "unit": "tokens/s", "cores": 1,
                                 "sample": f"{n1} full oracle decode steps on one thread at positions "
                                           f"{ctx}..{ctx + n1 - 1}, {secs1:.1f} s"}
+    batch = None
+    if not args.no_batch and backend == ll.LL_BACKEND_MEGAKERNEL and shape.hidden % 1024 == 0:
+        batch = batch_lines(shape, w, ctx, dev, K)
     line = {
         "metric": METRIC,
         "value": world * K / t_dev,
@@ -410,6 +468,8 @@ def run_ours(args):
         "e2e": {"value": world * K / t_e2e, "unit": "tokens/s", "us_per_token": 1e6 * t_e2e / K,
                 "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8},
         "gpu_launches": launches,
+        "prefill": prefill,
+        "batch": batch,
         "cpu_baseline": cpu,
         "clocks": clocks.summary() if clocks else None,
     }

@@ -38,6 +38,13 @@ def step_flops(shape: ModelShape, pos: int) -> int:
     return 2 * mats + attn
 
 
+def layer_weight_elements(shape: ModelShape) -> int:
+    """Elements of the layer matrices (every projection a prefill GEMM runs): the
+    algorithmic flops of a prefill of n positions are 2 * n * this (its attention
+    and the last position's LM head aside)."""
+    return shape.n_layers * sum(_numel(s) for k, s in shape.layer_shapes().items() if not k.endswith("norm"))
+
+
 def _numel(s) -> int:
     n = 1
     for d in s:

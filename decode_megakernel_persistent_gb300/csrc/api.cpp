@@ -29,6 +29,7 @@ struct ll_handle {
     KParams kp{};
     ll::ChainBufs cb{};
     std::vector<ll::LayerW> host_layers;
+    ll::PrefillBufs pf;          // prefill buffers, allocated by the first ll_prefill (grown by a longer one)
     std::vector<std::vector<Instr>> lists;
     Instr *d_instrs = nullptr;
     int max_instr = 0;
@@ -656,6 +657,28 @@ int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t
     return enqueue(h, 0, token_dev, pos, logits_dev, nullptr, n_steps, tokens_dev);
 }
 
+int ll_prefill(ll_handle *h, const int32_t *tokens_dev, int32_t n, int32_t pos0, float *logits_dev,
+               int32_t *next_token_dev) {
+    if (!h) return LL_ERR_ARG;
+    if (h->batch_api) return fail(h, LL_ERR_ARG, "prefill takes a single-sequence handle");
+    if (!tokens_dev || !next_token_dev) return fail(h, LL_ERR_ARG, "tokens_dev or next_token_dev is NULL");
+    if (n < 1 || pos0 < 0 || int64_t(pos0) + n > h->cfg.max_seq)
+        return fail(h, LL_ERR_ARG, "positions " + std::to_string(pos0) + ".." + std::to_string(int64_t(pos0) + n - 1) +
+                                       " outside [0, max_seq)");
+    if (logits_dev && !aligned16(logits_dev)) return fail(h, LL_ERR_ARG, "logits buffer not 16-byte aligned");
+    if (h->cfg.hidden % 64 || (h->cfg.n_q_heads * h->cfg.head_dim) % 64 || h->cfg.inter % 64)
+        return fail(h, LL_ERR_SHAPE, "prefill needs hidden, n_q_heads*head_dim and inter multiples of 64");
+    if (!ll::prefill_prepare(h->kp, h->host_layers.data(), n, h->pf))
+        return fail(h, LL_ERR_OOM, "prefill buffers for " + std::to_string(n) + " positions could not be made");
+    const int rc = ll::launch_prefill(h->kp, h->host_layers.data(), h->pf, tokens_dev, n, pos0, logits_dev,
+                                      next_token_dev, h->stream);
+    if (rc != LL_OK) {
+        cudaError_t e = cudaGetLastError();
+        return fail(h, rc, std::string("prefill launch failed: ") + cudaGetErrorString(e));
+    }
+    return LL_OK;
+}
+
 int ll_decode_steps_batch(ll_handle *h, const int32_t *tokens_in_dev, const int32_t *pos_host, int32_t n_steps,
                           float *logits_dev, int32_t *tokens_dev) {
     if (!h) return LL_ERR_ARG;
@@ -800,6 +823,7 @@ void ll_free(ll_handle *h) {
     cudaStreamSynchronize(h->stream);
     if (h->dmem) cudaFree(h->dmem);
     if (h->pinned) cudaFreeHost(h->pinned);
+    ll::prefill_release(h->pf);
     delete h;
 }
 

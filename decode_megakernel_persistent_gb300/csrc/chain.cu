@@ -269,6 +269,14 @@ int grid_for_rows(int rows, int nsm) {
 
 }  // namespace
 
+int launch_chain_head(const KParams &p, const float *x, float *h, float *logits, int32_t *next_dev, void *stream_) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream_);
+    k_rmsnorm<<<1, 1024, 0, st>>>(x, p.final_norm, p.H, p.eps, h);
+    k_matvec<<<grid_for_rows(p.V, p.nsm), 256, 0, st>>>(p.lm_head, h, p.V, p.H, logits, 0);
+    k_argmax<<<1, 1024, 0, st>>>(logits, p.V, next_dev, p.token_out, p.status);
+    return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
 int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream_) {
     cudaStream_t st = static_cast<cudaStream_t>(stream_);
     const int H = p.H, qd = p.nq * p.hd, kd = p.nkv * p.hd, I = p.I, G = p.nq / p.nkv;

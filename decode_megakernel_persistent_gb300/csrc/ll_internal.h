@@ -210,6 +210,32 @@ struct ChainBufs {
 // attention item per SM. Every entry point picks its splits with this.
 int attn_splits(int max_seq, int n_kv_heads, int nsm, int nb = 1);
 int launch_chain_step(const KParams &p, const ChainBufs &b, void *stream);
+// Final RMSNorm of the residual row x, LM head into logits (all vocab rows) and
+// greedy argmax into next_dev and p.token_out (p.status on all-NaN logits):
+// per-operation kernels of the chain, for the last position of a prefill.
+int launch_chain_head(const KParams &p, const float *x, float *h, float *logits, int32_t *next_dev, void *stream);
+
+// ---- prefill (prefill.cu): the prompt's positions through the model at once,
+// every projection a tcgen05 GEMM. Buffers for up to n_alloc tokens.
+struct PrefillBufs {
+    static constexpr int T = 3;          // bf16 terms of an activation matrix
+    int n_alloc = 0;
+    float *x = nullptr;                  // [n][H] residual stream
+    uint16_t *h[T] = {};                 // [n][H] normed input, as T bf16 terms
+    float *qkv = nullptr;                // [n][qd + 2 kd]
+    uint16_t *o[T] = {};                 // [n][qd] attention output, T terms
+    float *gate = nullptr;               // [n][I]
+    uint16_t *a[T] = {};                 // [n][I] silu(gate) * up, T terms
+    float *hrow = nullptr, *logits = nullptr;       // [H], [V]: the last position's head
+    TensorMap m_h[T], m_o[T], m_a[T];    // A operands (activations), boxes of 128 rows x 64 columns
+    std::vector<TensorMap> m_w;          // B operands: [L][7] wq, wk, wv, wo, wg, wu, wd, boxes of 128 rows x 64
+    void *mem = nullptr;
+};
+// Allocates (or grows) the buffers and encodes the maps; false on failure.
+bool prefill_prepare(const KParams &p, const LayerW *host_layers, int n, PrefillBufs &b);
+void prefill_release(PrefillBufs &b);
+int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, const int32_t *tokens_dev, int n,
+                   int pos0, float *logits, int32_t *next_dev, void *stream);
 
 // Host-side schedule construction (schedule.cpp). nb sequences (attention items
 // per sequence); an SM's LM-head rows in instructions of at most lm_rows rows.

@@ -47,7 +47,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libll.so")
 
 EXPORTS = ("ll_init", "ll_init_error", "ll_decode_step", "ll_decode_step_async", "ll_decode_steps", "ll_synchronize",
            "ll_set_trace", "ll_set_timeout_ns", "ll_query", "ll_debug_inject", "ll_plan", "ll_last_error",
-           "ll_free", "ll_decode_step_static", "ll_init_batch", "ll_decode_steps_batch", "ll_handle_plan")
+           "ll_free", "ll_decode_step_static", "ll_init_batch", "ll_decode_steps_batch", "ll_handle_plan",
+           "ll_prefill")
 
 
 class LLError(RuntimeError):
@@ -122,6 +123,8 @@ def lib() -> ctypes.CDLL:
     L.ll_decode_steps_batch.restype = ctypes.c_int
     L.ll_handle_plan.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(i32)]
     L.ll_handle_plan.restype = ctypes.c_int
+    L.ll_prefill.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.ll_prefill.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -229,6 +232,10 @@ def ll_plan(cfg: ll_config, nsm: int):
     if rc != LL_OK:
         raise LLError(rc, "ll_plan failed")
     return out
+
+
+def ll_prefill(h, tokens_dev, n: int, pos0: int, logits, next_token_dev) -> None:
+    _check(h, lib().ll_prefill(h, _ptr(tokens_dev), int(n), int(pos0), _ptr(logits), _ptr(next_token_dev)))
 
 
 def ll_handle_plan(h):
@@ -410,6 +417,16 @@ class Decoder:
         n = max(int(n_steps), 0)
         self._bufs(token_dev, logits, n, tokens_dev, n, out_required=True)
         ll_decode_steps(self.handle, token_dev, pos, n_steps, logits, tokens_dev)
+
+    def prefill(self, tokens_dev, pos0: int, logits, next_token_dev) -> None:
+        """All of tokens_dev (int32 [n]) at positions pos0..pos0+n-1 in one pass;
+        the last position's logits ([vocab] fp32, or None) and greedy token."""
+        import torch
+        n = int(tokens_dev.numel()) if tokens_dev is not None else 0
+        _need(tokens_dev, "tokens_dev", torch.int32, max(n, 1), self.device, optional=False)
+        _need(logits, "logits", torch.float32, int(self.shape.vocab), self.device)
+        _need(next_token_dev, "next_token_dev", torch.int32, 1, self.device, optional=False)
+        ll_prefill(self.handle, tokens_dev, n, pos0, logits, next_token_dev)
 
     def synchronize(self) -> None:
         ll_synchronize(self.handle)

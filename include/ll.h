@@ -141,6 +141,25 @@ int ll_decode_step_async(ll_handle *h, const int32_t *token_dev, int32_t pos, fl
 int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t n_steps, float *logits_dev,
                     int32_t *tokens_dev);
 
+/* Prefill: the n prompt tokens tokens_dev[0..n) (device int32) at positions
+ * pos0 .. pos0 + n - 1 through every layer at once, writing their K/V entries to
+ * the cache, then the last position's final RMSNorm, LM head and greedy token:
+ * logits_dev (device [vocab] fp32, or NULL) and next_token_dev (device int32).
+ * The same computation as n ll_decode_step calls at those positions (what the
+ * page's decode step computes, for many positions: the instruction list's
+ * projections become matrix products), here as tcgen05 GEMMs with TMA-staged
+ * bf16 operands and tensor-memory accumulators, the activations as two bf16
+ * terms, plus a causal attention over the cache entries 0..pos0 + t of each
+ * position t. Asynchronous on the handle's stream; a token out of range is
+ * reported by ll_synchronize (LL_ERR_ARG). Single-sequence handles only (LL_ERR_ARG
+ * on a batched one); needs hidden, n_q_heads*head_dim and inter multiples of 64
+ * (LL_ERR_SHAPE). The first call, and any call with more positions than before,
+ * allocates the prefill buffers (cudaMalloc, about n x (6 hidden + 3 q + 14
+ * inter) bytes plus the weight tensor maps; LL_ERR_OOM if that fails); ll_free
+ * releases them. */
+int ll_prefill(ll_handle *h, const int32_t *tokens_dev, int32_t n, int32_t pos0, float *logits_dev,
+               int32_t *next_token_dev);
+
 /* Small-batch decode: n_seq independent sequences (1, 2, 4 or 8) share every
  * pass over the weights. The page's method is batch 1; it says a batch turns the
  * matrix-vector products into skinny matrix products, where tensor cores pay

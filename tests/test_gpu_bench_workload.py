@@ -1,14 +1,15 @@
 """Parity on the workload bench.py times, as bench.py runs it: the Llama-3.2-1B
-shape, a 1024-token random prompt prefilled through the kernel one position at
-a time (chained single-step launches, each writing its K/V entry), then greedy
-steps in one ll_decode_steps launch.
+shape, a 1024-token random prompt through ll_prefill (tcgen05 GEMMs), then
+greedy steps in one ll_decode_steps launch; and the same prompt prefilled one
+position at a time by chained single-step launches (the chain-backend and
+fallback way), whose per-position logits are checked too.
 
 The oracle does not prefill 1024 positions in reasonable time, so:
-  * it recomputes the first 32 prefill positions on its own from an empty cache,
+  * it recomputes the first 32 prompt positions on its own from an empty cache,
     and each K/V entry the kernel wrote there must match its own;
-  * it recomputes 4 random later prefill positions p from the kernel's bf16
-    cache snapshot of positions 0..p-1: its K/V at p and logits at p against the
-    kernel's;
+  * it recomputes 4 random later positions p (and the last one) from the
+    kernel's bf16 cache snapshot of positions 0..p-1: its K/V at p, and for the
+    last position the logits, against the kernel's;
   * then, on the kernel's full 1024-position snapshot, every step of a 32-step
     greedy launch: logits element by element, and the token under the top-2
     margin rule (the oracle is fed the tokens the kernel chose, so both walk the
@@ -44,37 +45,47 @@ def _kv_entry_close(gpu_bits, orc_bits, what):
         assert np.max(np.abs(a[l] - b[l])) <= TOL_MAX * scale and rel <= TOL_L2, f"{what} layer {l}: rel {rel:.3e}"
 
 
-def test_prefilled_1b_ctx1024_then_greedy_launch():
+@pytest.mark.parametrize("how", ["ll_prefill", "single-step launches"])
+def test_prefilled_1b_ctx1024_then_greedy_launch(how):
     wl = synth.WORKLOADS["1b"]
     shape, ctx = wl.shape, wl.context
     n_dec = 32
     max_seq = ctx + n_dec + 1
     pr = Pair(shape, max_seq)
     rng = np.random.default_rng(4)
-    probe = sorted(int(p) for p in rng.choice(np.arange(64, ctx), size=4, replace=False))
+    probe = sorted(int(p) for p in rng.choice(np.arange(64, ctx - 1), size=4, replace=False)) + [ctx - 1]
     prompt = synth.make_tokens(shape.vocab, ctx, seed=1)
     prompt_dev = torch.tensor(prompt, dtype=torch.int32, device="cuda")
     logits = torch.empty((ctx, shape.vocab), dtype=torch.float32, device="cuda")
     nxt = torch.zeros(ctx, dtype=torch.int32, device="cuda")
-    # the prefill exactly as bench.py runs it: chained single-step launches
-    for pos in range(ctx):
-        pr.dec.step_async(prompt_dev[pos:pos + 1], pos, logits[pos], nxt[pos:pos + 1])
+    if how == "ll_prefill":  # as bench.py runs it: the prompt in one call
+        pr.dec.prefill(prompt_dev, 0, logits[ctx - 1], nxt[ctx - 1:ctx])
+        have = {ctx - 1}  # positions whose logits the call gives
+    else:
+        for pos in range(ctx):
+            pr.dec.step_async(prompt_dev[pos:pos + 1], pos, logits[pos], nxt[pos:pos + 1])
+        have = set(range(ctx))
     pr.dec.synchronize()
     k_snap, v_snap = synth.to_host_bits(pr.k), synth.to_host_bits(pr.v)
 
     # (1) the first 32 positions recomputed by the oracle from an empty cache
     for pos in range(32):
         ref, _ = pr.orc.decode_step(prompt[pos], pos)
-        compare_logits(logits[pos].cpu().numpy(), ref, f"prefill pos {pos}")
+        if pos in have:
+            compare_logits(logits[pos].cpu().numpy(), ref, f"prompt pos {pos}")
         _kv_entry_close(k_snap[:, :, pos], pr.orc.k_cache[:, :, pos], f"K pos {pos}")
         _kv_entry_close(v_snap[:, :, pos], pr.orc.v_cache[:, :, pos], f"V pos {pos}")
 
-    # (2) 4 random later positions from the kernel's snapshot of what precedes them
+    # (2) 4 random later positions and the last one, from the kernel's snapshot
+    # of what precedes them
     for pos in probe:
         pr.orc.k_cache[:, :, :pos] = k_snap[:, :, :pos]
         pr.orc.v_cache[:, :, :pos] = v_snap[:, :, :pos]
         ref, _ = pr.orc.decode_step(prompt[pos], pos)
-        compare_logits(logits[pos].cpu().numpy(), ref, f"prefill pos {pos}")
+        if pos in have:
+            compare_logits(logits[pos].cpu().numpy(), ref, f"prompt pos {pos}")
+            if pos == ctx - 1:
+                check_token(int(nxt[ctx - 1].item()), ref, "prompt's last position")
         _kv_entry_close(k_snap[:, :, pos], pr.orc.k_cache[:, :, pos], f"K pos {pos}")
         _kv_entry_close(v_snap[:, :, pos], pr.orc.v_cache[:, :, pos], f"V pos {pos}")
 
