@@ -37,7 +37,7 @@ def _inputs():
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
-    if os.environ.get("LL_DEBUG_CHECKS") == "1":
+    if os.environ.get("LL_DEBUG_CHECKS") == "1" or os.environ.get("LL_RING"):
         return True
     t = os.path.getmtime(LIB)
     return any(os.path.getmtime(f) > t for f in _inputs())
@@ -54,6 +54,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if os.environ.get("LL_DEBUG_CHECKS") == "1":
         # self-checking build: every hot-path index is bounds-checked on the device
         flags += ["-DLL_DEBUG_CHECKS"]
+    ring = os.environ.get("LL_RING")
+    if ring:
+        # another shared-memory ring geometry, for comparisons: "<pages>x<KB>", the
+        # 192 KB total kept (12x16 also cuts batches to 2 sequences for room)
+        pages, kb = (int(v) for v in ring.lower().split("x"))
+        flags += [f"-DLL_NPAGES={pages}", f"-DLL_PAGE_BYTES={kb * 1024}"]
+        if pages * kb != 192:
+            raise ValueError("LL_RING must keep 192 KB of pages")
+        if pages > 8:
+            flags += ["-DLL_MAX_B=2"]
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")

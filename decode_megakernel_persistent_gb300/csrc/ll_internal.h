@@ -17,8 +17,16 @@ namespace ll {
 constexpr int NCW = 16;
 constexpr int NCT = NCW * 32;              // consumer threads
 constexpr int NTHREADS = NCT + 32;         // + producer warp
-constexpr int PAGE_BYTES = 32768;
-constexpr int NPAGES = 6;
+// The ring geometry; another one can be built for comparison (LL_RING=12x16 or
+// 8x24 before build(): pages x KB), the total held at 192 KB.
+#ifndef LL_PAGE_BYTES
+#define LL_PAGE_BYTES 32768
+#endif
+#ifndef LL_NPAGES
+#define LL_NPAGES 6
+#endif
+constexpr int PAGE_BYTES = LL_PAGE_BYTES;
+constexpr int NPAGES = LL_NPAGES;
 constexpr int MAX_VPL = 4;                 // 16-byte input vectors per lane (register budget)
 constexpr int MAX_GQA = 8;                 // query heads per KV head
 constexpr int MAX_HD = 128;
@@ -30,7 +38,10 @@ constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden 
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
 constexpr int ATT_WARPS = 8;               // warps that split an attention page's P.V
 constexpr int TRACE_WORDS = 12;            // timestamps per traced instruction
-constexpr int MAX_B = 8;                   // sequences one batched handle decodes together
+#ifndef LL_MAX_B
+#define LL_MAX_B 8
+#endif
+constexpr int MAX_B = LL_MAX_B;            // sequences one batched handle decodes together
 constexpr int BACC_FLOATS = 1024;          // per-SM row results x sequences of a tensor-core instruction
 constexpr int PTRACE_PAGES = 4096;         // pages per SM the page trace keeps (a ring)
 

@@ -5,6 +5,9 @@
       `--metrics gpu__time_duration.sum --csv --log-file` run)
   python -m decode_megakernel_persistent_gb300.ncu_summary raw RAW.csv
       selected counters of one captured launch (from `ncu -i REP --page raw --csv`)
+  python -m decode_megakernel_persistent_gb300.ncu_summary metrics METRICS.csv
+      every launch of a `--metrics a,b,... --csv --log-file` run, one row per
+      launch, one column per metric
 """
 from __future__ import annotations
 
@@ -58,6 +61,26 @@ def launches(path: str) -> str:
     return "\n".join(out)
 
 
+def metrics(path: str) -> str:
+    rows = _rows(path)
+    hdr = rows[0]
+    ii, ki, mi, vi = hdr.index("ID"), hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    ui = hdr.index("Metric Unit")
+    per = collections.OrderedDict()
+    names = []
+    for r in rows[1:]:
+        if len(r) <= vi:
+            continue
+        key = (r[ii], r[ki].split("(")[0])
+        per.setdefault(key, {})[r[mi]] = f"{r[vi]} {r[ui]}".strip()
+        if r[mi] not in names:
+            names.append(r[mi])
+    out = ["| launch | kernel | " + " | ".join(names) + " |", "|---" * (len(names) + 2) + "|"]
+    for (i, k), d in per.items():
+        out.append(f"| {i} | {k} | " + " | ".join(d.get(n, "") for n in names) + " |")
+    return "\n".join(out)
+
+
 def raw(path: str) -> str:
     rows = _rows(path)
     hdr, units, vals = rows[0], rows[1], rows[2]
@@ -72,4 +95,4 @@ def raw(path: str) -> str:
 
 if __name__ == "__main__":
     kind, path = sys.argv[1], sys.argv[2]
-    print(launches(path) if kind == "launches" else raw(path))
+    print({"launches": launches, "raw": raw, "metrics": metrics}[kind](path))

@@ -131,6 +131,11 @@ def main():
                     help="a 2-layer hidden-1024 model whose weights (~90 MB) stay in L2")
     ap.add_argument("--batch", type=int, default=0,
                     help="trace a batched handle of this many sequences (ll_init_batch)")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="with --notrace: run ll_prefill of this many prompt tokens (twice) instead of decode "
+                         "steps (a target for external profilers)")
+    ap.add_argument("--backend", default="megakernel", choices=["megakernel", "chain"],
+                    help="with --notrace: the backend whose steps run")
     args = ap.parse_args()
     if args.load:
         d = np.load(args.load)
@@ -152,14 +157,26 @@ def main():
         kv = [synth.make_kv(shape, max_seq, ctx, seed=2 + b, device="cuda") for b in range(args.batch)]
         dec = ll.BatchDecoder(shape, w, [x[0] for x in kv], [x[1] for x in kv], max_seq)
     else:
-        k, v = synth.make_kv(shape, max_seq, ctx, seed=2, device="cuda")
-        dec = ll.Decoder(shape, w, k, v, max_seq)
+        if args.prefill:
+            max_seq = max(max_seq, args.prefill + 1)
+        k, v = synth.make_kv(shape, max_seq, ctx if not args.prefill else 0, seed=2, device="cuda")
+        dec = ll.Decoder(shape, w, k, v, max_seq,
+                         ll.LL_BACKEND_CHAIN if args.backend == "chain" else ll.LL_BACKEND_MEGAKERNEL)
     nbytes = dec.query(ll.LL_Q_TRACE_BYTES)
     buf = torch.zeros(nbytes // 8, dtype=torch.int64, device="cuda")
     if not args.notrace:
         ll.ll_set_trace(dec.handle, buf)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     tok = 1
+    if args.prefill and args.notrace:
+        prompt = torch.tensor(synth.make_tokens(shape.vocab, args.prefill, seed=1), dtype=torch.int32, device="cuda")
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            dec.prefill(prompt, 0, logits, nxt)
+        dec.synchronize()
+        print(json.dumps({"prefill": args.prefill, "workload": wl.name, "traced": False}))
+        dec.close()
+        return
     for i in range(args.steps):
         if args.batch:  # every sequence one step, one launch per step
             toks = torch.ones((1, args.batch), dtype=torch.int32, device="cuda")

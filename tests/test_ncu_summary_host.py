@@ -31,3 +31,17 @@ def test_raw_counters_in_fixed_order(tmp_path):
                  '"decode_megakernel","2.5","672.2","7"\n')
     out = ncu_summary.raw(str(p)).splitlines()
     assert out[2:] == ["| gpu__time_duration.sum | 672.2 | us |", "| dram__bytes_read.sum | 2.5 | Gbyte |"]
+
+
+def test_metrics_one_row_per_launch(tmp_path):
+    p = tmp_path / "m.csv"
+    p.write_text(HDR +
+                 row(0, "k_gemm<0>(GemmArgs)", "us", "10.5") +
+                 row(0, "k_gemm<0>(GemmArgs)", "%", "41.2", metric="sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active") +
+                 row(1, "k_gemm<1>(GemmArgs)", "us", "7.25") +
+                 row(1, "k_gemm<1>(GemmArgs)", "%", "38", metric="sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"))
+    out = ncu_summary.metrics(str(p)).splitlines()
+    assert out[0] == ("| launch | kernel | gpu__time_duration.sum | "
+                      "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active |")
+    assert out[2] == "| 0 | k_gemm<0> | 10.5 us | 41.2 % |"
+    assert out[3] == "| 1 | k_gemm<1> | 7.25 us | 38 % |"
