@@ -235,8 +235,7 @@ struct PrefillBufs {
     uint16_t *h[T] = {};                 // [n][H] normed input, as T bf16 terms
     float *qkv = nullptr;                // [n][qd + 2 kd]
     uint16_t *o[T] = {};                 // [n][qd] attention output, T terms
-    float *gate = nullptr;               // [n][I]
-    uint16_t *a[T] = {};                 // [n][I] silu(gate) * up, T terms
+    uint16_t *a[T] = {};                 // [n][I] silu(gate) * up, T terms (gate and up: one GEMM)
     float *hrow = nullptr, *logits = nullptr;       // [H], [V]: the last position's head
     TensorMap m_h[T], m_o[T], m_a[T];    // A operands (activations), boxes of 128 rows x 64 columns
     std::vector<TensorMap> m_w;          // B operands: [L][7] wq, wk, wv, wo, wg, wu, wd, boxes of 128 rows x 64

@@ -17,12 +17,12 @@
 // accumulate in the same tensor-memory tile: the GEMM runs its K loop three
 // times.
 //
-// Per layer: RMSNorm into the two terms; Q, K, V GEMMs; RoPE with the K/V
-// rounded to bf16 into the cache; causal attention over the cache (CUDA cores,
-// one warp per query position and head); O GEMM added into the residual;
-// RMSNorm; gate GEMM; up GEMM whose epilogue forms silu(gate) * up in two terms;
-// down GEMM added into the residual. Then the last position's final norm, LM
-// head and argmax.
+// Per layer: RMSNorm into the terms; Q, K, V GEMMs; RoPE with the K/V rounded
+// to bf16 into the cache; causal attention over the cache (mma.sync tiles, one
+// warp per query position and KV head); O GEMM added into the residual;
+// RMSNorm; one GEMM for gate and up (two tensor-memory accumulators) whose
+// epilogue forms silu(gate) * up in terms; down GEMM added into the residual.
+// Then the last position's final norm, LM head and argmax.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,7 +39,6 @@ namespace {
 constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 4, GTHREADS = 128;
 constexpr int NTERMS = 3;  // bf16 terms of an activation
 constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A and B alike)
-constexpr int GEMM_SMEM = GSTAGES * 2 * int(GTILE) + 1024;
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -105,27 +104,31 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const TensorMap *map, int x,
         : "memory");
 }
 
-enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU_MUL = 2 };
+enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_GATEUP = 2 };
 
 struct GemmArgs {
-    TensorMap a[NTERMS], b;   // A terms [rows][K] and B [N][K], bf16, K-major, boxes 64 x 128, 128-byte swizzle
-    int M, N, K;              // positions, outputs, inner width (K a multiple of 64)
-    float *c;                 // [M][ldc] fp32: EPI_STORE c = A B^T, EPI_ADD c += A B^T
+    TensorMap a[NTERMS], b, b2;  // A terms [rows][K]; B [N][K] (EPI_GATEUP: b the gate, b2 the up matrix); bf16,
+                                 // K-major, boxes 64 x 128, 128-byte swizzle
+    int M, N, K;                 // positions, outputs, inner width (K a multiple of 64)
+    float *c;                    // [M][ldc] fp32: EPI_STORE c = A B^T, EPI_ADD c += A B^T
     int ldc;
-    const float *gate;        // EPI_SILU_MUL: gate [M][ldc]; act = silu(gate) * (A B^T) as NTERMS bf16 terms
-    uint16_t *act[NTERMS];
+    uint16_t *act[NTERMS];       // EPI_GATEUP: silu(A Bg^T) * (A Bu^T) as NTERMS bf16 terms, [M][ldc]
     int32_t *status;
     uint64_t timeout_ns;
 };
 
-// One 128 x 128 tile of C per block: warp 0 lane 0 feeds the pipeline with TMA,
+// One 128 x 128 tile of C per block (EPI_GATEUP: the same tile of the gate and
+// the up products, two accumulators): warp 0 lane 0 feeds the pipeline with TMA,
 // warp 1 lane 0 issues the MMAs, all four warps run the epilogue (warp w owns
 // tensor-memory lanes, i.e. tile rows, 32 w .. 32 w + 31).
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
+    constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
+    constexpr uint32_t STAGE = GTILE * (1 + NB);
+    constexpr uint32_t TCOLS = 128 * NB;
     extern __shared__ __align__(1024) uint8_t gsm[];
     uint8_t *tiles = gsm;
-    uint64_t *full = reinterpret_cast<uint64_t *>(gsm + GSTAGES * 2 * GTILE);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gsm + GSTAGES * STAGE);
     uint64_t *empty = full + GSTAGES;
     uint64_t *done = empty + GSTAGES;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
@@ -142,9 +145,10 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *err = 0;
     }
-    if (warp == 0) {  // 128 fp32 columns of tensor memory: the 128 x 128 accumulator
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
-                         saddr(const_cast<uint32_t *>(tmem_slot)))
+    if (warp == 0) {  // fp32 columns of tensor memory: one 128 x 128 accumulator per B operand
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         saddr(const_cast<uint32_t *>(tmem_slot))),
+                     "n"(TCOLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -158,13 +162,13 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
         for (int it = 0; it < iters; it++) {
             const int s = it % GSTAGES;
             if (it >= GSTAGES && !mbar_wait(&empty[s], ((it / GSTAGES) - 1) & 1, g.timeout_ns, g.status, err)) break;
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[s])),
-                         "r"(2 * GTILE)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[s])), "r"(STAGE)
                          : "memory");
             const int kc = (it % nk) * GK;
-            const uint32_t a_dst = saddr(tiles + size_t(s) * 2 * GTILE);
+            const uint32_t a_dst = saddr(tiles + size_t(s) * STAGE);
             tma2d(a_dst, &g.a[it / nk], kc, m0, &full[s]);
             tma2d(a_dst + GTILE, &g.b, kc, n0, &full[s]);
+            if (NB == 2) tma2d(a_dst + 2 * GTILE, &g.b2, kc, n0, &full[s]);
             sent++;
         }
         // never leave with copies in flight into this block's shared memory (after
@@ -176,68 +180,99 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
         }
     } else if (warp == 1 && lane == 0) {
         constexpr uint32_t idesc = idesc_bf16(GM, GN);
-        int issued = 0;
         for (int it = 0; it < iters; it++) {
             const int s = it % GSTAGES;
             if (!mbar_wait(&full[s], (it / GSTAGES) & 1, g.timeout_ns, g.status, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a_addr = saddr(tiles + size_t(s) * 2 * GTILE);
-            const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(a_addr + GTILE);
+            const uint32_t a_addr = saddr(tiles + size_t(s) * STAGE);
+            const uint64_t ad = smem_desc_sw128(a_addr);
 #pragma unroll
-            for (int kk = 0; kk < GK / 16; kk++) {
-                const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-                    "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
-                    : "memory");
+            for (int nb = 0; nb < NB; nb++) {
+                const uint64_t bd = smem_desc_sw128(a_addr + GTILE * (1 + nb));
+#pragma unroll
+                for (int kk = 0; kk < GK / 16; kk++) {
+                    const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + uint32_t(128 * nb)),
+                        "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
+                        : "memory");
+                }
             }
             // the stage is free once these products have read it
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                              saddr(&empty[s]))
                          : "memory");
-            issued++;
         }
-        // the accumulator is complete once every product issued so far is
+        // the accumulators are complete once every product issued so far is
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(done))
                      : "memory");
-        (void)issued;
     }
     __syncwarp();
     const bool ok = mbar_wait(done, 0, g.timeout_ns, g.status, err) && !*err;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int row = m0 + warp * 32 + lane;
+    auto ld16 = [&](uint32_t col, uint32_t (&r)[16]) {
+        const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + col;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    };
     if (ok) {
 #pragma unroll 1
         for (int c0 = 0; c0 < GN; c0 += 16) {
             uint32_t r[16];
-            const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0);
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-                "%14, %15}, [%16];"
-                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (row >= g.M) continue;
+            ld16(uint32_t(c0), r);
+            uint32_t u[16];
+            if (EPI == EPI_GATEUP) ld16(uint32_t(128 + c0), u);
+            const int col0 = n0 + c0;
+            if (row >= g.M || col0 >= g.N) continue;
+            const size_t at = size_t(row) * g.ldc + col0;
+            const bool whole = col0 + 16 <= g.N;  // 16 columns at once (N is a multiple of 16 here)
+            if (EPI == EPI_STORE || EPI == EPI_ADD) {
+                float4 *cp = reinterpret_cast<float4 *>(g.c + at);
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int col = n0 + c0 + j;
-                if (col >= g.N) break;
-                const float y = __uint_as_float(r[j]);
-                const size_t at = size_t(row) * g.ldc + col;
-                if (EPI == EPI_STORE) {
-                    g.c[at] = y;
-                } else if (EPI == EPI_ADD) {
-                    g.c[at] += y;
-                } else {
-                    const float z = g.gate[at];
-                    float a = z / (1.0f + expf(-z)) * y;
+                for (int q = 0; q < 4; q++) {
+                    float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                           __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    if (!whole) break;
+                    if (EPI == EPI_ADD) {
+                        const float4 o = cp[q];
+                        v.x += o.x;
+                        v.y += o.y;
+                        v.z += o.z;
+                        v.w += o.w;
+                    }
+                    cp[q] = v;
+                }
+            } else {
+                uint32_t w[NTERMS][8];
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    float a2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const float z = __uint_as_float(r[j + e]);
+                        a2[e] = z / (1.0f + expf(-z)) * __uint_as_float(u[j + e]);
+                    }
 #pragma unroll
                     for (int q = 0; q < NTERMS; q++) {
-                        const __nv_bfloat16 tq = __float2bfloat16_rn(a);
-                        g.act[q][at] = __bfloat16_as_ushort(tq);
-                        a -= __bfloat162float(tq);
+                        const __nv_bfloat162 t2 = __floats2bfloat162_rn(a2[0], a2[1]);
+                        w[q][j / 2] = *reinterpret_cast<const uint32_t *>(&t2);
+                        a2[0] -= __low2float(t2);
+                        a2[1] -= __high2float(t2);
+                    }
+                }
+                if (whole) {
+#pragma unroll
+                    for (int q = 0; q < NTERMS; q++) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(g.act[q] + at);
+                        dst[0] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+                        dst[1] = make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]);
                     }
                 }
             }
@@ -245,7 +280,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TCOLS) : "memory");
 }
 
 // x[t] = E[tokens[t]] (fp32), tokens checked.
@@ -323,82 +358,178 @@ __global__ void k_pf_rope_kv(float *qkv, const float2 *rope, int pos0, int nq, i
     }
 }
 
-// Causal attention of the prompt's positions: one warp per (position t, query
-// head h) over cache entries 0..pos0 + t of KV head h / (nq / nkv). The warp's
-// four groups of eight lanes take positions j, j + 1, j + 2, j + 3; each lane
-// holds hd / 8 dimensions of q (scaled by 1/sqrt(hd)) and a running (m, l, o) of
-// its group, merged across the groups at the end. Output: o as NTERMS bf16 terms.
-template <int DPL>  // dimensions per lane: hd / 8
-__global__ void k_pf_attention(const float *qkv, const uint16_t *kc, const uint16_t *vc, size_t layer_base, int pos0,
-                               int n, int nq, int nkv, int max_seq, Terms o_t) {
-    constexpr int HD = DPL * 8;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= n * nq) return;
-    const int t = warp / nq, h = warp % nq, grp = lane >> 3, sub = lane & 7;
-    const int g = h / (nq / nkv), qd = nq * HD, kd = nkv * HD;
+// Tensor-core causal attention of the prompt's positions. Block (8 positions, KV
+// head g): warp w takes position t = 8 blockIdx.x + w and the G query heads of
+// KV head g as the rows of an m16n8k16 A operand, each head's q (scaled by
+// 1/sqrt(hd)) as two bf16 terms (hi in rows 0..7, lo in rows 8..15). The block
+// walks the cache entries 0..pos0 + t in tiles of 16 positions, loaded once for
+// its eight warps into shared memory as [K | V][64-dim half][position][64 dims]
+// with 128-byte rows whose 16-byte chunk c sits at c ^ (row % 8) (so ldmatrix
+// rows fall in different bank groups); the next tile's loads are in flight
+// while this one is used. Per tile: S = Q K^T (K rows by ldmatrix as B), the
+// running max and sum of each head over the 4 lanes holding it, P = exp(S - m)
+// as hi and lo bf16 rows (already the A operand of P V), O += P V (V by
+// ldmatrix.trans). Positions past t are masked. Output: o as NTERMS bf16 terms.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(256) k_pf_attn_tc(const float *qkv, const uint16_t *kc, const uint16_t *vc,
+                                                   size_t layer_base, int pos0, int n, int nq, int nkv, int max_seq,
+                                                   Terms o_t) {
+    constexpr int DH = HD / 64, KS = HD / 16, CPT = 4 * HD / 256;  // 64-dim halves, k-steps, 16-byte chunks per thread
+    __shared__ __align__(1024) uint8_t tile[2][DH][16][128];       // [K | V][half][position][128 bytes]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    const int g = blockIdx.y, G = nq / nkv, qd = nq * HD, kd = nkv * HD;
+    const int t = blockIdx.x * 8 + warp;
+    const int last = pos0 + min(t, n - 1);                          // this warp's last position
+    const int block_last = pos0 + min(blockIdx.x * 8 + 7, n - 1);  // the block's
     const float scale = 1.0f / sqrtf(float(HD));
-    float q[DPL], o[DPL];
-    const float *qr = qkv + size_t(t) * (qd + 2 * kd) + size_t(h) * HD + sub * DPL;
+    // q as A fragments: k-step ks, lane (gq, tq): head gq at dims 16 ks + 2tq, +1 (hi in x, lo in y) and +8, +9 (z, w)
+    uint4 qa[KS];
 #pragma unroll
-    for (int e = 0; e < DPL; e++) {
-        q[e] = qr[e] * scale;
-        o[e] = 0.f;
+    for (int ks = 0; ks < KS; ks++) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (gq < G && t < n) {
+            const float *qr = qkv + size_t(t) * (qd + 2 * kd) + size_t(g * G + gq) * HD + 16 * ks + 2 * tq;
+            v[0] = qr[0] * scale;
+            v[1] = qr[1] * scale;
+            v[2] = qr[8] * scale;
+            v[3] = qr[9] * scale;
+        }
+        const uint32_t h01 = pack_bf16(v[0], v[1]), h89 = pack_bf16(v[2], v[3]);
+        const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
+        const __nv_bfloat162 b89 = *reinterpret_cast<const __nv_bfloat162 *>(&h89);
+        qa[ks] = make_uint4(h01, pack_bf16(v[0] - __low2float(b01), v[1] - __high2float(b01)), h89,
+                            pack_bf16(v[2] - __low2float(b89), v[3] - __high2float(b89)));
     }
-    float m = -INFINITY, l = 0.f;
-    const uint16_t *K = kc + layer_base + size_t(g) * max_seq * HD + sub * DPL;
-    const uint16_t *Vv = vc + layer_base + size_t(g) * max_seq * HD + sub * DPL;
-    const int last = pos0 + t;
-    for (int j0 = 0; j0 <= last; j0 += 4) {
-        const int j = j0 + grp;
-        float s = -INFINITY;
-        float v[DPL];
-        if (j <= last) {
-            float acc = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, o[HD / 8][2];
 #pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-                const uint32_t kw = *reinterpret_cast<const uint32_t *>(K + size_t(j) * HD + e);
-                acc = fmaf(q[e], __uint_as_float(kw << 16), acc);
-                acc = fmaf(q[e + 1], __uint_as_float(kw & 0xffff0000u), acc);
-                const uint32_t vw = *reinterpret_cast<const uint32_t *>(Vv + size_t(j) * HD + e);
-                v[e] = __uint_as_float(vw << 16);
-                v[e + 1] = __uint_as_float(vw & 0xffff0000u);
+    for (int d = 0; d < HD / 8; d++) o[d][0] = o[d][1] = 0.f;
+    const uint16_t *kbase = kc + layer_base + size_t(g) * max_seq * HD;
+    const uint16_t *vbase = vc + layer_base + size_t(g) * max_seq * HD;
+    // this thread's 16-byte chunks of a tile: (K or V, position, chunk of the row)
+    auto fetch = [&](int j0, uint4 (&buf)[CPT]) {
+#pragma unroll
+        for (int u = 0; u < CPT; u++) {
+            const int i = tid + u * 256, kv = i / (16 * HD / 8), rem = i % (16 * HD / 8);
+            const int pos = rem / (HD / 8), c = rem % (HD / 8);
+            const int j = j0 + pos;
+            buf[u] = j <= block_last
+                         ? *reinterpret_cast<const uint4 *>((kv ? vbase : kbase) + size_t(j) * HD + c * 8)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    uint4 nxt[CPT];
+    fetch(0, nxt);
+    for (int j0 = 0; j0 <= block_last; j0 += 16) {
+        __syncthreads();  // the previous tile is used up
+#pragma unroll
+        for (int u = 0; u < CPT; u++) {
+            const int i = tid + u * 256, kv = i / (16 * HD / 8), rem = i % (16 * HD / 8);
+            const int pos = rem / (HD / 8), c = rem % (HD / 8), h = c / 8, cc = c % 8;
+            *reinterpret_cast<uint4 *>(&tile[kv][h][pos][(cc ^ (pos & 7)) * 16]) = nxt[u];
+        }
+        __syncthreads();
+        if (j0 + 16 <= block_last) fetch(j0 + 16, nxt);  // in flight during this tile
+        if (j0 > last) continue;
+        // S = Q K^T: c[nb] holds positions j0 + 8 nb .. + 7
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int jk = 8 * (mi >> 1) + r8;  // this lane's ldmatrix row: position in the tile
+#pragma unroll
+            for (int ks = 0; ks < KS; ks++) {
+                const uint32_t ch = uint32_t(2 * (ks & 3) + (mi & 1));
+                uint32_t b[4];
+                ldsm4(saddr(&tile[0][ks >> 2][jk][(ch ^ uint32_t(jk & 7)) * 16]), b);
+                mma16816(c[0], qa[ks], b[0], b[1]);
+                mma16816(c[1], qa[ks], b[2], b[3]);
             }
-            s = acc;
-        } else {
-#pragma unroll
-            for (int e = 0; e < DPL; e++) v[e] = 0.f;
         }
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 4);
-        if (j <= last) {
-            const float mn = fmaxf(m, s);
-            const float a = m == -INFINITY ? 0.f : expf(m - mn), pj = expf(s - mn);
-            l = l * a + pj;
+        float sc[4];
 #pragma unroll
-            for (int e = 0; e < DPL; e++) o[e] = fmaf(pj, v[e], o[e] * a);
-            m = mn;
+        for (int nb = 0; nb < 2; nb++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int j = j0 + 8 * nb + 2 * tq + e;
+                sc[2 * nb + e] = j <= last ? c[nb][e] + c[nb][e + 2] : -INFINITY;
+            }
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        const float m_new = fmaxf(m_run, mt);  // finite: position j0 <= last exists
+        const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
+        float pr[4], ps = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
+            ps += pr[e];
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l_run = l_run * alpha + ps;
+        m_run = m_new;
+        const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
+        const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
+        const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162 *>(&h23);
+        const uint4 pa = make_uint4(h01, pack_bf16(pr[0] - __low2float(b01), pr[1] - __high2float(b01)), h23,
+                                    pack_bf16(pr[2] - __low2float(b23), pr[3] - __high2float(b23)));
+        // O += P V: 8 dims per product, two per ldmatrix
+        const int jv = 8 * (mi & 1) + r8;
+#pragma unroll
+        for (int dd = 0; dd < HD / 16; dd++) {
+            const uint32_t ch = uint32_t(2 * (dd & 3) + (mi >> 1));
+            uint32_t b[4];
+            ldsm4t(saddr(&tile[1][dd >> 2][jv][(ch ^ uint32_t(jv & 7)) * 16]), b);
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int d = 2 * dd + u;
+                float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
+                mma16816(acc, pa, b[2 * u], b[2 * u + 1]);
+                o[d][0] = acc[0] + acc[2];
+                o[d][1] = acc[1] + acc[3];
+            }
         }
     }
-    // merge the four groups (lanes sub, sub + 8, sub + 16, sub + 24)
+    if (t >= n || gq >= G) return;
+    // lane (gq, tq) holds head gq at dims 8 d + 2 tq, + 1
+    const size_t at = size_t(t) * qd + size_t(g * G + gq) * HD;
+    const float inv = 1.0f / l_run;
 #pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, off), lo = __shfl_xor_sync(0xffffffffu, l, off);
-        const float M = fmaxf(m, mo);
-        const float wa = m == -INFINITY ? 0.f : expf(m - M), wb = mo == -INFINITY ? 0.f : expf(mo - M);
-#pragma unroll
-        for (int e = 0; e < DPL; e++) {
-            const float oo = __shfl_xor_sync(0xffffffffu, o[e], off);
-            o[e] = o[e] * wa + oo * wb;
-        }
-        l = l * wa + lo * wb;
-        m = M;
+    for (int d = 0; d < HD / 8; d++) {
+        put_terms(o[d][0] * inv, o_t.t, at + 8 * d + 2 * tq);
+        put_terms(o[d][1] * inv, o_t.t, at + 8 * d + 2 * tq + 1);
     }
-    if (grp == 0) {
-        const size_t at = size_t(t) * qd + size_t(h) * HD + sub * DPL;
-#pragma unroll
-        for (int e = 0; e < DPL; e++) put_terms(o[e] / l, o_t.t, at + e);
-    }
+}
+
+int launch_attention(const KParams &p, const PrefillBufs &b, size_t lb, int pos0, int n, const Terms &to,
+                     cudaStream_t st) {
+    const dim3 grid((n + 7) / 8, p.nkv);
+    if (p.hd == 64)
+        k_pf_attn_tc<64><<<grid, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
+    else
+        k_pf_attn_tc<128><<<grid, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
+    return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -438,30 +569,32 @@ bool encode_operand(const uint16_t *base, int64_t rows, int K, TensorMap &out) {
 }
 
 template <int EPI>
-int gemm(const TensorMap *a, const TensorMap &b, int M, int N, int K, float *c, int ldc, const float *gate,
+int gemm(const TensorMap *a, const TensorMap &b, const TensorMap *b2, int M, int N, int K, float *c, int ldc,
          const Terms *act, const KParams &p, cudaStream_t st) {
+    constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;
+    constexpr int SMEM = GSTAGES * int(GTILE) * (1 + NB) + 1024;
     GemmArgs g;
     for (int q = 0; q < NTERMS; q++) {
         g.a[q] = a[q];
         g.act[q] = act ? act->t[q] : nullptr;
     }
     g.b = b;
+    g.b2 = b2 ? *b2 : b;
     g.M = M;
     g.N = N;
     g.K = K;
     g.c = c;
     g.ldc = ldc;
-    g.gate = gate;
     g.status = p.status;
     g.timeout_ns = p.timeout_ns;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(k_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) != cudaSuccess)
+        if (cudaFuncSetAttribute(k_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
             return LL_ERR_CUDA;
         attr = true;
     }
     const dim3 grid((N + GN - 1) / GN, (M + GM - 1) / GM);
-    k_gemm<EPI><<<grid, GTHREADS, GEMM_SMEM, st>>>(g);
+    k_gemm<EPI><<<grid, GTHREADS, SMEM, st>>>(g);
     return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
@@ -475,9 +608,9 @@ bool prefill_prepare(const KParams &p, const LayerW *host_layers, int n, Prefill
     const size_t H = p.H, qd = size_t(p.nq) * p.hd, kd = size_t(p.nkv) * p.hd, I = p.I;
     auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t sz_x = r256(na * H * 4), sz_h = r256(na * H * 2), sz_qkv = r256(na * (qd + 2 * kd) * 4),
-                 sz_o = r256(na * qd * 2), sz_g = r256(na * I * 4), sz_a = r256(na * I * 2), sz_hr = r256(H * 4),
+                 sz_o = r256(na * qd * 2), sz_a = r256(na * I * 2), sz_hr = r256(H * 4),
                  sz_l = r256(size_t(p.V) * 4);
-    const size_t total = sz_x + NTERMS * sz_h + sz_qkv + NTERMS * sz_o + sz_g + NTERMS * sz_a + sz_hr + sz_l;
+    const size_t total = sz_x + NTERMS * sz_h + sz_qkv + NTERMS * sz_o + NTERMS * sz_a + sz_hr + sz_l;
     if (cudaMalloc(&b.mem, total) != cudaSuccess) {
         cudaGetLastError();
         b.mem = nullptr;
@@ -497,7 +630,6 @@ bool prefill_prepare(const KParams &p, const LayerW *host_layers, int n, Prefill
     for (int q = 0; q < NTERMS; q++) b.h[q] = reinterpret_cast<uint16_t *>(take(sz_h));
     b.qkv = reinterpret_cast<float *>(take(sz_qkv));
     for (int q = 0; q < NTERMS; q++) b.o[q] = reinterpret_cast<uint16_t *>(take(sz_o));
-    b.gate = reinterpret_cast<float *>(take(sz_g));
     for (int q = 0; q < NTERMS; q++) b.a[q] = reinterpret_cast<uint16_t *>(take(sz_a));
     b.hrow = reinterpret_cast<float *>(take(sz_hr));
     b.logits = reinterpret_cast<float *>(take(sz_l));
@@ -543,22 +675,18 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         const size_t lb = size_t(l) * per_layer;
         const int ld = qd + 2 * kd;
         k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.attn_norm, H, p.eps, th);
-        rc = gemm<EPI_STORE>(b.m_h, m[0], n, qd, H, b.qkv, ld, nullptr, nullptr, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[1], n, kd, H, b.qkv + qd, ld, nullptr, nullptr, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[2], n, kd, H, b.qkv + qd + kd, ld, nullptr, nullptr, p, st);
+        rc = gemm<EPI_STORE>(b.m_h, m[0], nullptr, n, qd, H, b.qkv, ld, nullptr, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[1], nullptr, n, kd, H, b.qkv + qd, ld, nullptr, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[2], nullptr, n, kd, H, b.qkv + qd + kd, ld, nullptr, p, st);
         if (rc != LL_OK) break;
         k_pf_rope_kv<<<n, 256, 0, st>>>(b.qkv, p.rope_cs, pos0, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
-        const int blocks = (n * p.nq * 32 + 255) / 256;
-        if (p.hd == 64)
-            k_pf_attention<8><<<blocks, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
-        else
-            k_pf_attention<16><<<blocks, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
-        rc = gemm<EPI_ADD>(b.m_o, m[3], n, H, qd, b.x, H, nullptr, nullptr, p, st);
+        rc = launch_attention(p, b, lb, pos0, n, to, st);
+        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m[3], nullptr, n, H, qd, b.x, H, nullptr, p, st);
         if (rc != LL_OK) break;
         k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
-        rc = gemm<EPI_STORE>(b.m_h, m[4], n, I, H, b.gate, I, nullptr, nullptr, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_SILU_MUL>(b.m_h, m[5], n, I, H, nullptr, I, b.gate, &ta, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m[6], n, H, I, b.x, H, nullptr, nullptr, p, st);
+        // gate and up in one GEMM (two accumulators), silu(gate) * up as terms
+        rc = gemm<EPI_GATEUP>(b.m_h, m[4], &m[5], n, I, H, nullptr, I, &ta, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m[6], nullptr, n, H, I, b.x, H, nullptr, p, st);
     }
     if (rc != LL_OK) return rc;
     if (cudaGetLastError() != cudaSuccess) return LL_ERR_CUDA;

@@ -148,15 +148,15 @@ int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t
  * The same computation as n ll_decode_step calls at those positions (what the
  * page's decode step computes, for many positions: the instruction list's
  * projections become matrix products), here as tcgen05 GEMMs with TMA-staged
- * bf16 operands and tensor-memory accumulators, the activations as two bf16
- * terms, plus a causal attention over the cache entries 0..pos0 + t of each
- * position t. Asynchronous on the handle's stream; a token out of range is
+ * bf16 operands and tensor-memory accumulators, the activations as three
+ * bf16 terms, plus a causal attention (mma.sync tiles) over the cache entries
+ * 0..pos0 + t of each position t. Asynchronous on the handle's stream; a token out of range is
  * reported by ll_synchronize (LL_ERR_ARG). Single-sequence handles only (LL_ERR_ARG
  * on a batched one); needs hidden, n_q_heads*head_dim and inter multiples of 64
  * (LL_ERR_SHAPE). The first call, and any call with more positions than before,
- * allocates the prefill buffers (cudaMalloc, about n x (6 hidden + 3 q + 14
- * inter) bytes plus the weight tensor maps; LL_ERR_OOM if that fails); ll_free
- * releases them. */
+ * allocates the prefill buffers (cudaMalloc, about n x (10 hidden + 10 q + 8 kv
+ * + 6 inter) bytes plus the weight tensor maps; LL_ERR_OOM if that fails);
+ * ll_free releases them. */
 int ll_prefill(ll_handle *h, const int32_t *tokens_dev, int32_t n, int32_t pos0, float *logits_dev,
                int32_t *next_token_dev);
 
