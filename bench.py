@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "µs/token & tokens/s, batch-1 Llama-3.2-1B-shape decode; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 SPEC_HBM_GBS = 8000.0
 
 
@@ -68,6 +69,16 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Measured dense bf16 GEMM rate (TFLOP/s, burst), else the fallback figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def _code_only(text: str) -> str:
     """C/C++/CUDA source without its comments and blank space (no string literal
     of these sources contains a comment marker)."""
@@ -76,12 +87,24 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_sha() -> str:
-    """Hash of the library's code (comments and layout excluded), which ties
-    recorded ncu counters to the code they were taken on."""
+# Sources that do not go into a backend's decode kernels (so changing them leaves
+# that backend's recorded counters valid).
+NOT_IN_BACKEND = {
+    "megakernel": {"chain.cu", "prefill.cu", "static_step.cu"},
+    "chain": {"megakernel.cuh", "mk_cuda_cores.cu", "mk_tensor_cores.cu", "prefill.cu", "static_step.cu"},
+}
+
+
+def kernel_sha(backend: str = "megakernel") -> str:
+    """Hash of the code a backend's decode step is built from (comments and
+    layout excluded), which ties recorded ncu counters to the code they were
+    taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_megakernel_persistent_gb300", "csrc")
+    skip = NOT_IN_BACKEND.get(backend, set())
     for name in sorted(os.listdir(csrc)):
+        if name in skip:
+            continue
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -96,7 +119,7 @@ def recorded_traffic(workload_name: str, backend: str):
             rec = json.load(f).get(f"{backend}:{workload_name}")
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_sha") != kernel_sha():
+    if not rec or rec.get("kernel_sha") != kernel_sha(backend):
         return None
     return rec.get("bytes_per_launch")
 
@@ -270,13 +293,14 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------------
 
-def batch_lines(shape, w, ctx, dev, K):
+def batch_lines(shape, w, ctx, dev, K, peak):
     """Decode throughput of batched handles (2, 4, 8 sequences) at context ctx on
     seeded N(0,1) caches: one ll_decode_steps_batch launch of K steps, timed with
-    CUDA events after a warm-up launch."""
+    CUDA events after a warm-up launch; achieved GB/s from the algorithmic bytes
+    of the K steps (weights once per step, each sequence's K/V)."""
     import torch
 
-    from decode_megakernel_persistent_gb300 import ll, synth
+    from decode_megakernel_persistent_gb300 import bytemodel, ll, synth
     out = {}
     for n in (2, 4, 8):
         max_seq = ctx + K + 8
@@ -295,7 +319,9 @@ def batch_lines(shape, w, ctx, dev, K):
         torch.cuda.synchronize(dev)
         dec.synchronize()
         secs = e0.elapsed_time(e1) / 1e3
+        nbytes = sum(bytemodel.batch_step_bytes(shape, ctx + 4 + i, n) for i in range(K))
         out[str(n)] = {"tokens_per_s": n * K / secs, "us_per_step": 1e6 * secs / K,
+                       "achieved_gbs": nbytes / secs / 1e9, "frac": nbytes / secs / 1e9 / peak,
                        "kv_splits": dec.query(ll.LL_Q_ATTN_SPLITS)}
         dec.close()
         del kv
@@ -343,9 +369,12 @@ def run_ours(args):
                 torch.cuda.synchronize(dev)
                 secs = p0.elapsed_time(p1) / 1e3
                 flops = 2.0 * ctx * bytemodel.layer_weight_elements(shape)
+                tpeak, tpeak_kind = bf16_peak()
                 prefill = {"tokens": ctx, "ms": 1e3 * secs, "tokens_per_s": ctx / secs,
                            "tflops_algorithmic": flops / secs / 1e12,
                            "tflops_tensor": 3 * flops / secs / 1e12,
+                           "tensor_peak": tpeak, "tensor_peak_kind": tpeak_kind,
+                           "tensor_frac": 3 * flops / secs / 1e12 / tpeak,
                            "call": "ll_prefill: every projection a tcgen05 GEMM, activations as 3 bf16 terms"}
             else:
                 for pos in range(ctx):
@@ -437,7 +466,7 @@ def run_ours(args):
                                           f"{ctx}..{ctx + n1 - 1}, {secs1:.1f} s"}
     batch = None
     if not args.no_batch and backend == ll.LL_BACKEND_MEGAKERNEL and shape.hidden % 1024 == 0:
-        batch = batch_lines(shape, w, ctx, dev, K)
+        batch = batch_lines(shape, w, ctx, dev, K, peak)
     line = {
         "metric": METRIC,
         "value": world * K / t_dev,

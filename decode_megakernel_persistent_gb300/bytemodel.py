@@ -29,6 +29,13 @@ def step_bytes(shape: ModelShape, pos: int, logits: bool = True) -> int:
     return weight_bytes(shape) + kv_bytes(shape, pos) + (4 * shape.vocab if logits else 0)
 
 
+def batch_step_bytes(shape: ModelShape, pos: int, n: int, logits: bool = False) -> int:
+    """One step of n sequences at ``pos`` sharing a pass over the weights: the
+    weights once, and per sequence its K/V, its embedding row and its logits."""
+    per_seq = kv_bytes(shape, pos) + 2 * shape.hidden + (4 * shape.vocab if logits else 0)
+    return weight_bytes(shape) - 2 * shape.hidden + n * per_seq
+
+
 def step_flops(shape: ModelShape, pos: int) -> int:
     """2 flops per weight element of the matrices plus 4*hd per (query head, position)."""
     mats = shape.n_layers * sum(_numel(s) for k, s in shape.layer_shapes().items()

@@ -37,6 +37,27 @@ def test_recorded_traffic_is_tied_to_the_code(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w", "chain") is None
 
 
+def test_kernel_sha_covers_the_backends_own_sources(tmp_path, monkeypatch):
+    # a tree of stand-in sources: the megakernel's hash moves with the megakernel's
+    # files and the shared runtime, not with the prefill or chain files
+    csrc = tmp_path / "decode_megakernel_persistent_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("megakernel.cuh", "chain.cu", "prefill.cu", "api.cpp"):
+        (csrc / name).write_text(f"int {name.split('.')[0]};")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    mk, ch = bench.kernel_sha("megakernel"), bench.kernel_sha("chain")
+    (csrc / "prefill.cu").write_text("int changed;")
+    assert (bench.kernel_sha("megakernel"), bench.kernel_sha("chain")) == (mk, ch)
+    (csrc / "chain.cu").write_text("int changed;")
+    assert bench.kernel_sha("megakernel") == mk and bench.kernel_sha("chain") != ch
+    ch = bench.kernel_sha("chain")
+    (csrc / "megakernel.cuh").write_text("int changed;")
+    assert bench.kernel_sha("megakernel") != mk and bench.kernel_sha("chain") == ch
+    mk = bench.kernel_sha("megakernel")
+    (csrc / "api.cpp").write_text("int changed;")
+    assert bench.kernel_sha("megakernel") != mk and bench.kernel_sha("chain") != ch
+
+
 def test_clock_summary_reads_samples_inside_the_timed_region(monkeypatch):
     # no nvidia-smi here: the sampler still records marks and parses what its
     # output file holds; samples outside the marks are ignored, "Not Active"

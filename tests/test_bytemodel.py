@@ -50,3 +50,15 @@ def test_step_flops_two_per_matrix_weight():
     mats = L * (q * h + 2 * kv * h + h * q + 3 * inter * h) + V * h
     attn = 4 * L * 32 * 64 * (1100 + 1)
     assert bytemodel.step_flops(synth.LLAMA_1B, 1100) == 2 * mats + attn
+
+
+def test_batch_step_bytes_weights_once_kv_per_sequence():
+    # n sequences: the weights (less the one embedding row) once, then each
+    # sequence's K/V at pos 1100 and its own embedding row
+    weights_wo_row = 2_471_632_896 - 2 * 2048
+    for n in (1, 2, 8):
+        want = weights_wo_row + n * (32_768 * 1101 + 2 * 2048)
+        assert bytemodel.batch_step_bytes(synth.LLAMA_1B, 1100, n) == want
+    assert bytemodel.batch_step_bytes(synth.LLAMA_1B, 1100, 1) == bytemodel.step_bytes(synth.LLAMA_1B, 1100, logits=False)
+    assert (bytemodel.batch_step_bytes(synth.LLAMA_1B, 1100, 4, logits=True)
+            - bytemodel.batch_step_bytes(synth.LLAMA_1B, 1100, 4)) == 4 * 4 * 128256
