@@ -165,8 +165,17 @@ void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::v
 
 // The tensor-core kernel holds at most BACC_FLOATS (row, sequence) results per
 // instruction, so it takes an SM's vocabulary rows in pieces of this many rows.
+// The CUDA-core kernel keeps the (row, k-slice) partial sums of an instruction,
+// at most KPART_FLOATS of them, so its LM-head pieces are cut to fit as well
+// (whole pages of the hidden-width geometry).
+int lm_rows_cuda(const ll::MvShape &mh) {
+    const int rows = ll::KPART_FLOATS / std::max(1, mh.ws);
+    return std::max(mh.rpp, rows / std::max(1, mh.rpp) * mh.rpp);
+}
+
 int lm_rows_of(const ll_handle *h) {
-    return h->kp.mv_h.tc ? std::max(ll::TC_ROWS, ll::BACC_FLOATS / h->nb / ll::TC_ROWS * ll::TC_ROWS) : (1 << 30);
+    return h->kp.mv_h.tc ? std::max(ll::TC_ROWS, ll::BACC_FLOATS / h->nb / ll::TC_ROWS * ll::TC_ROWS)
+                         : lm_rows_cuda(h->kp.mv_h);
 }
 
 void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists, h->nb, lm_rows_of(h)); }
@@ -344,7 +353,9 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
     auto per_sm = [&](int64_t rows) { return (rows + h->nsm - 1) / h->nsm; };
     const int64_t qkv_rows = int64_t(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     if (per_sm(qkv_rows) > ll::ACC_FLOATS || 2 * per_sm(c.inter) > ll::ACC_FLOATS ||
-        per_sm(c.hidden) > ll::XOWN_MAX || per_sm(c.vocab) > ll::ACC_FLOATS) {
+        per_sm(c.hidden) > ll::XOWN_MAX || per_sm(c.vocab) > ll::ACC_FLOATS ||
+        per_sm(qkv_rows) * mh.ws > ll::KPART_FLOATS || 2 * per_sm(c.inter) * mh.ws > ll::KPART_FLOATS ||
+        per_sm(c.hidden) * std::max(mq.ws, mi.ws) > ll::KPART_FLOATS) {
         delete h;
         return bad(LL_ERR_SHAPE, "a projection has more rows per SM than the kernel holds");
     }
@@ -567,6 +578,8 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
     if (const char *e = std::getenv("LL_MAX_INFLIGHT")) p.max_inflight = static_cast<uint32_t>(std::atoi(e));
     p.producer_sleep_ns = 64;
     if (const char *e = std::getenv("LL_PRODUCER_SLEEP_NS")) p.producer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
+    p.consumer_sleep_ns = 0;
+    if (const char *e = std::getenv("LL_CONSUMER_SLEEP_NS")) p.consumer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
     h->d_instrs = d_instrs;
 
     ll::ChainBufs &cb = h->cb;
@@ -807,7 +820,9 @@ int ll_plan(const ll_config *cfg, int32_t nsm, int32_t *out, size_t out_len, int
     if (!cfg || nsm <= 0 || cfg->n_layers < 1 || cfg->n_kv_heads <= 0 || cfg->n_q_heads % cfg->n_kv_heads != 0)
         return LL_ERR_ARG;
     std::vector<std::vector<Instr>> lists;
-    build_lists_for(*cfg, nsm, attn_splits(*cfg, nsm), lists);
+    ll::MvShape mh{};
+    if (!ll::mv_shape(cfg->hidden, mh, 32)) return LL_ERR_SHAPE;
+    build_lists_for(*cfg, nsm, attn_splits(*cfg, nsm), lists, 1, lm_rows_cuda(mh));
     return dump_lists(lists, out, out_len, max_instr);
 }
 

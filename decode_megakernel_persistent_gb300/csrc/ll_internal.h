@@ -34,6 +34,7 @@ constexpr int MAX_RPP = 64;                // rows per page (hidden 256 at one v
 constexpr int MAX_PART = 128;              // (row, k-slice) partial sums per page
 constexpr int ACC_FLOATS = 2048;           // per-SM row results held until the instruction ends
 constexpr int XIN_FLOATS = 4096;           // largest O-projection input (n_q_heads * head_dim)
+constexpr int KPART_FLOATS = XIN_FLOATS - ACC_FLOATS;  // (row, k-slice) partial sums of one instruction
 constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden / SMs, rounded up)
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
 constexpr int ATT_WARPS = 8;               // warps that split an attention page's P.V
@@ -189,6 +190,7 @@ struct KParams {
     uint32_t l2_prefetch;     // pages the producer may prefetch into L2 beyond its ring
     uint32_t evict_first;     // weight pages loaded with an L2 evict-first hint
     uint32_t producer_sleep_ns; // back-off of the producer while the ring is full
+    uint32_t consumer_sleep_ns; // back-off of a consumer warp whose page is not issued yet
     uint32_t max_inflight;    // pages issued but not yet landed, at most (NPAGES: only the ring bounds it)
     // optional globaltimer trace, [nsm][max_instr][TRACE_WORDS]: consumer begin,
     // dependency met + input loaded, pages done, end; producer first and last issue;

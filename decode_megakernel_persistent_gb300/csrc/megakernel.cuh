@@ -55,8 +55,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
@@ -192,7 +192,10 @@ struct alignas(16) Smem {
     union {
         float xin[XIN_FLOATS];  // O-projection input: the merged attention output; also the
                                 // attention P.V partials of the P.V warps
-        float acc[ACC_FLOATS];  // the SM's row results of the current matrix-vector instruction
+        struct {
+            float acc[ACC_FLOATS];      // the SM's row results of the current matrix-vector instruction
+            float kpart[KPART_FLOATS];  // its (row, k-slice) partial sums, [row][k-slice]
+        };
         struct {                                // attention, block-wide softmax per page:
             float ared_lo[ATT_WARPS * 4 * 64];  // P.V partials of four heads of 64 dims
             float sc[MAX_GQA][132];             // scores of up to 129 positions
@@ -202,10 +205,9 @@ struct alignas(16) Smem {
         float ared[NCW / 2][AT_SLOT];        // attention, per-warp softmax: (o, m, l) of warps being merged
     };
     uint64_t full[NPAGES];   // page filled (tx bytes landed)
-    uint64_t empty[NPAGES];  // page released by the consumers
+    uint64_t empty[NPAGES];  // page released by the consumers: NCW arrivals in all per page
     int32_t pcnt[NPAGES];    // warps done with the page in the slot
     volatile uint32_t slot_page[NPAGES];  // page number the producer last put in the slot
-    float part[NPAGES][MAX_PART];  // per page: (row, k-slice) partial sums
     float qr[MAX_GQA][MAX_HD];  // the attention item's rotated, scaled query heads
     alignas(16) uint16_t knew[MAX_HD];
     alignas(16) uint16_t vnew[MAX_HD];
@@ -299,6 +301,8 @@ __device__ bool wait_page(const KParams &p, Smem &s, uint32_t page) {
     if (s.slot_page[slot] != page) {
         const uint64_t t0 = gtimer();
         for (uint32_t it = 1; s.slot_page[slot] != page; ++it) {
+            // back off, so that the warps working on landed pages keep the issue slots
+            if (p.consumer_sleep_ns) __nanosleep(p.consumer_sleep_ns);
             if ((it & 15u) == 0) {
                 if (s.abort) return false;
                 if (gtimer() - t0 > p.timeout_ns) {
@@ -695,6 +699,9 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     const int W = NCW / mv.teams, team = warp / W, wt = warp % W;
     const int active = mv.ws * mv.rg;  // working warps per team
     const int sw = wt % mv.ws, rgi = wt / mv.ws;
+    // a page is released by the NCW arrivals its team's active warps make in all
+    const uint32_t my_arrivals = uint32_t(wt == 0 ? NCW - (active - 1) * (NCW / active) : NCW / active);
+    int ntot = 0;  // rows of s.acc this instruction fills
     const uint32_t row_bytes = uint32_t(mv.K) * 2;
     const int nrows = ins.r1 - ins.r0;
     constexpr int GROUP = 32 / RW;  // lanes that end up holding one row's sum
@@ -705,11 +712,12 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
         const Seg sg = seg[si];
         // where the segment's rows land in s.acc
         const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
+        ntot = max(ntot, acc0 + sg.nrows);
         for (int pr = 0; pr < sg.nrows; pr += mv.rpp) {
             const int nr = min(mv.rpp, sg.nrows - pr);
             const uint32_t slot = cpage % NPAGES;
             const uint32_t this_page = cpage++;
-            if (int(this_page % uint32_t(mv.teams)) != team || wt >= active) continue;
+            if (int(this_page & uint32_t(mv.teams - 1)) != team || wt >= active) continue;
             if (bad || !wait_page(p, s, this_page)) {
                 bad = true;
                 continue;
@@ -755,35 +763,28 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
                 }
             }
             const float sum = transpose_reduce<RW>(v);
-            const int q = lane / GROUP;
-            if ((lane % GROUP) == 0 && LL_OK_IDX(2, (rgi + q * mv.rg) * mv.ws + sw, MAX_PART))
-                s.part[slot][(rgi + q * mv.rg) * mv.ws + sw] = sum;
+            // this warp's k-slice of its rows; the page goes back to the producer
+            // as soon as every active warp has read it (the k-slices are summed
+            // once per instruction, below)
+            const int r = rgi + (lane / GROUP) * mv.rg;
+            if ((lane % GROUP) == 0 && r < nr && LL_OK_IDX(2, (acc0 + pr + r) * mv.ws + sw, KPART_FLOATS))
+                s.kpart[(acc0 + pr + r) * mv.ws + sw] = sum;
             __syncwarp();
-            int last = 0;
             if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(&s.pcnt[slot], 1) == active - 1;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {  // this warp finishes the page: sum the k-slices of every row
-                __threadfence_block();
-                for (int r = lane; r < nr; r += 32) {
-                    float y = 0.f;
-                    for (int w = 0; w < mv.ws; w++)
-                        if (LL_OK_IDX(3, r * mv.ws + w, MAX_PART)) y += s.part[slot][r * mv.ws + w];
-                    if (LL_OK_IDX(4, acc0 + pr + r, ACC_FLOATS)) s.acc[acc0 + pr + r] = y;
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    s.pcnt[slot] = 0;
-                    ptrace_put(p, this_page, 2);
-                    mbar_arrive(&s.empty[slot]);
-                }
+                ptrace_put(p, this_page, 2);
+                mbar_arrive_cnt(&s.empty[slot], my_arrivals);
             }
         }
     }
     if (tid == 0) trace_put(p, ii, 7);
-    if (consumer_any(bad)) return false;  // else every page is reduced into s.acc
+    if (consumer_any(bad)) return false;  // else every k-slice of every row is in s.kpart
+    for (int i = tid; i < ntot; i += NCT) {
+        float y = 0.f;
+        for (int w = 0; w < mv.ws; w++)
+            if (LL_OK_IDX(3, i * mv.ws + w, KPART_FLOATS)) y += s.kpart[i * mv.ws + w];
+        if (LL_OK_IDX(4, i, ACC_FLOATS)) s.acc[i] = y;
+    }
+    consumer_sync();
     mv_store(p, s, ins, ii, best, best_idx);
     return true;
 }
@@ -1114,7 +1115,7 @@ __device__ bool attn_item(const KParams &p, Smem &s, uint8_t *pages, const Instr
         attn_block<DL>(p, s, pg, pg + PAGE_BYTES / 4, n, with_new, oacc, G, ii);  // V at half a page
         if (tid == 0) {
             ptrace_put(p, cpage, 2);
-            mbar_arrive(&s.empty[slot]);
+            mbar_arrive_cnt(&s.empty[slot], NCW);
         }
         ++cpage;
     }
@@ -1393,7 +1394,7 @@ __device__ bool attn_item_flash(const KParams &p, Smem &s, uint8_t *pages, const
             if (atomicAdd(&s.pcnt[slot], 1) == DG * W - 1) {
                 s.pcnt[slot] = 0;
                 ptrace_put(p, page, 2);
-                mbar_arrive(&s.empty[slot]);
+                mbar_arrive_cnt(&s.empty[slot], NCW);
             }
         }
     }
@@ -1849,7 +1850,7 @@ __device__ bool mv_instr_tc(const KParams &p, Smem &s, uint8_t *pages, const Ins
                     if (lane == 0) {
                         s.pcnt[slot] = 0;
                         ptrace_put(p, this_page, 2);
-                        mbar_arrive(&s.empty[slot]);
+                        mbar_arrive_cnt(&s.empty[slot], NCW);
                     }
                 }
             }
@@ -2163,7 +2164,8 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
 #undef LL_MV_CASE
                 default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
             }
-            if (ok && ins.op == OP_LMHEAD) lm_finish(p, s, best, best_idx);
+            // (an SM's vocabulary rows may come in several pieces: the last one finishes)
+            if (ok && ins.op == OP_LMHEAD && ins.sub) lm_finish(p, s, best, best_idx);
         }
         if (ok) ok = instr_sync(s);
         if (!ok) return false;
@@ -2196,7 +2198,7 @@ __device__ __forceinline__ void megakernel_body(const KParams &p) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < NPAGES; i++) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.empty[i], NCW);
             s.pcnt[i] = 0;
             s.slot_page[i] = 0xffffffffu;
         }
