@@ -32,9 +32,9 @@ constexpr int MAX_GQA = 8;                 // query heads per KV head
 constexpr int MAX_HD = 128;
 constexpr int MAX_RPP = 64;                // rows per page (hidden 256 at one vector per lane)
 constexpr int MAX_PART = 128;              // (row, k-slice) partial sums per page
-constexpr int ACC_FLOATS = 2048;           // per-SM row results held until the instruction ends
+constexpr int ACC_FLOATS = 2048;           // rows of one SM's matrix-vector instruction, at most
 constexpr int XIN_FLOATS = 4096;           // largest O-projection input (n_q_heads * head_dim)
-constexpr int KPART_FLOATS = XIN_FLOATS - ACC_FLOATS;  // (row, k-slice) partial sums of one instruction
+constexpr int KPART_FLOATS = XIN_FLOATS;   // (row, k-slice) partial sums of one instruction
 constexpr int XOWN_MAX = 64;               // residual rows one SM owns (hidden / SMs, rounded up)
 constexpr int ATTN_SPLIT_POS = 128;        // cached positions one attention split aims at
 constexpr int ATT_WARPS = 8;               // warps that split an attention page's P.V
@@ -80,6 +80,10 @@ struct Instr {
 // own kc / NCW columns of the chunk.
 struct MvShape {
     int32_t K, ws, vpl, rpp, rg, rw, teams, tc, kc, nch;
+    // per consumer warp w (CUDA-core pages): its team, k-slice and row group, and
+    // the arrivals it makes on a page's release (0: no work in its team); set by
+    // mv_shape so that the kernel divides by none of the runtime sizes
+    uint8_t w_team[NCW], w_sw[NCW], w_rgi[NCW], w_arrive[NCW];
 };
 constexpr int TC_ROWS = 8;        // rows of a tensor-core page (the MMA's n)
 constexpr int TC_MATS_PER_LAYER = 7;  // wq, wk, wv, wo, wg, wu, wd: the matrices whose pages may be tensor-core pages

@@ -192,10 +192,7 @@ struct alignas(16) Smem {
     union {
         float xin[XIN_FLOATS];  // O-projection input: the merged attention output; also the
                                 // attention P.V partials of the P.V warps
-        struct {
-            float acc[ACC_FLOATS];      // the SM's row results of the current matrix-vector instruction
-            float kpart[KPART_FLOATS];  // its (row, k-slice) partial sums, [row][k-slice]
-        };
+        float kpart[KPART_FLOATS];  // the current matrix-vector instruction's (row, k-slice) partial sums
         struct {                                // attention, block-wide softmax per page:
             float ared_lo[ATT_WARPS * 4 * 64];  // P.V partials of four heads of 64 dims
             float sc[MAX_GQA][132];             // scores of up to 129 positions
@@ -479,7 +476,7 @@ template <int VPL>
 __device__ __forceinline__ void load_gain(const KParams &p, const Smem &s, const Instr &ins, const MvShape &mv, uint4 (&gv)[VPL]) {
     const uint16_t *gain = norm_gain(p, s, ins);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sw = (warp % (NCW / mv.teams)) % mv.ws;
+    const int sw = mv.w_sw[warp];
 #pragma unroll
     for (int j = 0; j < VPL; j++)
         gv[j] = gain ? __ldg(reinterpret_cast<const uint4 *>(gain) + j * 32 * mv.ws + sw * 32 + lane) : make_uint4(0, 0, 0, 0);
@@ -494,7 +491,7 @@ template <int VPL>
 __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
                            float (&xr)[VPL * 8], const uint4 (&gv)[VPL]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int sw = (warp % (NCW / mv.teams)) % mv.ws;
+    const int sw = mv.w_sw[warp];
     const bool normed = norm_gain(p, s, ins) != nullptr;
     const uint64_t *src = nullptr;
     uint32_t tag = 0;
@@ -572,11 +569,11 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
         }
     }
     // (wide inputs: also every warp is done with its part of s.xin, which
-    // s.acc overlaps, before any team writes row results)
+    // s.kpart overlaps, before any team writes partial sums)
     if (!staged && src && consumer_any(s.abort)) return false;
     if (!normed) {
-        // s.acc shares space with s.xin: every warp holds its input before any
-        // team writes row results
+        // s.kpart shares space with s.xin: every warp holds its input before any
+        // team writes partial sums
         if (staged) consumer_sync();
         return true;
     }
@@ -629,21 +626,31 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[R]) {
     return v[0];
 }
 
-// The epilogue of a matrix-vector instruction, once every row's result is in
-// s.acc: q/k/v, the residual stream, silu(gate) * up, or the logits and each
-// thread's running argmax, stored as the instruction's outputs. Inlined: as a
-// called function it made the 1B step ~7 % slower (measured).
-__device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr &ins, int ii, float &best,
+// The epilogue of a matrix-vector instruction, once every (row, k-slice)
+// partial is in s.kpart: each row's sum of its ws k-slices, stored as q/k/v, the
+// residual stream, silu(gate) * up, or the logits and each thread's running
+// argmax. Inlined: as a called function it made the 1B step ~7 % slower (measured).
+__device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr &ins, int ii, int ws, float &best,
                                          int &best_idx) {
     const int tid = threadIdx.x;
     const int nrows = ins.r1 - ins.r0;
     const int r0 = ins.r0;
     const uint32_t wtag = write_tag(p, s, ins);
+    struct RowSum {  // the row's k-slices, summed in k-slice order
+        const float *kp;
+        int ws;
+        __device__ float operator[](int t) const {
+            float y = 0.f;
+            for (int w = 0; w < ws; w++)
+                if (LL_OK_IDX(3, t * ws + w, KPART_FLOATS)) y += kp[t * ws + w];
+            return y;
+        }
+    } acc{s.kpart, ws};
     switch (ins.op) {
         case OP_QKV:
             for (int t = tid; t < nrows; t += NCT)
                 if (LL_OK_IDX(5, r0 + t, (p.nq + 2 * p.nkv) * p.hd) && LL_OK_IDX(6, t, ACC_FLOATS))
-                    st_tag(p.t_qkv + r0 + t, s.acc[t], wtag);
+                    st_tag(p.t_qkv + r0 + t, acc[t], wtag);
             break;
         case OP_OPROJ:
         case OP_DOWN: {
@@ -654,7 +661,7 @@ __device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr 
                 const int row = r0 + t;
                 if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) continue;
                 const float base = from_embed ? bf16_to_f(p.embed[size_t(s.token) * p.H + row]) : s.xown[t];
-                const float v = base + s.acc[t];
+                const float v = base + acc[t];
                 s.xown[t] = v;
                 st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + row, v, wtag);
             }
@@ -662,14 +669,14 @@ __device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr 
         }
         case OP_GATEUP:
             for (int t = tid; t < nrows; t += NCT) {
-                const float g = s.acc[t];
+                const float g = acc[t];
                 if (LL_OK_IDX(8, r0 + t, p.I) && LL_OK_IDX(9, nrows + t, ACC_FLOATS))
-                    st_tag(p.t_act + r0 + t, g / (1.0f + expf(-g)) * s.acc[nrows + t], wtag);
+                    st_tag(p.t_act + r0 + t, g / (1.0f + expf(-g)) * acc[nrows + t], wtag);
             }
             break;
         default:  // OP_LMHEAD: logits out, running argmax per thread (rows ascend per thread)
             for (int t = tid; t < nrows; t += NCT) {
-                const float y = s.acc[t];
+                const float y = acc[t];
                 if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[r0 + t] = y;
                 if (y > best) {
                     best = y;
@@ -696,12 +703,9 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     if (threadIdx.x == 0) trace_put(p, ii, 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int W = NCW / mv.teams, team = warp / W, wt = warp % W;
-    const int active = mv.ws * mv.rg;  // working warps per team
-    const int sw = wt % mv.ws, rgi = wt / mv.ws;
-    // a page is released by the NCW arrivals its team's active warps make in all
-    const uint32_t my_arrivals = uint32_t(wt == 0 ? NCW - (active - 1) * (NCW / active) : NCW / active);
-    int ntot = 0;  // rows of s.acc this instruction fills
+    const int team = mv.w_team[warp], sw = mv.w_sw[warp], rgi = mv.w_rgi[warp];
+    // a page is released by the NCW arrivals its team's working warps make in all
+    const uint32_t my_arrivals = mv.w_arrive[warp];  // 0: no work in this warp
     const uint32_t row_bytes = uint32_t(mv.K) * 2;
     const int nrows = ins.r1 - ins.r0;
     constexpr int GROUP = 32 / RW;  // lanes that end up holding one row's sum
@@ -710,19 +714,18 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
 
     for (int si = 0; si < nseg; si++) {
         const Seg sg = seg[si];
-        // where the segment's rows land in s.acc
+        // where the segment's rows land among the instruction's rows (s.kpart)
         const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
-        ntot = max(ntot, acc0 + sg.nrows);
         for (int pr = 0; pr < sg.nrows; pr += mv.rpp) {
             const int nr = min(mv.rpp, sg.nrows - pr);
             const uint32_t slot = cpage % NPAGES;
             const uint32_t this_page = cpage++;
-            if (int(this_page & uint32_t(mv.teams - 1)) != team || wt >= active) continue;
+            if (int(this_page & uint32_t(mv.teams - 1)) != team || my_arrivals == 0) continue;
             if (bad || !wait_page(p, s, this_page)) {
                 bad = true;
                 continue;
             }
-            if (wt == 0 && lane == 0) {
+            if ((sw | rgi) == 0 && lane == 0) {  // the team's first warp
                 ptrace_put(p, this_page, 1);
                 if (si == 0 && pr == 0) trace_put(p, ii, 6);
             }
@@ -778,14 +781,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     }
     if (tid == 0) trace_put(p, ii, 7);
     if (consumer_any(bad)) return false;  // else every k-slice of every row is in s.kpart
-    for (int i = tid; i < ntot; i += NCT) {
-        float y = 0.f;
-        for (int w = 0; w < mv.ws; w++)
-            if (LL_OK_IDX(3, i * mv.ws + w, KPART_FLOATS)) y += s.kpart[i * mv.ws + w];
-        if (LL_OK_IDX(4, i, ACC_FLOATS)) s.acc[i] = y;
-    }
-    consumer_sync();
-    mv_store(p, s, ins, ii, best, best_idx);
+    mv_store(p, s, ins, ii, mv.ws, best, best_idx);
     return true;
 }
 

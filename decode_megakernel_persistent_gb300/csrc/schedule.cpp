@@ -97,7 +97,7 @@ static bool mv_combo_ok(int vpl, int rw) {
 bool mv_shape_tc(int K, MvShape &m) {
     if (K <= 0 || K % 1024 != 0 || K > 16384) return false;
     const int kc = K % 2048 == 0 ? 2048 : 1024;
-    m = MvShape{K, NCW, 0, TC_ROWS, 1, TC_ROWS, 1, 1, kc, K / kc};
+    m = MvShape{K, NCW, 0, TC_ROWS, 1, TC_ROWS, 1, 1, kc, K / kc, {}, {}, {}, {}};
     return true;
 }
 
@@ -123,10 +123,23 @@ bool mv_shape(int K, MvShape &m, int lane_floats) {
         if (active > best_active || (active == best_active && rpp > best_rpp)) {
             best_active = active;
             best_rpp = rpp;
-            m = MvShape{K, ws, vpl, rpp, rg, rw, teams, 0, K, 1};
+            m = MvShape{K, ws, vpl, rpp, rg, rw, teams, 0, K, 1, {}, {}, {}, {}};
         }
     }
-    return best_active > 0;
+    if (best_active == 0) return false;
+    // warp roles: warps [team * W, team * W + W) form a team; within it warp wt
+    // takes k-slice wt % ws of row group wt / ws, and the ws * rg working warps
+    // release a page with NCW arrivals in all (warp 0 of the team takes the rest)
+    const int active = m.ws * m.rg;
+    for (int w = 0; w < NCW; w++) {
+        const int wt = w % W;
+        m.w_team[w] = static_cast<uint8_t>(w / W);
+        m.w_sw[w] = static_cast<uint8_t>(wt % m.ws);
+        m.w_rgi[w] = static_cast<uint8_t>(wt / m.ws);
+        m.w_arrive[w] = static_cast<uint8_t>(wt >= active ? 0 : wt == 0 ? NCW - (active - 1) * (NCW / active)
+                                                                        : NCW / active);
+    }
+    return true;
 }
 
 // The producer lists: for every SM, the pages its consumers will take, in the
