@@ -36,9 +36,13 @@
 namespace ll {
 namespace {
 
-constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 4, GTHREADS = 128;
+constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 128;
 constexpr int NTERMS = 3;  // bf16 terms of an activation
 constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A and B alike)
+// A pipeline stage holds one K step of every A term and every B operand (the B
+// tile is loaded once for the three terms): 64 KB with one B operand, 80 KB with
+// two; as many stages as fit the 227 KB a block may have.
+__host__ __device__ constexpr int gstages(int nb) { return nb == 2 ? 2 : 3; }
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -107,8 +111,11 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const TensorMap *map, int x,
 enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_GATEUP = 2 };
 
 struct GemmArgs {
-    TensorMap a[NTERMS], b, b2;  // A terms [rows][K]; B [N][K] (EPI_GATEUP: b the gate, b2 the up matrix); bf16,
-                                 // K-major, boxes 64 x 128, 128-byte swizzle
+    TensorMap a[NTERMS];         // A terms [rows][K], bf16, K-major, boxes 64 x 128, 128-byte swizzle
+    TensorMap b[3];              // B [N][K] alike. EPI_GATEUP: b[0] the gate, b[1] the up matrix. Otherwise
+                                 // the output columns may stack up to three matrices: columns [0, bsplit1)
+                                 // come from b[0], [bsplit1, bsplit2) from b[1], the rest from b[2]
+    int bsplit1, bsplit2;        // multiples of GN (a tile never straddles two matrices)
     int M, N, K;                 // positions, outputs, inner width (K a multiple of 64)
     float *c;                    // [M][ldc] fp32: EPI_STORE c = A B^T, EPI_ADD c += A B^T
     int ldc;
@@ -124,7 +131,8 @@ struct GemmArgs {
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
-    constexpr uint32_t STAGE = GTILE * (1 + NB);
+    constexpr int GSTAGES = gstages(NB);
+    constexpr uint32_t STAGE = GTILE * (NTERMS + NB);
     constexpr uint32_t TCOLS = 128 * NB;
     extern __shared__ __align__(1024) uint8_t gsm[];
     uint8_t *tiles = gsm;
@@ -135,7 +143,10 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     volatile int *err = reinterpret_cast<volatile int *>(done + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
-    const int nk = g.K / GK, iters = NTERMS * nk;  // the K loop of term 0, then of term 1, ...
+    const int iters = g.K / GK;  // K steps; each stage carries every term
+    // the B matrix of this tile's columns and the tile's first row in it
+    const int bsel = NB == 2 ? 0 : (n0 >= g.bsplit2 ? 2 : n0 >= g.bsplit1 ? 1 : 0);
+    const int brow = n0 - (bsel == 2 ? g.bsplit2 : bsel == 1 ? g.bsplit1 : 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < GSTAGES; s++) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[s])) : "memory");
@@ -164,11 +175,16 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             if (it >= GSTAGES && !mbar_wait(&empty[s], ((it / GSTAGES) - 1) & 1, g.timeout_ns, g.status, err)) break;
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[s])), "r"(STAGE)
                          : "memory");
-            const int kc = (it % nk) * GK;
-            const uint32_t a_dst = saddr(tiles + size_t(s) * STAGE);
-            tma2d(a_dst, &g.a[it / nk], kc, m0, &full[s]);
-            tma2d(a_dst + GTILE, &g.b, kc, n0, &full[s]);
-            if (NB == 2) tma2d(a_dst + 2 * GTILE, &g.b2, kc, n0, &full[s]);
+            const int kc = it * GK;
+            const uint32_t dst = saddr(tiles + size_t(s) * STAGE);
+#pragma unroll
+            for (int q = 0; q < NTERMS; q++) tma2d(dst + q * GTILE, &g.a[q], kc, m0, &full[s]);
+            if (NB == 2) {
+                tma2d(dst + NTERMS * GTILE, &g.b[0], kc, n0, &full[s]);
+                tma2d(dst + (NTERMS + 1) * GTILE, &g.b[1], kc, n0, &full[s]);
+            } else {
+                tma2d(dst + NTERMS * GTILE, &g.b[bsel], kc, brow, &full[s]);
+            }
             sent++;
         }
         // never leave with copies in flight into this block's shared memory (after
@@ -184,19 +200,22 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             const int s = it % GSTAGES;
             if (!mbar_wait(&full[s], (it / GSTAGES) & 1, g.timeout_ns, g.status, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a_addr = saddr(tiles + size_t(s) * STAGE);
-            const uint64_t ad = smem_desc_sw128(a_addr);
+            const uint32_t base = saddr(tiles + size_t(s) * STAGE);
 #pragma unroll
-            for (int nb = 0; nb < NB; nb++) {
-                const uint64_t bd = smem_desc_sw128(a_addr + GTILE * (1 + nb));
+            for (int q = 0; q < NTERMS; q++) {
+                const uint64_t ad = smem_desc_sw128(base + q * GTILE);
 #pragma unroll
-                for (int kk = 0; kk < GK / 16; kk++) {
-                    const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + uint32_t(128 * nb)),
-                        "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
-                        : "memory");
+                for (int nb = 0; nb < NB; nb++) {
+                    const uint64_t bd = smem_desc_sw128(base + GTILE * (NTERMS + nb));
+#pragma unroll
+                    for (int kk = 0; kk < GK / 16; kk++) {
+                        const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + uint32_t(128 * nb)),
+                            "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
+                            : "memory");
+                    }
                 }
             }
             // the stage is free once these products have read it
@@ -212,15 +231,17 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     const bool ok = mbar_wait(done, 0, g.timeout_ns, g.status, err) && !*err;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int row = m0 + warp * 32 + lane;
+    // (the wait is in the same statement as the load, so no use of the
+    // registers can be placed before it)
     auto ld16 = [&](uint32_t col, uint32_t (&r)[16]) {
         const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + col;
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-            "%14, %15}, [%16];"
+            "%14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            : "r"(taddr)
+            : "memory");
     };
     if (ok) {
 #pragma unroll 1
@@ -568,18 +589,22 @@ bool encode_operand(const uint16_t *base, int64_t rows, int K, TensorMap &out) {
     return true;
 }
 
+// C = A B^T with B the nb (1 to 3) matrices bm[] stacked by output column (at
+// splits s1, s2: multiples of GN), or, for EPI_GATEUP, the gate and up matrices.
 template <int EPI>
-int gemm(const TensorMap *a, const TensorMap &b, const TensorMap *b2, int M, int N, int K, float *c, int ldc,
+int gemm(const TensorMap *a, const TensorMap *bm, int nb, int s1, int s2, int M, int N, int K, float *c, int ldc,
          const Terms *act, const KParams &p, cudaStream_t st) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;
-    constexpr int SMEM = GSTAGES * int(GTILE) * (1 + NB) + 1024;
+    constexpr int SMEM = gstages(NB) * int(GTILE) * (NTERMS + NB) + 1024;
+    static_assert(SMEM <= 232448, "stages fit in shared memory");
     GemmArgs g;
     for (int q = 0; q < NTERMS; q++) {
         g.a[q] = a[q];
         g.act[q] = act ? act->t[q] : nullptr;
     }
-    g.b = b;
-    g.b2 = b2 ? *b2 : b;
+    for (int j = 0; j < 3; j++) g.b[j] = bm[j < nb ? j : 0];
+    g.bsplit1 = nb > 1 && EPI != EPI_GATEUP ? s1 : 1 << 30;
+    g.bsplit2 = nb > 2 && EPI != EPI_GATEUP ? s2 : 1 << 30;
     g.M = M;
     g.N = N;
     g.K = K;
@@ -675,18 +700,22 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         const size_t lb = size_t(l) * per_layer;
         const int ld = qd + 2 * kd;
         k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.attn_norm, H, p.eps, th);
-        rc = gemm<EPI_STORE>(b.m_h, m[0], nullptr, n, qd, H, b.qkv, ld, nullptr, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[1], nullptr, n, kd, H, b.qkv + qd, ld, nullptr, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m[2], nullptr, n, kd, H, b.qkv + qd + kd, ld, nullptr, p, st);
+        if (qd % GN == 0 && kd % GN == 0) {  // q, k and v in one GEMM over the stacked rows
+            rc = gemm<EPI_STORE>(b.m_h, m, 3, qd, qd + kd, n, ld, H, b.qkv, ld, nullptr, p, st);
+        } else {
+            rc = gemm<EPI_STORE>(b.m_h, m, 1, 0, 0, n, qd, H, b.qkv, ld, nullptr, p, st);
+            if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m + 1, 1, 0, 0, n, kd, H, b.qkv + qd, ld, nullptr, p, st);
+            if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m + 2, 1, 0, 0, n, kd, H, b.qkv + qd + kd, ld, nullptr, p, st);
+        }
         if (rc != LL_OK) break;
         k_pf_rope_kv<<<n, 256, 0, st>>>(b.qkv, p.rope_cs, pos0, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
         rc = launch_attention(p, b, lb, pos0, n, to, st);
-        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m[3], nullptr, n, H, qd, b.x, H, nullptr, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m + 3, 1, 0, 0, n, H, qd, b.x, H, nullptr, p, st);
         if (rc != LL_OK) break;
         k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
         // gate and up in one GEMM (two accumulators), silu(gate) * up as terms
-        rc = gemm<EPI_GATEUP>(b.m_h, m[4], &m[5], n, I, H, nullptr, I, &ta, p, st);
-        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m[6], nullptr, n, H, I, b.x, H, nullptr, p, st);
+        rc = gemm<EPI_GATEUP>(b.m_h, m + 4, 2, 0, 0, n, I, H, nullptr, I, &ta, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m + 6, 1, 0, 0, n, H, I, b.x, H, nullptr, p, st);
     }
     if (rc != LL_OK) return rc;
     if (cudaGetLastError() != cudaSuccess) return LL_ERR_CUDA;
