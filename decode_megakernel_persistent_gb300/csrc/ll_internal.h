@@ -245,6 +245,7 @@ struct PrefillBufs {
     float *hrow = nullptr, *logits = nullptr;       // [H], [V]: the last position's head
     TensorMap m_h[T], m_o[T], m_a[T];    // A operands (activations), boxes of 128 rows x 64 columns
     std::vector<TensorMap> m_w;          // B operands: [L][7] wq, wk, wv, wo, wg, wu, wd, boxes of 128 rows x 64
+    TensorMap m_k, m_v;                  // the K and V caches as [L * n_kv * max_seq][hd], boxes of 16 rows x 64
     void *mem = nullptr;
 };
 // Allocates (or grows) the buffers and encodes the maps; false on failure.

@@ -379,18 +379,22 @@ __global__ void k_pf_rope_kv(float *qkv, const float2 *rope, int pos0, int nq, i
     }
 }
 
-// Tensor-core causal attention of the prompt's positions. Block (8 positions, KV
-// head g): warp w takes position t = 8 blockIdx.x + w and the G query heads of
-// KV head g as the rows of an m16n8k16 A operand, each head's q (scaled by
-// 1/sqrt(hd)) as two bf16 terms (hi in rows 0..7, lo in rows 8..15). The block
-// walks the cache entries 0..pos0 + t in tiles of 16 positions, loaded once for
-// its eight warps into shared memory as [K | V][64-dim half][position][64 dims]
-// with 128-byte rows whose 16-byte chunk c sits at c ^ (row % 8) (so ldmatrix
-// rows fall in different bank groups); the next tile's loads are in flight
-// while this one is used. Per tile: S = Q K^T (K rows by ldmatrix as B), the
-// running max and sum of each head over the 4 lanes holding it, P = exp(S - m)
-// as hi and lo bf16 rows (already the A operand of P V), O += P V (V by
-// ldmatrix.trans). Positions past t are masked. Output: o as NTERMS bf16 terms.
+// Tensor-core causal attention of the prompt's positions. Block (16 positions,
+// KV head g), 8 consumer warps and a producer warp. A warp takes two positions
+// (one when the group has more than 4 query heads) and the G query heads of KV
+// head g as the rows of an m16n8k16 A operand: row r < 8 is position r / G, head
+// r % G, its q (scaled by 1/sqrt(hd)) as the hi bf16 term, row r + 8 the lo term.
+// The producer streams the cache entries 0..pos0 + the block's last position in
+// tiles of 16 positions through a ring of shared-memory stages by TMA (the
+// tensor maps' 128-byte swizzle puts 16-byte chunk c of row r at c ^ (r % 8), so
+// ldmatrix rows fall in different bank groups), each landing on the stage's
+// mbarrier and released by the consumer warps' arrivals. Per tile: S = Q K^T (K
+// rows by ldmatrix as B), each row's running max and sum over the 4 lanes
+// holding it, P = exp(S - m) as hi and lo bf16 rows (already the A operand of
+// P V), O += P V (V by ldmatrix.trans). Positions past a row's own are masked;
+// V rows past the block's last position are read as zeros (the cache there may
+// hold anything, and 0 * Inf is NaN).
+// Blocks with the most positions to walk come first. Output: o as NTERMS terms.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -413,26 +417,87 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+constexpr int AT_NW = 8;      // consumer warps of an attention block
+constexpr int AT_STAGES = 4;  // tiles in flight
+
+struct PfAttnArgs {
+    TensorMap kmap, vmap;  // the caches, boxes of 16 rows x 64 columns, 128-byte swizzle
+    const float *qkv;      // [n][qd + 2 kd]
+    int row0;              // cache row of (layer, KV head 0, position 0)
+    int pos0, n, nq, nkv, max_seq;
+    Terms o_t;
+    int32_t *status;
+    uint64_t timeout_ns;
+};
+
 template <int HD>
-__global__ void __launch_bounds__(256) k_pf_attn_tc(const float *qkv, const uint16_t *kc, const uint16_t *vc,
-                                                   size_t layer_base, int pos0, int n, int nq, int nkv, int max_seq,
-                                                   Terms o_t) {
-    constexpr int DH = HD / 64, KS = HD / 16, CPT = 4 * HD / 256;  // 64-dim halves, k-steps, 16-byte chunks per thread
-    __shared__ __align__(1024) uint8_t tile[2][DH][16][128];       // [K | V][half][position][128 bytes]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+__global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_constant__ PfAttnArgs a) {
+    constexpr int DH = HD / 64, KS = HD / 16;  // 64-dim halves, k-steps
+    constexpr uint32_t TILE_BYTES = 2u * DH * 16 * 128;
+    __shared__ __align__(1024) uint8_t tile[AT_STAGES][2][DH][16][128];  // [stage][K | V][half][position][128 bytes]
+    __shared__ __align__(8) uint64_t full[AT_STAGES], empty[AT_STAGES];
+    __shared__ __align__(16) uint32_t zrow[4];  // a zero 16-byte row for ldmatrix
+    __shared__ int err;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3, r8 = lane & 7;
-    const int g = blockIdx.y, G = nq / nkv, qd = nq * HD, kd = nkv * HD;
-    const int t = blockIdx.x * 8 + warp;
-    const int last = pos0 + min(t, n - 1);                          // this warp's last position
-    const int block_last = pos0 + min(blockIdx.x * 8 + 7, n - 1);  // the block's
+    const int g = blockIdx.y, G = a.nq / a.nkv, qd = a.nq * HD, kd = a.nkv * HD;
+    const int qpw = G <= 4 ? 2 : 1, qpb = AT_NW * qpw;  // positions per warp, per block
+    const int t_base = (gridDim.x - 1 - int(blockIdx.x)) * qpb;  // the longest walks first
+    const int block_last = a.pos0 + min(t_base + qpb - 1, a.n - 1);
+    const int ntiles = block_last / 16 + 1;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < AT_STAGES; st++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[st])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&empty[st])), "r"(AT_NW) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        err = 0;
+    }
+    if (threadIdx.x < 4) zrow[threadIdx.x] = 0u;
+    __syncthreads();
+    volatile int *errp = &err;
+    if (warp == AT_NW) {  // producer
+        if (lane == 0) {
+            const int row = a.row0 + g * a.max_seq;
+            int sent = 0;
+            for (int ti = 0; ti < ntiles; ti++) {
+                const int st = ti % AT_STAGES;
+                if (ti >= AT_STAGES &&
+                    !mbar_wait(&empty[st], ((ti / AT_STAGES) - 1) & 1, a.timeout_ns, a.status, errp))
+                    break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[st])),
+                             "r"(TILE_BYTES)
+                             : "memory");
+#pragma unroll
+                for (int h = 0; h < DH; h++) {
+                    tma2d(saddr(&tile[st][0][h][0][0]), &a.kmap, 64 * h, row + 16 * ti, &full[st]);
+                    tma2d(saddr(&tile[st][1][h][0][0]), &a.vmap, 64 * h, row + 16 * ti, &full[st]);
+                }
+                sent++;
+            }
+            // never leave with copies in flight into this block's shared memory
+            for (int q = sent > AT_STAGES ? sent - AT_STAGES : 0; q < sent; q++) {
+                const uint64_t t0 = now_ns();
+                while (!mbar_try(&full[q % AT_STAGES], (q / AT_STAGES) & 1) && now_ns() - t0 < a.timeout_ns) {
+                }
+            }
+        }
+        return;
+    }
+    // this lane's row: position pi of the warp, head h of the group
+    const bool row_ok = gq < qpw * G;
+    const int pi = row_ok ? gq / G : 0, hh = row_ok ? gq % G : 0;
+    const int t = t_base + warp * qpw + pi;
+    const int last = a.pos0 + min(t, a.n - 1);                                 // this row's last position
+    const int warp_last = a.pos0 + min(t_base + warp * qpw + qpw - 1, a.n - 1);  // the warp's
     const float scale = 1.0f / sqrtf(float(HD));
-    // q as A fragments: k-step ks, lane (gq, tq): head gq at dims 16 ks + 2tq, +1 (hi in x, lo in y) and +8, +9 (z, w)
+    // q as A fragments: k-step ks, lane (gq, tq): its row at dims 16 ks + 2tq, +1 (hi in x, lo in y) and +8, +9 (z, w)
     uint4 qa[KS];
 #pragma unroll
     for (int ks = 0; ks < KS; ks++) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (gq < G && t < n) {
-            const float *qr = qkv + size_t(t) * (qd + 2 * kd) + size_t(g * G + gq) * HD + 16 * ks + 2 * tq;
+        if (row_ok && t < a.n) {
+            const float *qr = a.qkv + size_t(t) * (qd + 2 * kd) + size_t(g * G + hh) * HD + 16 * ks + 2 * tq;
             v[0] = qr[0] * scale;
             v[1] = qr[1] * scale;
             v[2] = qr[8] * scale;
@@ -447,109 +512,105 @@ __global__ void __launch_bounds__(256) k_pf_attn_tc(const float *qkv, const uint
     float m_run = -INFINITY, l_run = 0.f, o[HD / 8][2];
 #pragma unroll
     for (int d = 0; d < HD / 8; d++) o[d][0] = o[d][1] = 0.f;
-    const uint16_t *kbase = kc + layer_base + size_t(g) * max_seq * HD;
-    const uint16_t *vbase = vc + layer_base + size_t(g) * max_seq * HD;
-    // this thread's 16-byte chunks of a tile: (K or V, position, chunk of the row)
-    auto fetch = [&](int j0, uint4 (&buf)[CPT]) {
-#pragma unroll
-        for (int u = 0; u < CPT; u++) {
-            const int i = tid + u * 256, kv = i / (16 * HD / 8), rem = i % (16 * HD / 8);
-            const int pos = rem / (HD / 8), c = rem % (HD / 8);
-            const int j = j0 + pos;
-            buf[u] = j <= block_last
-                         ? *reinterpret_cast<const uint4 *>((kv ? vbase : kbase) + size_t(j) * HD + c * 8)
-                         : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    uint4 nxt[CPT];
-    fetch(0, nxt);
-    for (int j0 = 0; j0 <= block_last; j0 += 16) {
-        __syncthreads();  // the previous tile is used up
-#pragma unroll
-        for (int u = 0; u < CPT; u++) {
-            const int i = tid + u * 256, kv = i / (16 * HD / 8), rem = i % (16 * HD / 8);
-            const int pos = rem / (HD / 8), c = rem % (HD / 8), h = c / 8, cc = c % 8;
-            *reinterpret_cast<uint4 *>(&tile[kv][h][pos][(cc ^ (pos & 7)) * 16]) = nxt[u];
-        }
-        __syncthreads();
-        if (j0 + 16 <= block_last) fetch(j0 + 16, nxt);  // in flight during this tile
-        if (j0 > last) continue;
-        // S = Q K^T: c[nb] holds positions j0 + 8 nb .. + 7
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
+    for (int ti = 0; ti < ntiles; ti++) {
+        const int st = ti % AT_STAGES, j0 = 16 * ti;
+        if (!mbar_wait(&full[st], (ti / AT_STAGES) & 1, a.timeout_ns, a.status, errp)) break;
+        if (j0 <= warp_last) {
+            // S = Q K^T: c[nb] holds positions j0 + 8 nb .. + 7
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             const int jk = 8 * (mi >> 1) + r8;  // this lane's ldmatrix row: position in the tile
 #pragma unroll
             for (int ks = 0; ks < KS; ks++) {
                 const uint32_t ch = uint32_t(2 * (ks & 3) + (mi & 1));
                 uint32_t b[4];
-                ldsm4(saddr(&tile[0][ks >> 2][jk][(ch ^ uint32_t(jk & 7)) * 16]), b);
+                ldsm4(saddr(&tile[st][0][ks >> 2][jk][(ch ^ uint32_t(jk & 7)) * 16]), b);
                 mma16816(c[0], qa[ks], b[0], b[1]);
                 mma16816(c[1], qa[ks], b[2], b[3]);
             }
-        }
-        float sc[4];
+            float sc[4];
 #pragma unroll
-        for (int nb = 0; nb < 2; nb++)
+            for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const int j = j0 + 8 * nb + 2 * tq + e;
-                sc[2 * nb + e] = j <= last ? c[nb][e] + c[nb][e + 2] : -INFINITY;
+                for (int e = 0; e < 2; e++) {
+                    const int j = j0 + 8 * nb + 2 * tq + e;
+                    sc[2 * nb + e] = j <= last ? c[nb][e] + c[nb][e + 2] : -INFINITY;
+                }
+            float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            // (a row past its last position in this tile keeps its state: m_new = m_run)
+            const float m_new = fmaxf(m_run, mt);
+            const float alpha = m_run == m_new ? 1.f : (m_run == -INFINITY ? 0.f : expf(m_run - m_new));
+            float pr[4], ps = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
+                ps += pr[e];
             }
-        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-        const float m_new = fmaxf(m_run, mt);  // finite: position j0 <= last exists
-        const float alpha = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
-        float pr[4], ps = 0.f;
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+            l_run = l_run * alpha + ps;
+            m_run = m_new;
+            const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
+            const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
+            const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162 *>(&h23);
+            const uint4 pa = make_uint4(h01, pack_bf16(pr[0] - __low2float(b01), pr[1] - __high2float(b01)), h23,
+                                        pack_bf16(pr[2] - __low2float(b23), pr[3] - __high2float(b23)));
+            // O += P V: 8 dims per product, two per ldmatrix
+            // (V rows past the block's last position read a zero row instead: the
+            // cache there may hold anything, and 0 * Inf is NaN)
+            const int jv = 8 * (mi & 1) + r8;
+            const bool vrow = j0 + jv <= block_last;
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-            pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
-            ps += pr[e];
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-        l_run = l_run * alpha + ps;
-        m_run = m_new;
-        const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
-        const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
-        const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162 *>(&h23);
-        const uint4 pa = make_uint4(h01, pack_bf16(pr[0] - __low2float(b01), pr[1] - __high2float(b01)), h23,
-                                    pack_bf16(pr[2] - __low2float(b23), pr[3] - __high2float(b23)));
-        // O += P V: 8 dims per product, two per ldmatrix
-        const int jv = 8 * (mi & 1) + r8;
+            for (int dd = 0; dd < HD / 16; dd++) {
+                const uint32_t ch = uint32_t(2 * (dd & 3) + (mi >> 1));
+                uint32_t b[4];
+                ldsm4t(vrow ? saddr(&tile[st][1][dd >> 2][jv][(ch ^ uint32_t(jv & 7)) * 16]) : saddr(zrow), b);
 #pragma unroll
-        for (int dd = 0; dd < HD / 16; dd++) {
-            const uint32_t ch = uint32_t(2 * (dd & 3) + (mi >> 1));
-            uint32_t b[4];
-            ldsm4t(saddr(&tile[1][dd >> 2][jv][(ch ^ uint32_t(jv & 7)) * 16]), b);
-#pragma unroll
-            for (int u = 0; u < 2; u++) {
-                const int d = 2 * dd + u;
-                float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
-                mma16816(acc, pa, b[2 * u], b[2 * u + 1]);
-                o[d][0] = acc[0] + acc[2];
-                o[d][1] = acc[1] + acc[3];
+                for (int u = 0; u < 2; u++) {
+                    const int d = 2 * dd + u;
+                    float acc[4] = {o[d][0] * alpha, o[d][1] * alpha, 0.f, 0.f};
+                    mma16816(acc, pa, b[2 * u], b[2 * u + 1]);
+                    o[d][0] = acc[0] + acc[2];
+                    o[d][1] = acc[1] + acc[3];
+                }
             }
         }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&empty[st])) : "memory");
     }
-    if (t >= n || gq >= G) return;
-    // lane (gq, tq) holds head gq at dims 8 d + 2 tq, + 1
-    const size_t at = size_t(t) * qd + size_t(g * G + gq) * HD;
+    if (*errp || !row_ok || t >= a.n) return;
+    // lane (gq, tq) holds its row at dims 8 d + 2 tq, + 1
+    const size_t at = size_t(t) * qd + size_t(g * G + hh) * HD;
     const float inv = 1.0f / l_run;
 #pragma unroll
     for (int d = 0; d < HD / 8; d++) {
-        put_terms(o[d][0] * inv, o_t.t, at + 8 * d + 2 * tq);
-        put_terms(o[d][1] * inv, o_t.t, at + 8 * d + 2 * tq + 1);
+        put_terms(o[d][0] * inv, a.o_t.t, at + 8 * d + 2 * tq);
+        put_terms(o[d][1] * inv, a.o_t.t, at + 8 * d + 2 * tq + 1);
     }
 }
 
-int launch_attention(const KParams &p, const PrefillBufs &b, size_t lb, int pos0, int n, const Terms &to,
+int launch_attention(const KParams &p, const PrefillBufs &b, int layer, int pos0, int n, const Terms &to,
                      cudaStream_t st) {
-    const dim3 grid((n + 7) / 8, p.nkv);
+    PfAttnArgs a;
+    a.kmap = b.m_k;
+    a.vmap = b.m_v;
+    a.qkv = b.qkv;
+    a.row0 = layer * p.nkv * p.max_seq;
+    a.pos0 = pos0;
+    a.n = n;
+    a.nq = p.nq;
+    a.nkv = p.nkv;
+    a.max_seq = p.max_seq;
+    a.o_t = to;
+    a.status = p.status;
+    a.timeout_ns = p.timeout_ns;
+    const int qpb = AT_NW * (p.nq / p.nkv <= 4 ? 2 : 1);
+    const dim3 grid((n + qpb - 1) / qpb, p.nkv);
     if (p.hd == 64)
-        k_pf_attn_tc<64><<<grid, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
+        k_pf_attn_tc<64><<<grid, (AT_NW + 1) * 32, 0, st>>>(a);
     else
-        k_pf_attn_tc<128><<<grid, 256, 0, st>>>(b.qkv, p.k_cache, p.v_cache, lb, pos0, n, p.nq, p.nkv, p.max_seq, to);
+        k_pf_attn_tc<128><<<grid, (AT_NW + 1) * 32, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
@@ -663,6 +724,21 @@ bool prefill_prepare(const KParams &p, const LayerW *host_layers, int n, Prefill
     for (int q = 0; q < NTERMS && ok; q++)
         ok = encode_operand(b.h[q], int64_t(na), p.H, b.m_h[q]) && encode_operand(b.o[q], int64_t(na), int(qd), b.m_o[q]) &&
              encode_operand(b.a[q], int64_t(na), p.I, b.m_a[q]);
+    {  // the caches, [L * n_kv * max_seq][hd], in tiles of 16 rows x 64 columns
+        EncodeTiled enc = encoder();
+        const int64_t rows = int64_t(p.L) * p.nkv * p.max_seq;
+        const cuuint64_t dims[2] = {cuuint64_t(p.hd), cuuint64_t(rows)};
+        const cuuint64_t strides[1] = {cuuint64_t(p.hd) * 2};
+        const cuuint32_t box[2] = {64, 16}, estr[2] = {1, 1};
+        for (int i = 0; i < 2 && ok; i++) {
+            CUtensorMap m;
+            ok = enc && rows < (int64_t(1) << 31) &&
+                 enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i ? p.v_cache : p.k_cache, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            if (ok) std::memcpy(i ? &b.m_v : &b.m_k, &m, sizeof m);
+        }
+    }
     b.m_w.assign(size_t(p.L) * 7, TensorMap{});
     for (int l = 0; l < p.L && ok; l++) {
         const LayerW &w = host_layers[l];
@@ -709,7 +785,7 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         }
         if (rc != LL_OK) break;
         k_pf_rope_kv<<<n, 256, 0, st>>>(b.qkv, p.rope_cs, pos0, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
-        rc = launch_attention(p, b, lb, pos0, n, to, st);
+        rc = launch_attention(p, b, l, pos0, n, to, st);
         if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m + 3, 1, 0, 0, n, H, qd, b.x, H, nullptr, p, st);
         if (rc != LL_OK) break;
         k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
