@@ -91,7 +91,7 @@ def _code_only(text: str) -> str:
 # that backend's recorded counters valid).
 NOT_IN_BACKEND = {
     "megakernel": {"chain.cu", "prefill.cu", "static_step.cu"},
-    "chain": {"megakernel.cuh", "mk_cuda_cores.cu", "mk_tensor_cores.cu", "prefill.cu", "static_step.cu"},
+    "chain": {"megakernel.cuh", "mk_cuda_cores.cu", "mk_tensor_cores.cu", "mk_geo.cu", "prefill.cu", "static_step.cu"},
 }
 
 

@@ -16,8 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libll.so")
-SOURCES = ("mk_cuda_cores.cu", "mk_tensor_cores.cu", "chain.cu", "schedule.cpp", "api.cpp", "static_step.cu",
-           "prefill.cu")
+SOURCES = ("mk_cuda_cores.cu", "mk_tensor_cores.cu", "mk_geo.cu", "chain.cu", "schedule.cpp", "api.cpp",
+           "static_step.cu", "prefill.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

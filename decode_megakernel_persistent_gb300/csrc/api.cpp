@@ -578,6 +578,19 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
     if (const char *e = std::getenv("LL_MAX_INFLIGHT")) p.max_inflight = static_cast<uint32_t>(std::atoi(e));
     p.producer_sleep_ns = 64;
     if (const char *e = std::getenv("LL_PRODUCER_SLEEP_NS")) p.producer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
+    // the kernel instantiation with only this model's matrix-vector geometries,
+    // where one covers all three input widths (LL_GEO=0 forces the general one)
+    {
+        auto is = [](const ll::MvShape &m, int v, int r) { return !m.tc && m.vpl == v && m.rw == r; };
+        auto fam = [&](const ll::MvShape &m, int geo) {
+            return geo == ll::GEO_2048 ? (is(m, 2, 8) || is(m, 4, 2)) : (is(m, 4, 4) || is(m, 4, 1));
+        };
+        p.geo = ll::GEO_ALL;
+        for (int geo : {ll::GEO_2048, ll::GEO_4096})
+            if (fam(p.mv_h, geo) && fam(p.mv_q, geo) && fam(p.mv_i, geo)) p.geo = geo;
+        if (const char *e = std::getenv("LL_GEO"))
+            if (std::atoi(e) == 0) p.geo = ll::GEO_ALL;
+    }
     p.consumer_sleep_ns = 0;
     if (const char *e = std::getenv("LL_CONSUMER_SLEEP_NS")) p.consumer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
     h->d_instrs = d_instrs;

@@ -78,6 +78,11 @@ struct Instr {
 // into nch chunks of kc; a page holds up to TC_ROWS rows of one chunk, loaded by
 // TMA in the 128-byte swizzle, and all NCW warps work on every page, each on its
 // own kc / NCW columns of the chunk.
+// Geometry families of the CUDA-core kernel instantiations (see geo_has): hidden
+// 2048 with inter 8192 ((2, 8) and (4, 2)), hidden 4096 with inter 14336 ((4, 4)
+// and (4, 1)).
+enum : int { GEO_ALL = 0, GEO_2048 = 1, GEO_4096 = 2 };
+
 struct MvShape {
     int32_t K, ws, vpl, rpp, rg, rw, teams, tc, kc, nch;
     // per consumer warp w (CUDA-core pages): its team, k-slice and row group, and
@@ -194,6 +199,7 @@ struct KParams {
     uint32_t l2_prefetch;     // pages the producer may prefetch into L2 beyond its ring
     uint32_t evict_first;     // weight pages loaded with an L2 evict-first hint
     uint32_t producer_sleep_ns; // back-off of the producer while the ring is full
+    int32_t geo;                // GEO_*: the kernel instantiation whose geometries this handle uses
     uint32_t consumer_sleep_ns; // back-off of a consumer warp whose page is not issued yet
     uint32_t max_inflight;    // pages issued but not yet landed, at most (NPAGES: only the ring bounds it)
     // optional globaltimer trace, [nsm][max_instr][TRACE_WORDS]: consumer begin,

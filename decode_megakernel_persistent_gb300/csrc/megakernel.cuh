@@ -2130,7 +2130,16 @@ __device__ bool consumer_step_begin(const KParams &p, Smem &s, int st) {
     return !consumer_any(s.abort);
 }
 
-template <bool FLASH, bool TC>
+// The (vpl, rw) matrix-vector geometries a kernel carries: all of them (GEO 0), or
+// only those of one model family (the host picks such a kernel when a model's
+// three input widths all fall in it): the per-warp attention kernel ran 1.5-2.4 %
+// faster without the geometries it does not use.
+__host__ __device__ constexpr bool geo_has(int geo, int vpl, int rw) {
+    return geo == 0 || (geo == GEO_2048 && ((vpl == 2 && rw == 8) || (vpl == 4 && rw == 2))) ||
+           (geo == GEO_4096 && ((vpl == 4 && rw == 4) || (vpl == 4 && rw == 1)));
+}
+
+template <bool FLASH, bool TC, int GEO>
 __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const Instr *list, int n, uint32_t &cpage) {
     float best = -INFINITY;
     int best_idx = -1;
@@ -2152,8 +2161,15 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
         } else {
             const MvShape &mv = mv_of(p, ins.op);
             switch (mv.vpl * 16 + mv.rw) {
-#define LL_MV_CASE(V, R) \
-    case V * 16 + R: ok = mv_instr<V, R>(p, s, pages, ins, i, cpage, best, best_idx); break;
+#define LL_MV_CASE(V, R)                                                                     \
+    case V * 16 + R:                                                                         \
+        if constexpr (geo_has(GEO, V, R)) {                                                  \
+            ok = mv_instr<V, R>(p, s, pages, ins, i, cpage, best, best_idx);                 \
+        } else {                                                                             \
+            ok = false;                                                                      \
+            raise_status(p, s, LL_ERR_SHAPE);                                                \
+        }                                                                                    \
+        break;
                 // the (vpl, rw) pairs mv_shape can choose (see mv_combo_ok)
                 LL_MV_CASE(1, 8) LL_MV_CASE(2, 8) LL_MV_CASE(3, 1) LL_MV_CASE(3, 2)
                 LL_MV_CASE(3, 4) LL_MV_CASE(4, 1) LL_MV_CASE(4, 2) LL_MV_CASE(4, 4)
@@ -2170,14 +2186,14 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
     return true;
 }
 
-template <bool FLASH, bool TC>
+template <bool FLASH, bool TC, int GEO>
 __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
     const Instr *list = p.instrs + size_t(blockIdx.x) * p.max_instr;
     const int n = p.n_instr[blockIdx.x];
     uint32_t cpage = 0;
     for (int st = 0; st < p.n_steps; st++) {
         if (!(TC ? consumer_step_begin_b(p, s, st) : consumer_step_begin(p, s, st))) return;
-        if (!consumer_step<FLASH, TC>(p, s, pages, list, n, cpage)) return;
+        if (!consumer_step<FLASH, TC, GEO>(p, s, pages, list, n, cpage)) return;
     }
 }
 
@@ -2186,7 +2202,7 @@ __device__ void consumer(const KParams &p, Smem &s, uint8_t *pages) {
 // it (the host launches the TC kernel exactly when a width has mv.tc), so the
 // CUDA-core kernel carries none of that code: its size matters, the step being
 // sensitive to instruction-cache misses when the instruction kind changes.
-template <bool FLASH, bool TC>
+template <bool FLASH, bool TC, int GEO>
 __device__ __forceinline__ void megakernel_body(const KParams &p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *pages = smem;
@@ -2240,15 +2256,15 @@ __device__ __forceinline__ void megakernel_body(const KParams &p) {
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) producer<FLASH, TC>(p, s, pages);
     } else {
-        consumer<FLASH, TC>(p, s, pages);
+        consumer<FLASH, TC, GEO>(p, s, pages);
     }
 }
 
 // One block of NTHREADS per SM: ptxas gives each thread 96 registers (17 warps
 // on 4 schedulers: 5 warps share one scheduler's 16K registers).
-template <bool FLASH, bool TC>
+template <bool FLASH, bool TC, int GEO = 0>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ KParams p) {
-    megakernel_body<FLASH, TC>(p);
+    megakernel_body<FLASH, TC, GEO>(p);
 }
 
 
