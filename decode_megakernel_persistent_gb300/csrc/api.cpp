@@ -36,6 +36,7 @@ struct ll_handle {
     uint32_t epoch = 0;
     int nb = 1;                 // sequences decoded together (batched handles)
     bool batch_api = false;     // made by ll_init_batch: only ll_decode_steps_batch steps it
+    bool bcc = false;           // a batch of two on CUDA-core pages (mv_shape_bc geometry)
     int32_t *pinned = nullptr;  // [0, nb) next tokens, [nb] status
     uint8_t *tagged = nullptr;  // the megakernel's tagged activation words (cleared on reset)
     size_t tagged_bytes = 0;
@@ -168,14 +169,14 @@ void build_lists_for(const ll_config &c, int nsm, int splits, std::vector<std::v
 // The CUDA-core kernel keeps the (row, k-slice) partial sums of an instruction,
 // at most KPART_FLOATS of them, so its LM-head pieces are cut to fit as well
 // (whole pages of the hidden-width geometry).
-int lm_rows_cuda(const ll::MvShape &mh) {
-    const int rows = ll::KPART_FLOATS / std::max(1, mh.ws);
+int lm_rows_cuda(const ll::MvShape &mh, int nb = 1) {
+    const int rows = ll::KPART_FLOATS / std::max(1, mh.ws * nb);
     return std::max(mh.rpp, rows / std::max(1, mh.rpp) * mh.rpp);
 }
 
 int lm_rows_of(const ll_handle *h) {
     return h->kp.mv_h.tc ? std::max(ll::TC_ROWS, ll::BACC_FLOATS / h->nb / ll::TC_ROWS * ll::TC_ROWS)
-                         : lm_rows_cuda(h->kp.mv_h);
+                         : lm_rows_cuda(h->kp.mv_h, h->nb);
 }
 
 void build_lists(ll_handle *h) { build_lists_for(h->cfg, h->nsm, h->splits, h->lists, h->nb, lm_rows_of(h)); }
@@ -371,7 +372,25 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
     // weight tensor maps; a single-sequence handle without them keeps the
     // CUDA-core kernel.
     std::vector<ll::TensorMap> wmaps;
-    {
+    // A batch of two whose widths have two-sequence CUDA-core geometry runs on
+    // CUDA-core pages (each page read once for both sequences); LL_BATCH_CC=0
+    // keeps it on tensor-core pages.
+    if (batch_api && nb == 2 && c.backend == LL_BACKEND_MEGAKERNEL) {
+        ll::MvShape bh{}, bq{}, bi{};
+        bool cc = ll::mv_shape_bc(c.hidden, bh) && ll::mv_shape_bc(qd, bq) && ll::mv_shape_bc(c.inter, bi) &&
+                  per_sm(qkv_rows) * bh.ws * nb <= ll::KPART_FLOATS &&
+                  2 * per_sm(c.inter) * bh.ws * nb <= ll::KPART_FLOATS &&
+                  per_sm(c.hidden) * std::max(bq.ws, bi.ws) * nb <= ll::KPART_FLOATS &&
+                  per_sm(c.hidden) <= ll::XOWN_MAX;
+        if (const char *e = std::getenv("LL_BATCH_CC")) cc = cc && std::atoi(e) != 0;
+        if (cc) {
+            mh = bh;
+            mq = bq;
+            mi = bi;
+            h->bcc = true;
+        }
+    }
+    if (!h->bcc) {
         bool want_tc = batch_api;
         if (const char *e = std::getenv("LL_MV_TC")) want_tc = want_tc || std::atoi(e) != 0;
         ll::MvShape th{}, tq{}, ti{};
@@ -590,6 +609,7 @@ int init_handle(const ll_config *cfg, const ll_weights *w, uint16_t *const *k_ca
             if (fam(p.mv_h, geo) && fam(p.mv_q, geo) && fam(p.mv_i, geo)) p.geo = geo;
         if (const char *e = std::getenv("LL_GEO"))
             if (std::atoi(e) == 0) p.geo = ll::GEO_ALL;
+        if (h->bcc) p.geo = ll::GEO_BCC;
     }
     p.consumer_sleep_ns = 0;
     if (const char *e = std::getenv("LL_CONSUMER_SLEEP_NS")) p.consumer_sleep_ns = static_cast<uint32_t>(std::atoi(e));
@@ -774,6 +794,7 @@ int ll_query(const ll_handle *h, int what, int64_t *value) {
         case LL_Q_SMEM_BYTES: *value = h->smem_bytes; break;
         case LL_Q_MV_TC: *value = (h->kp.mv_h.tc ? 1 : 0) | (h->kp.mv_q.tc ? 2 : 0) | (h->kp.mv_i.tc ? 4 : 0); break;
         case LL_Q_BATCH: *value = h->nb; break;
+        case LL_Q_BATCH_CC: *value = h->bcc ? 1 : 0; break;
         case LL_Q_TRACE_BYTES:
             *value = (int64_t(h->nsm) * h->max_instr * ll::TRACE_WORDS + int64_t(h->nsm) * ll::PTRACE_PAGES * 3) *
                      int64_t(sizeof(uint64_t));

@@ -81,7 +81,7 @@ struct Instr {
 // Geometry families of the CUDA-core kernel instantiations (see geo_has): hidden
 // 2048 with inter 8192 ((2, 8) and (4, 2)), hidden 4096 with inter 14336 ((4, 4)
 // and (4, 1)).
-enum : int { GEO_ALL = 0, GEO_2048 = 1, GEO_4096 = 2 };
+enum : int { GEO_ALL = 0, GEO_2048 = 1, GEO_4096 = 2, GEO_BCC = 3 };  // GEO_BCC: two sequences on CUDA-core pages
 
 struct MvShape {
     int32_t K, ws, vpl, rpp, rg, rw, teams, tc, kc, nch;
@@ -267,6 +267,9 @@ void build_schedule(int L, int H, int qd, int kd, int I, int V, int nkv, int nsm
 // lane_floats: the most input floats a lane may hold per team copy of the
 // input (16 or 32); more allows more teams (pages in progress at once).
 bool mv_shape(int K, MvShape &m, int lane_floats = 16);
+// CUDA-core geometry for width K with two sequences' inputs held per lane (at
+// most 16 floats of each): only (vpl, rw) = (2, 8) or (2, 2); false otherwise.
+bool mv_shape_bc(int K, MvShape &m);
 // The tensor-core geometry for width K, if the kernel has it (K a multiple of
 // 1024, at most 16384): chunks of 2048 columns (1024 when 2048 does not divide K),
 // pages of TC_ROWS rows of one chunk, every warp on a whole number of 64-column

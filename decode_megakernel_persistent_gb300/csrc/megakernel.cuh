@@ -487,9 +487,9 @@ __device__ __forceinline__ void load_gain(const KParams &p, const Smem &s, const
 // that each tagged word is read once per block whatever the number of teams;
 // wider ones (the down projection's) are read straight into the lanes. Returns
 // false, in every consumer thread alike, if a wait failed.
-template <int VPL>
+template <int VPL, bool BAT = false>
 __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
-                           float (&xr)[VPL * 8], const uint4 (&gv)[VPL]) {
+                           float (&xr)[VPL * 8], const uint4 (&gv)[VPL], int b = 0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int sw = mv.w_sw[warp];
     const bool normed = norm_gain(p, s, ins) != nullptr;
@@ -508,6 +508,7 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
         case OP_OPROJ: src = p.t_o; tag = tag_of(p, s, ins.layer); break;
         default: break;
     }
+    if (BAT && src) src += size_t(b) * size_t(mv.K);  // sequence b's words (laid out sequence after sequence)
     const bool staged = src && mv.K <= XIN_FLOATS;
     if (staged) {
         constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
@@ -541,7 +542,7 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
             xr[j * 8 + 0] = a.x; xr[j * 8 + 1] = a.y; xr[j * 8 + 2] = a.z; xr[j * 8 + 3] = a.w;
             xr[j * 8 + 4] = b.x; xr[j * 8 + 5] = b.y; xr[j * 8 + 6] = b.z; xr[j * 8 + 7] = b.w;
         } else if (!src) {  // layer 0: the token's embedding row
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p.embed + size_t(s.token) * p.H) + v);
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p.embed + size_t(BAT ? s.btoken[b] : s.token) * p.H) + v);
             xr[j * 8 + 0] = bf_lo(u.x); xr[j * 8 + 1] = bf_hi(u.x);
             xr[j * 8 + 2] = bf_lo(u.y); xr[j * 8 + 3] = bf_hi(u.y);
             xr[j * 8 + 4] = bf_lo(u.z); xr[j * 8 + 5] = bf_hi(u.z);
@@ -782,6 +783,159 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     if (tid == 0) trace_put(p, ii, 7);
     if (consumer_any(bad)) return false;  // else every k-slice of every row is in s.kpart
     mv_store(p, s, ins, ii, mv.ws, best, best_idx);
+    return true;
+}
+
+// ---------------------------------------------------------------------------------
+// Two sequences on CUDA-core pages (batched handles whose input widths allow it,
+// see mv_shape_bc): every page is read once and multiplied with both sequences'
+// inputs, each lane holding 2 x VPL x 8 input floats. The (row, k-slice,
+// sequence) partials go to s.kpart; the epilogue sums them per (row, sequence)
+// and stores each sequence's outputs as the batched kernel lays them out.
+constexpr int NBC = 2;  // sequences of the batched CUDA-core kernel
+
+__device__ __forceinline__ void mv_store_bc(const KParams &p, Smem &s, const Instr &ins, int ii, int ws, float &best,
+                                            int &best_idx) {
+    const int tid = threadIdx.x;
+    const int nrows = ins.r1 - ins.r0, r0 = ins.r0;
+    const uint32_t wtag = write_tag(p, s, ins);
+    auto sum = [&](int t, int b) {  // row t's k-slices of sequence b, in k-slice order
+        float y = 0.f;
+        for (int w = 0; w < ws; w++)
+            if (LL_OK_IDX(3, (t * ws + w) * NBC + b, KPART_FLOATS)) y += s.kpart[(t * ws + w) * NBC + b];
+        return y;
+    };
+    const int qkvd = (p.nq + 2 * p.nkv) * p.hd;
+    // idx % NBC == tid % NBC: each thread keeps to one sequence (lm_finish_b's argmax)
+    for (int idx = tid; idx < nrows * NBC; idx += NCT) {
+        const int t = idx / NBC, b = idx % NBC;
+        const float y = sum(t, b);
+        switch (ins.op) {
+            case OP_QKV:
+                if (LL_OK_IDX(5, r0 + t, qkvd)) st_tag(p.t_qkv + size_t(b) * qkvd + r0 + t, y, wtag);
+                break;
+            case OP_OPROJ:
+            case OP_DOWN: {
+                const int row = r0 + t;
+                if (!LL_OK_IDX(7, row, p.H) || !LL_OK_IDX(20, t, XOWN_MAX)) break;
+                const float base = ins.op == OP_OPROJ && ins.layer == 0
+                                       ? bf16_to_f(p.embed[size_t(s.btoken[b]) * p.H + row])
+                                       : s.bxown[b][t];
+                const float v = base + y;
+                s.bxown[b][t] = v;
+                st_tag((ins.op == OP_OPROJ ? p.t_xmid : p.t_xout) + size_t(b) * p.H + row, v, wtag);
+                break;
+            }
+            case OP_GATEUP: {
+                const float u = sum(nrows + t, b);
+                if (LL_OK_IDX(8, r0 + t, p.I)) st_tag(p.t_act + size_t(b) * p.I + r0 + t, y / (1.0f + expf(-y)) * u, wtag);
+                break;
+            }
+            default:  // OP_LMHEAD: rows ascend per thread
+                if (s.c_logits && LL_OK_IDX(10, r0 + t, p.V)) s.c_logits[size_t(b) * p.V + r0 + t] = y;
+                if (y > best) {
+                    best = y;
+                    best_idx = r0 + t;
+                }
+                break;
+        }
+    }
+}
+
+template <int VPL, int RW>
+__device__ bool mv_instr_bc(const KParams &p, Smem &s, uint8_t *pages, const Instr &ins, int ii, uint32_t &cpage,
+                            float &best, int &best_idx) {
+    const MvShape &mv = mv_of(p, ins.op);
+    Seg seg[3];
+    const int nseg = mv_segments(p, s, ins, seg);
+    if (nseg == 0) return true;
+    float xr[NBC][VPL * 8];
+#pragma unroll
+    for (int b = 0; b < NBC; b++) {
+        uint4 gv[VPL];
+        load_gain<VPL>(p, s, ins, mv, gv);
+        if (!load_input<VPL, true>(p, s, ins, mv, xr[b], gv, b)) return false;
+    }
+    if (threadIdx.x == 0) trace_put(p, ii, 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int team = mv.w_team[warp], sw = mv.w_sw[warp], rgi = mv.w_rgi[warp];
+    const uint32_t my_arrivals = mv.w_arrive[warp];
+    const uint32_t row_bytes = uint32_t(mv.K) * 2;
+    const int nrows = ins.r1 - ins.r0;
+    constexpr int GROUP = 32 / RW;
+    constexpr int QB = (RW < 4 / VPL) ? RW : (4 / VPL > 0 ? 4 / VPL : 1);
+    bool bad = false;
+    for (int si = 0; si < nseg; si++) {
+        const Seg sg = seg[si];
+        const int acc0 = sg.kind == OUT_QKV ? sg.out0 + sg.row0 - ins.r0 : (sg.kind == OUT_UP ? nrows : 0);
+        for (int pr = 0; pr < sg.nrows; pr += mv.rpp) {
+            const int nr = min(mv.rpp, sg.nrows - pr);
+            const uint32_t slot = cpage % NPAGES;
+            const uint32_t this_page = cpage++;
+            if (int(this_page & uint32_t(mv.teams - 1)) != team || my_arrivals == 0) continue;
+            if (bad || !wait_page(p, s, this_page)) {
+                bad = true;
+                continue;
+            }
+            if ((sw | rgi) == 0 && lane == 0) {
+                ptrace_put(p, this_page, 1);
+                if (si == 0 && pr == 0) trace_put(p, ii, 6);
+            }
+            const uint32_t page = smem_addr(pages) + slot * PAGE_BYTES + (sw * 32 + lane) * 16;
+            float v[NBC][RW];
+#pragma unroll
+            for (int q0 = 0; q0 < RW; q0 += QB) {
+                uint4 wv[QB][VPL];
+#pragma unroll
+                for (int qq = 0; qq < QB; qq++) {
+                    const uint32_t wrow = page + uint32_t(rgi + (q0 + qq) * mv.rg) * row_bytes;
+#pragma unroll
+                    for (int j = 0; j < VPL; j++) {
+                        const uint32_t at = wrow + uint32_t(j * 32 * mv.ws) * 16u;
+                        if (LL_OK_IDX(1, (at + 16) - smem_addr(pages), NPAGES * PAGE_BYTES + 1))
+                            wv[qq][j] = lds128(at);
+                        else
+                            wv[qq][j] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < NBC; b++)
+#pragma unroll
+                    for (int qq = 0; qq < QB; qq++) {
+                        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < VPL; j++) {
+                            const uint4 w = wv[qq][j];
+                            a0 = fmaf(bf_lo(w.x), xr[b][j * 8 + 0], a0);
+                            a1 = fmaf(bf_hi(w.x), xr[b][j * 8 + 1], a1);
+                            a0 = fmaf(bf_lo(w.y), xr[b][j * 8 + 2], a0);
+                            a1 = fmaf(bf_hi(w.y), xr[b][j * 8 + 3], a1);
+                            a0 = fmaf(bf_lo(w.z), xr[b][j * 8 + 4], a0);
+                            a1 = fmaf(bf_hi(w.z), xr[b][j * 8 + 5], a1);
+                            a0 = fmaf(bf_lo(w.w), xr[b][j * 8 + 6], a0);
+                            a1 = fmaf(bf_hi(w.w), xr[b][j * 8 + 7], a1);
+                        }
+                        v[b][q0 + qq] = a0 + a1;
+                    }
+            }
+            const int r = rgi + (lane / GROUP) * mv.rg;
+#pragma unroll
+            for (int b = 0; b < NBC; b++) {
+                const float sum = transpose_reduce<RW>(v[b]);
+                const int k = ((acc0 + pr + r) * mv.ws + sw) * NBC + b;
+                if ((lane % GROUP) == 0 && r < nr && LL_OK_IDX(2, k, KPART_FLOATS)) s.kpart[k] = sum;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                ptrace_put(p, this_page, 2);
+                mbar_arrive_cnt(&s.empty[slot], my_arrivals);
+            }
+        }
+    }
+    if (tid == 0) trace_put(p, ii, 7);
+    if (consumer_any(bad)) return false;
+    mv_store_bc(p, s, ins, ii, mv.ws, best, best_idx);
     return true;
 }
 
@@ -2149,6 +2303,21 @@ __device__ bool consumer_step(const KParams &p, Smem &s, uint8_t *pages, const I
         bool ok;
         if (ins.op == OP_ATTN) {
             ok = attn_instr<FLASH, TC>(p, s, pages, ins, i, cpage);
+        } else if constexpr (TC && GEO == GEO_BCC) {
+            // two sequences on CUDA-core pages (the host launches this kernel only
+            // for the geometries mv_shape_bc gives)
+            const MvShape &mv = mv_of(p, ins.op);
+            switch (mv.vpl * 16 + mv.rw) {
+                case 2 * 16 + 8: ok = mv_instr_bc<2, 8>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                case 2 * 16 + 2: ok = mv_instr_bc<2, 2>(p, s, pages, ins, i, cpage, best, best_idx); break;
+                default: ok = false; raise_status(p, s, LL_ERR_SHAPE); break;
+            }
+            if (ok && ins.op == OP_LMHEAD && ins.sub) {
+                // lm_finish_b's scratch (s.xin) overlaps the partials the epilogue
+                // was reading: every thread is past them first
+                consumer_sync();
+                lm_finish_b(p, s, best, best_idx);
+            }
         } else if constexpr (TC) {
             // every width has tensor-core geometry here (the host launches this
             // kernel only then)

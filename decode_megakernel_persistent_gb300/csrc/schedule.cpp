@@ -101,7 +101,16 @@ bool mv_shape_tc(int K, MvShape &m) {
     return true;
 }
 
-bool mv_shape(int K, MvShape &m, int lane_floats) {
+static bool mv_shape_with(int K, MvShape &m, int lane_floats, int max_vpl, bool (*combo_ok)(int, int));
+
+bool mv_shape(int K, MvShape &m, int lane_floats) { return mv_shape_with(K, m, lane_floats, MAX_VPL, mv_combo_ok); }
+
+// (vpl, rw) pairs the two-sequence CUDA-core kernel is compiled for.
+static bool bc_combo_ok(int vpl, int rw) { return vpl == 2 && (rw == 8 || rw == 2); }
+
+bool mv_shape_bc(int K, MvShape &m) { return mv_shape_with(K, m, 16, 2, bc_combo_ok); }
+
+static bool mv_shape_with(int K, MvShape &m, int lane_floats, int max_vpl, bool (*combo_ok)(int, int)) {
     if (K <= 0 || K % 256 != 0 || K > 16384) return false;
     const int rows_fit = PAGE_BYTES / (2 * K);
     if (rows_fit < 1) return false;
@@ -109,7 +118,7 @@ bool mv_shape(int K, MvShape &m, int lane_floats) {
     while (teams < 4 && K * teams * 2 <= lane_floats * 32 * NCW) teams *= 2;
     const int W = NCW / teams;
     int best_active = 0, best_rpp = 0;
-    for (int vpl = 1; vpl <= MAX_VPL; vpl++) {
+    for (int vpl = 1; vpl <= max_vpl; vpl++) {
         if (K % (256 * vpl) != 0) continue;
         const int ws = K / (256 * vpl);
         if (ws > W) continue;
@@ -118,7 +127,7 @@ bool mv_shape(int K, MvShape &m, int lane_floats) {
         int rw = 1;
         while (rw * 2 * rg <= rows_fit && rw * 2 <= 8) rw *= 2;
         const int rpp = rg * rw;
-        if (rpp > MAX_RPP || rpp * ws > MAX_PART || !mv_combo_ok(vpl, rw)) continue;
+        if (rpp > MAX_RPP || rpp * ws > MAX_PART || !combo_ok(vpl, rw)) continue;
         const int active = ws * rg;
         if (active > best_active || (active == best_active && rpp > best_rpp)) {
             best_active = active;

@@ -32,6 +32,7 @@ LL_Q_LAUNCHES_PER_STEP = 6
 LL_Q_SMEM_BYTES = 7
 LL_Q_TRACE_BYTES = 8
 LL_Q_MV_TC = 9
+LL_Q_BATCH_CC = 12
 LL_Q_BATCH = 10
 LL_MAX_BATCH = 8
 

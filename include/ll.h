@@ -226,6 +226,7 @@ int ll_set_trace(ll_handle *h, uint64_t *trace_dev, size_t bytes);
 #define LL_Q_TRACE_BYTES 8      /* size of the buffer ll_set_trace needs */
 #define LL_Q_BATCH 10           /* sequences a handle decodes together */
 #define LL_Q_MV_TC 9            /* matrix-vector widths on tensor-core pages: bit 0 hidden, bit 1 n_q*head_dim, bit 2 inter */
+#define LL_Q_BATCH_CC 12        /* 1: a batch of two on CUDA-core pages (each page read once for both sequences) */
 int ll_query(const ll_handle *h, int what, int64_t *value);
 
 /* Fault injection for tests (host side only; nothing faults on the device):

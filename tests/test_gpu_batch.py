@@ -18,6 +18,9 @@ pytestmark = pytest.mark.gpu
 # a shape whose every width is a multiple of 1024 (the batched kernel's pages):
 # hidden 1024 (one chunk), n_q*head_dim 1024, inter 3072 (three chunks), GQA 4:1
 SMALL = synth.ModelShape("h1024", 2, 1024, 16, 4, 64, 3072, 4096, True)
+# the same with inter 2048: every width has two-sequence CUDA-core geometry, so a
+# batch of two runs on CUDA-core pages
+SMALL_CC = synth.ModelShape("h1024i2048", 2, 1024, 16, 4, 64, 2048, 4096, True)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,7 +35,7 @@ def _i32(vals):
     return torch.tensor(vals, dtype=torch.int32, device="cuda")
 
 
-def run_batch(shape, n, fills, n_steps, seed=0, jitter=0.0, tok0=None):
+def run_batch(shape, n, fills, n_steps, seed=0, jitter=0.0, tok0=None, expect_cc=None):
     """n sequences whose caches hold N(0,1) entries for their first fills[b]
     positions; one launch of n_steps steps from position fills[b]. Returns the
     oracles (fed the kernel's tokens), tokens [n_steps][n], logits [n_steps][n][V]."""
@@ -49,7 +52,11 @@ def run_batch(shape, n, fills, n_steps, seed=0, jitter=0.0, tok0=None):
         o.v_cache[...] = synth.to_host_bits(v)
         orcs.append(o)
     dec = ll.BatchDecoder(shape, w, ks, vs, max_seq)
-    assert dec.query(ll.LL_Q_BATCH) == n and dec.query(ll.LL_Q_MV_TC) == 7
+    # tensor-core pages, or (two sequences whose widths allow it) CUDA-core pages
+    assert dec.query(ll.LL_Q_BATCH) == n
+    assert dec.query(ll.LL_Q_MV_TC) == 7 or (n == 2 and dec.query(ll.LL_Q_BATCH_CC) == 1)
+    if expect_cc is not None:
+        assert dec.query(ll.LL_Q_BATCH_CC) == int(expect_cc)
     first = tok0 if tok0 is not None else synth.make_tokens(shape.vocab, n, seed=3)
     logits = torch.full((n_steps, n, shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
     toks = torch.zeros((n_steps, n), dtype=torch.int32, device="cuda")
@@ -176,3 +183,33 @@ def test_batch_argument_checks():
     with pytest.raises(ll.LLError) as e:
         ll.BatchDecoder(tiny, wt, [x[0] for x in kt], [x[1] for x in kt], 16)
     assert e.value.code == ll.LL_ERR_SHAPE
+
+
+def test_batch_of_two_on_cuda_core_pages_every_step():
+    # each page read once for both sequences; the sequences at different positions
+    fills = [70, 190]
+    orcs, first, out = run_batch(SMALL_CC, 2, fills, 8, jitter=0.25, expect_cc=True)
+    check_against_oracles(orcs, first, out, fills, 8, "cuda-core batch 2")
+
+
+def test_batch_of_two_on_cuda_core_pages_from_empty_and_per_warp(monkeypatch):
+    orcs, first, out = run_batch(SMALL_CC, 2, [0, 0], 12, expect_cc=True)
+    check_against_oracles(orcs, first, out, [0, 0], 12, "cuda-core batch 2 from empty")
+    monkeypatch.setenv("LL_ATTN_FLASH", "1")
+    fills = [300, 213]
+    orcs, first, out = run_batch(SMALL_CC, 2, fills, 4, expect_cc=True)
+    check_against_oracles(orcs, first, out, fills, 4, "cuda-core batch 2, per-warp attention")
+
+
+def test_batch_of_two_tensor_core_pages_on_request(monkeypatch):
+    monkeypatch.setenv("LL_BATCH_CC", "0")
+    fills = [70, 190]
+    orcs, first, out = run_batch(SMALL_CC, 2, fills, 3, expect_cc=False)
+    check_against_oracles(orcs, first, out, fills, 3, "tensor-core batch 2")
+
+
+def test_batch_llama1b_two_sequences_on_cuda_core_pages():
+    shape, ctx = synth.LLAMA_1B, 1024
+    fills = [ctx, ctx - 300]
+    orcs, first, out = run_batch(shape, 2, fills, 3, expect_cc=True)
+    check_against_oracles(orcs, first, out, fills, 3, "1b cuda-core batch 2")
