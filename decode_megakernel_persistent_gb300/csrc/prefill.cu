@@ -42,7 +42,13 @@ constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A a
 // A pipeline stage holds one K step of every A term and every B operand (the B
 // tile is loaded once for the three terms): 64 KB with one B operand, 80 KB with
 // two; as many stages as fit the 227 KB a block may have.
-__host__ __device__ constexpr int gstages(int nb) { return nb == 2 ? 2 : 3; }
+__host__ __device__ constexpr int gstages(int tiles) { return 196608 / (tiles * int(GTILE)); }  // tiles per stage
+// The A terms a GEMM takes: three for the Q, K, V projection (its K/V are the
+// cache entries the decode steps read, rounded to bf16, so they follow the fp32
+// input to its last bit), two for the others (16 of the 24 mantissa bits: their
+// outputs feed the residual stream and the MLP, whose parity bar is 1e-2 of the
+// logits; the two-term input is within 2^-17 of the fp32 one).
+__host__ __device__ constexpr int gterms(int epi) { return epi == 0 ? 3 : 2; }
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -131,8 +137,9 @@ struct GemmArgs {
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
-    constexpr int GSTAGES = gstages(NB);
-    constexpr uint32_t STAGE = GTILE * (NTERMS + NB);
+    constexpr int NT = gterms(EPI);                 // A terms
+    constexpr int GSTAGES = gstages(NT + NB);
+    constexpr uint32_t STAGE = GTILE * (NT + NB);
     constexpr uint32_t TCOLS = 128 * NB;
     extern __shared__ __align__(1024) uint8_t gsm[];
     uint8_t *tiles = gsm;
@@ -178,12 +185,12 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             const int kc = it * GK;
             const uint32_t dst = saddr(tiles + size_t(s) * STAGE);
 #pragma unroll
-            for (int q = 0; q < NTERMS; q++) tma2d(dst + q * GTILE, &g.a[q], kc, m0, &full[s]);
+            for (int q = 0; q < NT; q++) tma2d(dst + q * GTILE, &g.a[q], kc, m0, &full[s]);
             if (NB == 2) {
-                tma2d(dst + NTERMS * GTILE, &g.b[0], kc, n0, &full[s]);
-                tma2d(dst + (NTERMS + 1) * GTILE, &g.b[1], kc, n0, &full[s]);
+                tma2d(dst + NT * GTILE, &g.b[0], kc, n0, &full[s]);
+                tma2d(dst + (NT + 1) * GTILE, &g.b[1], kc, n0, &full[s]);
             } else {
-                tma2d(dst + NTERMS * GTILE, &g.b[bsel], kc, brow, &full[s]);
+                tma2d(dst + NT * GTILE, &g.b[bsel], kc, brow, &full[s]);
             }
             sent++;
         }
@@ -202,11 +209,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t base = saddr(tiles + size_t(s) * STAGE);
 #pragma unroll
-            for (int q = 0; q < NTERMS; q++) {
+            for (int q = 0; q < NT; q++) {
                 const uint64_t ad = smem_desc_sw128(base + q * GTILE);
 #pragma unroll
                 for (int nb = 0; nb < NB; nb++) {
-                    const uint64_t bd = smem_desc_sw128(base + GTILE * (NTERMS + nb));
+                    const uint64_t bd = smem_desc_sw128(base + GTILE * (NT + nb));
 #pragma unroll
                     for (int kk = 0; kk < GK / 16; kk++) {
                         const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
@@ -271,7 +278,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
                     cp[q] = v;
                 }
             } else {
-                uint32_t w[NTERMS][8];
+                constexpr int NW = gterms(EPI_ADD);  // the down GEMM's terms
+                uint32_t w[NW][8];
 #pragma unroll
                 for (int j = 0; j < 16; j += 2) {
                     float a2[2];
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
                         a2[e] = z / (1.0f + expf(-z)) * __uint_as_float(u[j + e]);
                     }
 #pragma unroll
-                    for (int q = 0; q < NTERMS; q++) {
+                    for (int q = 0; q < NW; q++) {
                         const __nv_bfloat162 t2 = __floats2bfloat162_rn(a2[0], a2[1]);
                         w[q][j / 2] = *reinterpret_cast<const uint32_t *>(&t2);
                         a2[0] -= __low2float(t2);
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
                 }
                 if (whole) {
 #pragma unroll
-                    for (int q = 0; q < NTERMS; q++) {
+                    for (int q = 0; q < NW; q++) {
                         uint4 *dst = reinterpret_cast<uint4 *>(g.act[q] + at);
                         dst[0] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
                         dst[1] = make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]);
@@ -656,7 +664,7 @@ template <int EPI>
 int gemm(const TensorMap *a, const TensorMap *bm, int nb, int s1, int s2, int M, int N, int K, float *c, int ldc,
          const Terms *act, const KParams &p, cudaStream_t st) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;
-    constexpr int SMEM = gstages(NB) * int(GTILE) * (NTERMS + NB) + 1024;
+    constexpr int SMEM = gstages(gterms(EPI) + NB) * int(GTILE) * (gterms(EPI) + NB) + 1024;
     static_assert(SMEM <= 232448, "stages fit in shared memory");
     GemmArgs g;
     for (int q = 0; q < NTERMS; q++) {

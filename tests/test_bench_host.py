@@ -94,3 +94,10 @@ def test_clock_summary_reads_samples_inside_the_timed_region(monkeypatch):
     assert r["sm_mhz"] == 2070
     assert r["sm_max_mhz"] == 2070
     assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_prefill_tensor_flops_count_each_gemms_terms():
+    from decode_megakernel_persistent_gb300 import synth
+    H, q, kv, I, L, n = 2048, 2048, 512, 8192, 16, 1024
+    want = 2.0 * n * L * (3 * (q * H + 2 * kv * H) + 2 * (H * q + 2 * I * H + H * I))
+    assert bench.prefill_tensor_flops(synth.LLAMA_1B, n) == want
