@@ -166,13 +166,19 @@ int ll_prefill(ll_handle *h, const int32_t *tokens_dev, int32_t n, int32_t pos0,
  * (its paragraph on CUDA-core against tensor-core matvec), so these handles run
  * the tensor-core kernel: each weight page is multiplied with all sequences'
  * inputs in the same m16n8k16 products, while every sequence keeps its own KV
- * cache, position, attention items, logits and greedy tokens.
+ * cache, position, attention items, logits and greedy tokens. Two sequences
+ * whose widths give at most 16 input floats per sequence and lane (hidden,
+ * n_q_heads*head_dim and inter of 1024, 2048 or 8192) run on CUDA-core pages
+ * instead, each page multiplied with both inputs (measured faster; the
+ * environment variable LL_BATCH_CC=0 at ll_init_batch keeps tensor-core pages;
+ * ll_query LL_Q_BATCH_CC reports which).
  *
  * ll_init_batch: as ll_init, with k_caches / v_caches host arrays of n_seq
  * device pointers, one cache pair per sequence, each laid out as ll_init's
- * (caller-owned, 16-byte aligned). Needs hidden, n_q_heads*head_dim and inter
- * multiples of 1024, the megakernel backend, and rows per SM x n_seq within the
- * kernel's accumulator (LL_ERR_SHAPE otherwise); attention uses the block-wide
+ * (caller-owned, 16-byte aligned). Needs the two-sequence CUDA-core widths
+ * above, or hidden, n_q_heads*head_dim and inter multiples of 1024, the
+ * megakernel backend, and rows per SM x n_seq within the kernel's accumulator
+ * (LL_ERR_SHAPE otherwise); attention uses the block-wide
  * softmax variant and about max_seq / 128 KV splits, at most n_sm / (n_kv *
  * n_seq). A batched handle is stepped only by ll_decode_steps_batch (the other
  * step calls return LL_ERR_ARG); ll_synchronize, ll_set_timeout_ns,
