@@ -213,3 +213,44 @@ def test_batch_llama1b_two_sequences_on_cuda_core_pages():
     fills = [ctx, ctx - 300]
     orcs, first, out = run_batch(shape, 2, fills, 3, expect_cc=True)
     check_against_oracles(orcs, first, out, fills, 3, "1b cuda-core batch 2")
+
+
+@pytest.mark.parametrize("cc", [True, False])
+def test_batch_dropped_signal_times_out_and_recovers(cc, monkeypatch):
+    # a gate/up instruction that stores its outputs with a tag no reader accepts:
+    # the launch reports a dependency timeout, and after the fault is removed the
+    # same steps run and match the oracles (CUDA-core and tensor-core pages)
+    if not cc:
+        monkeypatch.setenv("LL_BATCH_CC", "0")
+    shape, n, fills, steps = SMALL_CC, 2, [30, 57], 3
+    max_seq = max(fills) + steps + 1
+    w = synth.make_weights(shape, seed=0, device="cuda")
+    wh = synth.weights_to_host_bits(w)
+    ks, vs, orcs = [], [], []
+    for b in range(n):
+        k, v = synth.make_kv(shape, max_seq, fills[b], seed=10 + b, device="cuda")
+        ks.append(k)
+        vs.append(v)
+        o = oracle.OracleModel(shape.as_dict(), wh, max_seq, prec=32)
+        o.k_cache[...] = synth.to_host_bits(k)
+        o.v_cache[...] = synth.to_host_bits(v)
+        orcs.append(o)
+    dec = ll.BatchDecoder(shape, w, ks, vs, max_seq)
+    assert dec.query(ll.LL_Q_BATCH_CC) == int(cc)
+    first = synth.make_tokens(shape.vocab, n, seed=3)
+    toks = torch.zeros((steps, n), dtype=torch.int32, device="cuda")
+    ll.ll_set_timeout_ns(dec.handle, 20_000_000)  # 20 ms
+    ll.ll_debug_inject(dec.handle, ll.LL_FAULT_DROP_SIGNAL, 1, ll.OP_GATEUP)
+    dec.steps_batch(_i32(first), list(fills), 1, None, toks[:1])
+    with pytest.raises(ll.LLError) as e:
+        dec.synchronize()
+    assert e.value.code == ll.LL_ERR_DEP_TIMEOUT
+    ll.ll_debug_inject(dec.handle, ll.LL_FAULT_NONE)
+    ll.ll_set_timeout_ns(dec.handle, 1_000_000_000)
+    logits = torch.full((steps, n, shape.vocab), float("nan"), dtype=torch.float32, device="cuda")
+    dec.steps_batch(_i32(first), list(fills), steps, logits, toks)
+    dec.synchronize()
+    out = (toks.cpu().numpy(), logits.cpu().numpy(), [synth.to_host_bits(k) for k in ks],
+           [synth.to_host_bits(v) for v in vs])
+    dec.close()
+    check_against_oracles(orcs, first, out, fills, steps, f"after a dropped signal (cc={cc})")
