@@ -6,10 +6,10 @@
 // the weight matrix, filling the KV cache for the decode steps that follow.
 // Here every projection is a tcgen05 GEMM (the fifth-generation tensor cores):
 // TMA brings 128 x 64 bf16 tiles of both operands into shared memory in the
-// 128-byte swizzle through a 4-stage mbarrier pipeline, one thread issues
-// tcgen05.mma (M = 128 positions, N = 128 outputs, K = 16 per instruction) into a
-// tensor-memory accumulator, and the four warps read it back with tcgen05.ld for
-// the epilogue. The decode path keeps activations in fp32; a bf16 product with
+// 128-byte swizzle through a 3- or 4-stage mbarrier pipeline, one thread issues
+// tcgen05.mma (M = 128 positions, N = 128 outputs or 256 for gate and up
+// together, K = 16 per instruction) into a tensor-memory accumulator, and eight
+// warps read it back with tcgen05.ld for the epilogue. The decode path keeps activations in fp32; a bf16 product with
 // one term of them misses the logits' bar (and with two, bf16 roundings of the
 // K/V written to the cache flip measurably more often than in fp32), so each
 // activation matrix enters as three bf16 terms (t0 = bf16(x), t1 = bf16(x - t0),
@@ -36,7 +36,7 @@
 namespace ll {
 namespace {
 
-constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 128;
+constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 256;
 constexpr int NTERMS = 3;  // bf16 terms of an activation
 constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A and B alike)
 // A pipeline stage holds one K step of every A term and every B operand (the B
@@ -131,16 +131,25 @@ struct GemmArgs {
 };
 
 // One 128 x 128 tile of C per block (EPI_GATEUP: the same tile of the gate and
-// the up products, two accumulators): warp 0 lane 0 feeds the pipeline with TMA,
-// warp 1 lane 0 issues the MMAs, all four warps run the epilogue (warp w owns
-// tensor-memory lanes, i.e. tile rows, 32 w .. 32 w + 31).
+// the up products, side by side in one 128 x 256 accumulator): warp 0 lane 0
+// feeds the pipeline with TMA, warp 1 lane 0 issues the MMAs, all eight warps run
+// the epilogue (warp w reads tensor-memory lanes, i.e. tile rows,
+// 32 (w % 4) .. 32 (w % 4) + 31, and half w / 4 of the tile's columns).
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
     constexpr int NT = gterms(EPI);                 // A terms
     constexpr int GSTAGES = gstages(NT + NB);
     constexpr uint32_t STAGE = GTILE * (NT + NB);
-    constexpr uint32_t TCOLS = 128 * NB;
+    // EPI_STORE and EPI_ADD run transposed: the weight tile is the MMA's A (128
+    // output columns as the accumulator's lanes) and terms 0 and 1, adjacent in
+    // the stage, are one 256-row B (accumulator columns: term 0's 128 positions,
+    // then term 1's); a third term is an N = 128 product of its own into columns
+    // 256..383. The epilogue adds the terms' sums. Per K step of 16: one N = 256
+    // product (and one N = 128) instead of two (three) N = 128 ones.
+    constexpr bool TRANS = EPI != EPI_GATEUP;
+    constexpr uint32_t TCOLS = TRANS ? (NT == 2 ? 256 : 512) : 128 * NB;
+    static_assert(!TRANS || NT == 2 || NT == 3, "the transposed product takes two or three terms");
     extern __shared__ __align__(1024) uint8_t gsm[];
     uint8_t *tiles = gsm;
     uint64_t *full = reinterpret_cast<uint64_t *>(gsm + GSTAGES * STAGE);
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *err = 0;
     }
-    if (warp == 0) {  // fp32 columns of tensor memory: one 128 x 128 accumulator per B operand
+    if (warp == 0) {  // fp32 columns of tensor memory: TCOLS
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          saddr(const_cast<uint32_t *>(tmem_slot))),
                      "n"(TCOLS)
@@ -202,25 +211,33 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             }
         }
     } else if (warp == 1 && lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16(GM, GN);
+        // gate/up: the two B tiles sit one after the other in the stage, so one
+        // N = 256 product covers both (rows 128.. of the operand are the up tile)
+        constexpr uint32_t idesc = TRANS ? idesc_bf16(GN, 2 * GM) : idesc_bf16(GM, GN * NB);
+        constexpr uint32_t idesc3 = idesc_bf16(GN, GM);  // TRANS: the third term
         for (int it = 0; it < iters; it++) {
             const int s = it % GSTAGES;
             if (!mbar_wait(&full[s], (it / GSTAGES) & 1, g.timeout_ns, g.status, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t base = saddr(tiles + size_t(s) * STAGE);
 #pragma unroll
-            for (int q = 0; q < NT; q++) {
-                const uint64_t ad = smem_desc_sw128(base + q * GTILE);
+            for (int q = 0; q < (TRANS ? 1 : NT); q++) {
+                const uint64_t ad = smem_desc_sw128(TRANS ? base + GTILE * NT : base + q * GTILE);
+                const uint64_t bd = smem_desc_sw128(TRANS ? base : base + GTILE * NT);
 #pragma unroll
-                for (int nb = 0; nb < NB; nb++) {
-                    const uint64_t bd = smem_desc_sw128(base + GTILE * (NT + nb));
-#pragma unroll
-                    for (int kk = 0; kk < GK / 16; kk++) {
-                        const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
+                for (int kk = 0; kk < GK / 16; kk++) {
+                    const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                        "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
+                        : "memory");
+                    if (TRANS && NT == 3) {
+                        const uint64_t b3 = smem_desc_sw128(base + 2 * GTILE);
                         asm volatile(
                             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + uint32_t(128 * nb)),
-                            "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + 2u * GM),
+                            "l"(ad + uint64_t(2 * kk)), "l"(b3 + uint64_t(2 * kk)), "r"(idesc3), "r"(acc)
                             : "memory");
                     }
                 }
@@ -237,11 +254,12 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     __syncwarp();
     const bool ok = mbar_wait(done, 0, g.timeout_ns, g.status, err) && !*err;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int row = m0 + warp * 32 + lane;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = m0 + quarter * 32 + lane;
     // (the wait is in the same statement as the load, so no use of the
     // registers can be placed before it)
     auto ld16 = [&](uint32_t col, uint32_t (&r)[16]) {
-        const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + col;
+        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + col;
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
             "%14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
@@ -250,9 +268,35 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             : "r"(taddr)
             : "memory");
     };
-    if (ok) {
+    if (ok && TRANS) {
+        // lane: output column n0 + 32 quarter + lane; columns of the accumulator:
+        // positions (term 0 at c, term 1 at 128 + c, term 2 at 256 + c), this
+        // warp's half of them
+        const int col = n0 + quarter * 32 + lane;
 #pragma unroll 1
-        for (int c0 = 0; c0 < GN; c0 += 16) {
+        for (int c0 = half * (GM / 2); c0 < (half + 1) * (GM / 2); c0 += 16) {
+            uint32_t r[16], u[16], w[16];
+            ld16(uint32_t(c0), r);
+            ld16(uint32_t(GM + c0), u);
+            if (NT == 3) ld16(uint32_t(2 * GM + c0), w);
+            if (col >= g.N) continue;
+            float *const cp = g.c + size_t(m0 + c0) * g.ldc + col;
+            float old[16];
+            if (EPI == EPI_ADD) {  // all 16 loads in flight before the first store
+#pragma unroll
+                for (int e = 0; e < 16; e++) old[e] = m0 + c0 + e < g.M ? cp[size_t(e) * g.ldc] : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                float v = __uint_as_float(r[e]) + __uint_as_float(u[e]);
+                if (NT == 3) v += __uint_as_float(w[e]);
+                if (EPI == EPI_ADD) v += old[e];
+                if (m0 + c0 + e < g.M) cp[size_t(e) * g.ldc] = v;
+            }
+        }
+    } else if (ok && !TRANS) {
+#pragma unroll 1
+        for (int c0 = half * (GN / 2); c0 < (half + 1) * (GN / 2); c0 += 16) {
             uint32_t r[16];
             ld16(uint32_t(c0), r);
             uint32_t u[16];
