@@ -63,30 +63,46 @@ __global__ void k_rmsnorm(const float *x, const uint16_t *g, int n, float eps, f
     for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = x[i] * r * bf(g[i]);
 }
 
-// out[r] (+)= W[r] . in, one warp per row, 16-byte streaming loads of W.
+// 16 bytes of a weight row, streamed past L1 (no side effects: the compiler may
+// batch these loads ahead of their uses).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 u;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+        : "l"(p));
+    return u;
+}
+
+// out[r] (+)= W[r] . in, one warp per row, 16-byte streaming loads of W: up to
+// 8 per lane (a 2048-wide row) in flight before the first product.
 __global__ void k_matvec(const uint16_t *__restrict__ W, const float *__restrict__ in, int rows, int K,
                          float *out, int accumulate) {
+    constexpr int U = 8;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int nvec = K / 8;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
         const uint4 *w = reinterpret_cast<const uint4 *>(W + size_t(r) * K);
         float a0 = 0.f, a1 = 0.f;
-        for (int v = lane; v < nvec; v += 32) {
-            uint4 u;
-            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                         : "l"(w + v));
-            const float4 xa = reinterpret_cast<const float4 *>(in)[2 * v];
-            const float4 xb = reinterpret_cast<const float4 *>(in)[2 * v + 1];
-            a0 = fmaf(__uint_as_float(u.x << 16), xa.x, a0);
-            a1 = fmaf(__uint_as_float(u.x & 0xffff0000u), xa.y, a1);
-            a0 = fmaf(__uint_as_float(u.y << 16), xa.z, a0);
-            a1 = fmaf(__uint_as_float(u.y & 0xffff0000u), xa.w, a1);
-            a0 = fmaf(__uint_as_float(u.z << 16), xb.x, a0);
-            a1 = fmaf(__uint_as_float(u.z & 0xffff0000u), xb.y, a1);
-            a0 = fmaf(__uint_as_float(u.w << 16), xb.z, a0);
-            a1 = fmaf(__uint_as_float(u.w & 0xffff0000u), xb.w, a1);
+        for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+            uint4 u[U];
+#pragma unroll
+            for (int j = 0; j < U; j++) u[j] = v0 + 32 * j < nvec ? ld_stream(w + v0 + 32 * j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int j = 0; j < U; j++) {
+                const int v = v0 + 32 * j;
+                if (v >= nvec) break;
+                const float4 xa = reinterpret_cast<const float4 *>(in)[2 * v];
+                const float4 xb = reinterpret_cast<const float4 *>(in)[2 * v + 1];
+                a0 = fmaf(__uint_as_float(u[j].x << 16), xa.x, a0);
+                a1 = fmaf(__uint_as_float(u[j].x & 0xffff0000u), xa.y, a1);
+                a0 = fmaf(__uint_as_float(u[j].y << 16), xa.z, a0);
+                a1 = fmaf(__uint_as_float(u[j].y & 0xffff0000u), xa.w, a1);
+                a0 = fmaf(__uint_as_float(u[j].z << 16), xb.x, a0);
+                a1 = fmaf(__uint_as_float(u[j].z & 0xffff0000u), xb.y, a1);
+                a0 = fmaf(__uint_as_float(u[j].w << 16), xb.z, a0);
+                a1 = fmaf(__uint_as_float(u[j].w & 0xffff0000u), xb.w, a1);
+            }
         }
         const float y = wsum(a0 + a1);
         if (lane == 0) out[r] = accumulate ? out[r] + y : y;
@@ -226,16 +242,42 @@ __global__ void k_silu_mul(const float *g, const float *u, float *a, int n) {
 
 // One block: greedy argmax, lowest index on ties. Logits that hold no orderable
 // value (all NaN) have no greedy token: the status word records LL_ERR_NUMERIC.
+// Greedy token: the smallest index holding the largest logit (NaNs never win;
+// all NaN is an error). One block: each thread keeps U running (max, index)
+// pairs over float4 groups i, i + 4 blockDim, ... so that U loads are in flight.
+__device__ __forceinline__ void argmax_take(float v, int i, float &best, int &idx) {
+    if (v > best || (v == best && best > -INFINITY && i < idx)) {
+        best = v;
+        idx = i;
+    }
+}
+
 __global__ void k_argmax(const float *v, int n, int32_t *next_dev, int32_t *token_out, int32_t *status) {
+    constexpr int U = 4;
     __shared__ float bv[32];
     __shared__ int bi[32];
     float best = -INFINITY;
     int idx = 0x7fffffff;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        if (v[i] > best) {
-            best = v[i];
-            idx = i;
+    const int n4 = n / 4, step = int(blockDim.x);
+    const float4 *v4 = reinterpret_cast<const float4 *>(v);
+    if ((reinterpret_cast<uintptr_t>(v) & 15u) != 0) {  // (unaligned: plain loads)
+        for (int i = threadIdx.x; i < n; i += step) argmax_take(v[i], i, best, idx);
+    } else {
+        for (int g0 = threadIdx.x; g0 < n4; g0 += U * step) {
+            float4 x[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) x[u] = g0 + u * step < n4 ? v4[g0 + u * step] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                if (g0 + u * step >= n4) break;
+                const int i = 4 * (g0 + u * step);
+                argmax_take(x[u].x, i, best, idx);
+                argmax_take(x[u].y, i + 1, best, idx);
+                argmax_take(x[u].z, i + 2, best, idx);
+                argmax_take(x[u].w, i + 3, best, idx);
+            }
         }
+        for (int i = 4 * n4 + int(threadIdx.x); i < n; i += step) argmax_take(v[i], i, best, idx);
     }
     for (int o = 16; o > 0; o >>= 1) {
         const float ob = __shfl_xor_sync(0xffffffffu, best, o);

@@ -383,51 +383,91 @@ struct Terms {
 };
 
 // One block per position: h = x / sqrt(mean(x^2) + eps) * g as NTERMS bf16 terms.
+// Thread j holds elements 8j .. 8j + 7 (H a multiple of 8, blockDim >= H / 8):
+// one 32-byte read of x, 16-byte writes of each term.
 __global__ void k_pf_norm_split(const float *x, const uint16_t *g, int H, float eps, Terms h) {
     __shared__ float red[32];
+    const int i0 = 8 * int(threadIdx.x);
+    const bool on = i0 < H;
     const float *xr = x + size_t(blockIdx.x) * H;
+    float v[8];
+    if (on) {
+        const float4 a = *reinterpret_cast<const float4 *>(xr + i0), b = *reinterpret_cast<const float4 *>(xr + i0 + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; e++) v[e] = 0.f;
+    }
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+#pragma unroll
+    for (int e = 0; e < 8; e++) ss = fmaf(v[e], v[e], ss);
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (threadIdx.x == 0) red[0] = v;
+        float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) red[0] = t;
     }
     __syncthreads();
+    if (!on) return;
     const float r = 1.0f / sqrtf(red[0] / float(H) + eps);
-    for (int i = threadIdx.x; i < H; i += blockDim.x)
-        put_terms(xr[i] * r * __uint_as_float(uint32_t(g[i]) << 16), h.t, size_t(blockIdx.x) * H + i);
+    const uint4 gw = *reinterpret_cast<const uint4 *>(g + i0);
+    const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+    for (int e = 0; e < 8; e++) v[e] = v[e] * r * __uint_as_float(e & 1 ? gg[e / 2] & 0xffff0000u : gg[e / 2] << 16);
+    const size_t at = size_t(blockIdx.x) * H + i0;
+#pragma unroll
+    for (int q = 0; q < NTERMS; q++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[e], v[e + 1]);
+            w[e / 2] = *reinterpret_cast<const uint32_t *>(&b2);
+            v[e] -= __low2float(b2);
+            v[e + 1] -= __high2float(b2);
+        }
+        *reinterpret_cast<uint4 *>(h.t[q] + at) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 // One block per position t: RoPE ("rotate half") on its q heads in place and on
 // its k heads, k and v rounded to bf16 (nearest even) into the cache at pos0 + t.
+// A thread takes four consecutive pairs (i, i + hd / 2) of a head: 16-byte loads
+// and stores of q, 8-byte stores into the cache.
+__device__ __forceinline__ uint2 bf16x4(float a, float b, float c, float d) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+
 __global__ void k_pf_rope_kv(float *qkv, const float2 *rope, int pos0, int nq, int nkv, int hd, uint16_t *kc,
                              uint16_t *vc, size_t layer_base, int max_seq) {
-    const int t = blockIdx.x, half = hd / 2, pos = pos0 + t;
+    const int t = blockIdx.x, half = hd / 2, quads = half / 4, pos = pos0 + t;
     const int qd = nq * hd, kd = nkv * hd;
     float *row = qkv + size_t(t) * (qd + 2 * kd);
-    const float2 *c = rope + size_t(pos) * half;
-    for (int u = threadIdx.x; u < (nq + nkv) * half; u += blockDim.x) {
-        const int h = u / half, i = u % half;
+    const float4 *c = reinterpret_cast<const float4 *>(rope + size_t(pos) * half);  // two (cos, sin) per float4
+    for (int u = threadIdx.x; u < (nq + nkv) * quads; u += blockDim.x) {
+        const int h = u / quads, i = 4 * (u % quads);
         float *v = row + size_t(h) * hd;  // heads 0..nq-1 are q, then k
-        const float a = v[i], b = v[i + half];
-        const float ra = a * c[i].x - b * c[i].y, rb = a * c[i].y + b * c[i].x;
+        const float4 a = *reinterpret_cast<const float4 *>(v + i), b = *reinterpret_cast<const float4 *>(v + i + half);
+        const float4 c01 = c[i / 2], c23 = c[i / 2 + 1];
+        const float4 ra = make_float4(a.x * c01.x - b.x * c01.y, a.y * c01.z - b.y * c01.w, a.z * c23.x - b.z * c23.y,
+                                      a.w * c23.z - b.w * c23.w);
+        const float4 rb = make_float4(a.x * c01.y + b.x * c01.x, a.y * c01.w + b.y * c01.z, a.z * c23.y + b.z * c23.x,
+                                      a.w * c23.w + b.w * c23.z);
         if (h < nq) {
-            v[i] = ra;
-            v[i + half] = rb;
+            *reinterpret_cast<float4 *>(v + i) = ra;
+            *reinterpret_cast<float4 *>(v + i + half) = rb;
         } else {
             const size_t dst = layer_base + (size_t(h - nq) * max_seq + pos) * hd;
-            kc[dst + i] = __bfloat16_as_ushort(__float2bfloat16_rn(ra));
-            kc[dst + i + half] = __bfloat16_as_ushort(__float2bfloat16_rn(rb));
+            *reinterpret_cast<uint2 *>(kc + dst + i) = bf16x4(ra.x, ra.y, ra.z, ra.w);
+            *reinterpret_cast<uint2 *>(kc + dst + i + half) = bf16x4(rb.x, rb.y, rb.z, rb.w);
         }
     }
-    for (int u = threadIdx.x; u < kd; u += blockDim.x) {
+    for (int u = 4 * int(threadIdx.x); u < kd; u += 4 * int(blockDim.x)) {
         const int g = u / hd, d = u % hd;
-        vc[layer_base + (size_t(g) * max_seq + pos) * hd + d] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(row[qd + kd + u]));
+        const float4 x = *reinterpret_cast<const float4 *>(row + qd + kd + u);
+        *reinterpret_cast<uint2 *>(vc + layer_base + (size_t(g) * max_seq + pos) * hd + d) = bf16x4(x.x, x.y, x.z, x.w);
     }
 }
 
@@ -923,6 +963,7 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         to.t[q] = b.o[q];
         ta.t[q] = b.a[q];
     }
+    const int norm_threads = (H / 8 + 31) / 32 * 32;  // a thread per 8 elements of a row (H <= 8192)
     k_pf_embed<<<n, 256, 0, st>>>(p.embed, tokens_dev, n, H, p.V, b.x, p.status);
     int rc = cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
     for (int l = 0; l < p.L && rc == LL_OK; l++) {
@@ -930,7 +971,7 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         const TensorMap *m = &b.m_w[size_t(l) * 7];
         const size_t lb = size_t(l) * per_layer;
         const int ld = qd + 2 * kd;
-        k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.attn_norm, H, p.eps, th);
+        k_pf_norm_split<<<n, norm_threads, 0, st>>>(b.x, w.attn_norm, H, p.eps, th);
         if (qd % GN == 0 && kd % GN == 0) {  // q, k and v in one GEMM over the stacked rows
             rc = gemm<EPI_STORE>(b.m_h, m, 3, qd, qd + kd, n, ld, H, b.qkv, ld, nullptr, p, st);
         } else {
@@ -943,7 +984,7 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         rc = launch_attention(p, b, l, pos0, n, to, st);
         if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m + 3, 1, 0, 0, n, H, qd, b.x, H, nullptr, p, st);
         if (rc != LL_OK) break;
-        k_pf_norm_split<<<n, 256, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
+        k_pf_norm_split<<<n, norm_threads, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
         // gate and up in one GEMM (two accumulators), silu(gate) * up as terms
         rc = gemm<EPI_GATEUP>(b.m_h, m + 4, 2, 0, 0, n, I, H, nullptr, I, &ta, p, st);
         if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m + 6, 1, 0, 0, n, H, I, b.x, H, nullptr, p, st);
