@@ -714,8 +714,6 @@ int ll_prefill(ll_handle *h, const int32_t *tokens_dev, int32_t n, int32_t pos0,
     if (logits_dev && !aligned16(logits_dev)) return fail(h, LL_ERR_ARG, "logits buffer not 16-byte aligned");
     if (h->cfg.hidden % 64 || (h->cfg.n_q_heads * h->cfg.head_dim) % 64 || h->cfg.inter % 64)
         return fail(h, LL_ERR_SHAPE, "prefill needs hidden, n_q_heads*head_dim and inter multiples of 64");
-    if (h->cfg.hidden > 8192 || h->cfg.head_dim % 8)
-        return fail(h, LL_ERR_SHAPE, "prefill needs hidden <= 8192 and head_dim a multiple of 8");
     if (!ll::prefill_prepare(h->kp, h->host_layers.data(), n, h->pf))
         return fail(h, LL_ERR_OOM, "prefill buffers for " + std::to_string(n) + " positions could not be made");
     const int rc = ll::launch_prefill(h->kp, h->host_layers.data(), h->pf, tokens_dev, n, pos0, logits_dev,

@@ -383,24 +383,56 @@ struct Terms {
 };
 
 // One block per position: h = x / sqrt(mean(x^2) + eps) * g as NTERMS bf16 terms.
-// Thread j holds elements 8j .. 8j + 7 (H a multiple of 8, blockDim >= H / 8):
-// one 32-byte read of x, 16-byte writes of each term.
+// Thread j takes the 8-element groups j, j + blockDim, ... (H a multiple of 8):
+// 32-byte reads of x, 16-byte writes of each term. A thread with one group (H
+// <= 8 blockDim, the usual launch) keeps it in registers between the two passes.
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// the normed group of 8 at i0 (x values v, gain g) as NTERMS bf16 terms
+__device__ __forceinline__ void norm_store8(const float (&v)[8], float r, const uint16_t *g, int i0, size_t at,
+                                            const Terms &h) {
+    const uint4 gw = *reinterpret_cast<const uint4 *>(g + i0);
+    const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) y[e] = v[e] * r * __uint_as_float(e & 1 ? gg[e / 2] & 0xffff0000u : gg[e / 2] << 16);
+#pragma unroll
+    for (int q = 0; q < NTERMS; q++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(y[e], y[e + 1]);
+            w[e / 2] = *reinterpret_cast<const uint32_t *>(&b2);
+            y[e] -= __low2float(b2);
+            y[e + 1] -= __high2float(b2);
+        }
+        *reinterpret_cast<uint4 *>(h.t[q] + at) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 __global__ void k_pf_norm_split(const float *x, const uint16_t *g, int H, float eps, Terms h) {
     __shared__ float red[32];
-    const int i0 = 8 * int(threadIdx.x);
-    const bool on = i0 < H;
+    const int groups = H / 8, step = int(blockDim.x), j = int(threadIdx.x);
+    const bool single = groups <= step;
     const float *xr = x + size_t(blockIdx.x) * H;
     float v[8];
-    if (on) {
-        const float4 a = *reinterpret_cast<const float4 *>(xr + i0), b = *reinterpret_cast<const float4 *>(xr + i0 + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; e++) v[e] = 0.f;
-    }
     float ss = 0.f;
+    if (single) {
+        if (j < groups) {
+            load8(xr + 8 * j, v);
 #pragma unroll
-    for (int e = 0; e < 8; e++) ss = fmaf(v[e], v[e], ss);
+            for (int e = 0; e < 8; e++) ss = fmaf(v[e], v[e], ss);
+        }
+    } else {
+        for (int gi = j; gi < groups; gi += step) {
+            load8(xr + 8 * gi, v);
+#pragma unroll
+            for (int e = 0; e < 8; e++) ss = fmaf(v[e], v[e], ss);
+        }
+    }
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
@@ -410,24 +442,15 @@ __global__ void k_pf_norm_split(const float *x, const uint16_t *g, int H, float 
         if (threadIdx.x == 0) red[0] = t;
     }
     __syncthreads();
-    if (!on) return;
     const float r = 1.0f / sqrtf(red[0] / float(H) + eps);
-    const uint4 gw = *reinterpret_cast<const uint4 *>(g + i0);
-    const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
-#pragma unroll
-    for (int e = 0; e < 8; e++) v[e] = v[e] * r * __uint_as_float(e & 1 ? gg[e / 2] & 0xffff0000u : gg[e / 2] << 16);
-    const size_t at = size_t(blockIdx.x) * H + i0;
-#pragma unroll
-    for (int q = 0; q < NTERMS; q++) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[e], v[e + 1]);
-            w[e / 2] = *reinterpret_cast<const uint32_t *>(&b2);
-            v[e] -= __low2float(b2);
-            v[e + 1] -= __high2float(b2);
+    const size_t row = size_t(blockIdx.x) * H;
+    if (single) {
+        if (j < groups) norm_store8(v, r, g, 8 * j, row + 8 * j, h);
+    } else {
+        for (int gi = j; gi < groups; gi += step) {
+            load8(xr + 8 * gi, v);
+            norm_store8(v, r, g, 8 * gi, row + 8 * gi, h);
         }
-        *reinterpret_cast<uint4 *>(h.t[q] + at) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -963,7 +986,7 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         to.t[q] = b.o[q];
         ta.t[q] = b.a[q];
     }
-    const int norm_threads = (H / 8 + 31) / 32 * 32;  // a thread per 8 elements of a row (H <= 8192)
+    const int norm_threads = std::min(1024, (H / 8 + 31) / 32 * 32);  // a thread per 8 elements of a row
     k_pf_embed<<<n, 256, 0, st>>>(p.embed, tokens_dev, n, H, p.V, b.x, p.status);
     int rc = cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
     for (int l = 0; l < p.L && rc == LL_OK; l++) {

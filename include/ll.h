@@ -152,8 +152,8 @@ int ll_decode_steps(ll_handle *h, const int32_t *token_dev, int32_t pos, int32_t
  * bf16 terms, plus a causal attention (mma.sync tiles) over the cache entries
  * 0..pos0 + t of each position t. Asynchronous on the handle's stream; a token out of range is
  * reported by ll_synchronize (LL_ERR_ARG). Single-sequence handles only (LL_ERR_ARG
- * on a batched one); needs hidden, n_q_heads*head_dim and inter multiples of 64,
- * hidden <= 8192 and head_dim a multiple of 8 (LL_ERR_SHAPE). The first call, and any call with more positions than before,
+ * on a batched one); needs hidden, n_q_heads*head_dim and inter multiples of 64
+ * (LL_ERR_SHAPE). The first call, and any call with more positions than before,
  * allocates the prefill buffers (cudaMalloc, about n x (10 hidden + 10 q + 8 kv
  * + 6 inter) bytes plus the weight tensor maps; LL_ERR_OOM if that fails);
  * ll_free releases them. */
