@@ -1760,6 +1760,9 @@ __device__ bool consumer_step_begin_b(const KParams &p, Smem &s, int st) {
             }
             asm volatile("fence.acq_rel.gpu;" ::: "memory");
             s.btoken[b] = static_cast<int32_t>(static_cast<uint32_t>(w));
+            // a step without a greedy token (no orderable logit) hands on -1:
+            // stop here rather than index the embedding with it
+            if (s.btoken[b] < 0 || s.btoken[b] >= p.V) raise_status(p, s, LL_ERR_NUMERIC);
         }
     }
     if (consumer_any(s.abort)) return false;
@@ -2278,6 +2281,9 @@ __device__ bool consumer_step_begin(const KParams &p, Smem &s, int st) {
             }
             asm volatile("fence.acq_rel.gpu;" ::: "memory");
             s.token = static_cast<int32_t>(static_cast<uint32_t>(w));
+            // a step without a greedy token (no orderable logit) hands on -1:
+            // stop here rather than index the embedding with it
+            if (s.token < 0 || s.token >= p.V) raise_status(p, s, LL_ERR_NUMERIC);
             s.tok_step = st;
         }
     }

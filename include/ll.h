@@ -46,7 +46,8 @@ extern "C" {
 #define LL_ERR_DEP_TIMEOUT (-4)  /* a device-side wait ran past its time limit; the step was abandoned */
 #define LL_ERR_OOM (-5)          /* library scratch could not be allocated */
 #define LL_ERR_DEVICE (-6)       /* device is not sm_103 or cannot co-schedule one block per SM */
-#define LL_ERR_NUMERIC (-7)      /* the logits held no orderable value (all NaN): no greedy token */
+#define LL_ERR_NUMERIC (-7)      /* the logits held no orderable value (all NaN): no greedy token (the
+                                    token outputs read -1, and a multi-step launch stops there) */
 
 #define LL_BACKEND_MEGAKERNEL 0  /* one persistent kernel per decode step */
 #define LL_BACKEND_CHAIN 1       /* one kernel per operation, for comparison */
