@@ -487,9 +487,13 @@ __device__ __forceinline__ void load_gain(const KParams &p, const Smem &s, const
 // that each tagged word is read once per block whatever the number of teams;
 // wider ones (the down projection's) are read straight into the lanes. Returns
 // false, in every consumer thread alike, if a wait failed.
+// kbase: where the instruction's (row, k-slice) partials start in s.kpart (which
+// shares space with s.xin). Past the staged input when they fit there (one
+// sequence): a warp may then write its partials while others still read their
+// input, with no barrier between; else 0, behind a barrier.
 template <int VPL, bool BAT = false>
 __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const MvShape &mv,
-                           float (&xr)[VPL * 8], const uint4 (&gv)[VPL], int b = 0) {
+                           float (&xr)[VPL * 8], const uint4 (&gv)[VPL], int &kbase, int b = 0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int sw = mv.w_sw[warp];
     const bool normed = norm_gain(p, s, ins) != nullptr;
@@ -510,6 +514,12 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
     }
     if (BAT && src) src += size_t(b) * size_t(mv.K);  // sequence b's words (laid out sequence after sequence)
     const bool staged = src && mv.K <= XIN_FLOATS;
+    const int need = (ins.op == OP_GATEUP ? 2 : 1) * (ins.r1 - ins.r0) * mv.ws;
+    const bool apart = !BAT && staged && mv.K + need <= KPART_FLOATS;
+    kbase = apart ? mv.K : 0;
+    // per-warp sums of squares; a batch's sequences each have their own, so
+    // that the next sequence's input may be taken in while this one's are read
+    auto nred = [&](int w) -> float & { return BAT ? s.nredb[w][b] : s.nred[w]; };
     if (staged) {
         constexpr int PAIRS = XIN_FLOATS / (2 * NCT);
         uint64_t w[2 * PAIRS];
@@ -522,16 +532,25 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
                 else ww[2 * k] = ww[2 * k + 1] = static_cast<uint64_t>(tag) << 32;
             }
         });
+        // a normed input's sum of squares is taken here, each element once, so
+        // that the barrier publishing s.xin publishes the warps' sums as well
+        float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < PAIRS; k++) {
             const int i = (tid + k * NCT) * 2;
             if (i < K) {
-                s.xin[i] = tag_val(w[2 * k]);
-                s.xin[i + 1] = tag_val(w[2 * k + 1]);
+                const float a = tag_val(w[2 * k]), c = tag_val(w[2 * k + 1]);
+                s.xin[i] = a;
+                s.xin[i + 1] = c;
+                ss = fmaf(c, c, fmaf(a, a, ss));
             }
         }
+        if (normed) {
+            ss = warp_sum(ss);
+            if (lane == 0) nred(warp) = ss;
+        }
     }
-    if (staged && consumer_any(s.abort)) return false;  // also publishes s.xin
+    if (staged && consumer_any(s.abort)) return false;  // also publishes s.xin (and the sums)
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
         const int v = j * 32 * mv.ws + sw * 32 + lane;
@@ -572,21 +591,25 @@ __device__ bool load_input(const KParams &p, Smem &s, const Instr &ins, const Mv
     // (wide inputs: also every warp is done with its part of s.xin, which
     // s.kpart overlaps, before any team writes partial sums)
     if (!staged && src && consumer_any(s.abort)) return false;
-    if (!normed) {
-        // s.kpart shares space with s.xin: every warp holds its input before any
-        // team writes partial sums
-        if (staged) consumer_sync();
-        return true;
-    }
-    // RMSNorm: the warps w < ws together hold every element once.
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < VPL * 8; e++) ss = fmaf(xr[e], xr[e], ss);
-    ss = warp_sum(ss);
-    if (lane == 0 && warp < mv.ws) s.nred[warp] = ss;
-    consumer_sync();
+    // s.kpart shares space with s.xin: unless the partials go past the input,
+    // every warp holds its input before any team writes partial sums
+    if (staged && !apart) consumer_sync();
+    if (!normed) return true;
+    // RMSNorm. Staged: the NCW warps' sums of their staged elements. Else the
+    // warps w < ws together hold every element once in their registers.
     float tot = 0.f;
-    for (int w = 0; w < mv.ws; w++) tot += s.nred[w];
+    if (staged) {
+#pragma unroll
+        for (int w = 0; w < NCW; w++) tot += nred(w);
+    } else {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < VPL * 8; e++) ss = fmaf(xr[e], xr[e], ss);
+        ss = warp_sum(ss);
+        if (lane == 0 && warp < mv.ws) nred(warp) = ss;
+        consumer_sync();
+        for (int w = 0; w < mv.ws; w++) tot += nred(w);
+    }
     const float r = 1.0f / sqrtf(tot / static_cast<float>(mv.K) + p.eps);
 #pragma unroll
     for (int j = 0; j < VPL; j++) {
@@ -631,22 +654,22 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[R]) {
 // partial is in s.kpart: each row's sum of its ws k-slices, stored as q/k/v, the
 // residual stream, silu(gate) * up, or the logits and each thread's running
 // argmax. Inlined: as a called function it made the 1B step ~7 % slower (measured).
-__device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr &ins, int ii, int ws, float &best,
-                                         int &best_idx) {
+__device__ __forceinline__ void mv_store(const KParams &p, Smem &s, const Instr &ins, int ii, int ws, int kbase,
+                                         float &best, int &best_idx) {
     const int tid = threadIdx.x;
     const int nrows = ins.r1 - ins.r0;
     const int r0 = ins.r0;
     const uint32_t wtag = write_tag(p, s, ins);
     struct RowSum {  // the row's k-slices, summed in k-slice order
         const float *kp;
-        int ws;
+        int ws, kbase;
         __device__ float operator[](int t) const {
             float y = 0.f;
             for (int w = 0; w < ws; w++)
-                if (LL_OK_IDX(3, t * ws + w, KPART_FLOATS)) y += kp[t * ws + w];
+                if (LL_OK_IDX(3, kbase + t * ws + w, KPART_FLOATS)) y += kp[kbase + t * ws + w];
             return y;
         }
-    } acc{s.kpart, ws};
+    } acc{s.kpart, ws, kbase};
     switch (ins.op) {
         case OP_QKV:
             for (int t = tid; t < nrows; t += NCT)
@@ -700,7 +723,8 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     uint4 gv[VPL];
     load_gain<VPL>(p, s, ins, mv, gv);
     float xr[VPL * 8];
-    if (!load_input<VPL>(p, s, ins, mv, xr, gv)) return false;
+    int kbase;
+    if (!load_input<VPL>(p, s, ins, mv, xr, gv, kbase)) return false;
     if (threadIdx.x == 0) trace_put(p, ii, 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -771,8 +795,8 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
             // as soon as every active warp has read it (the k-slices are summed
             // once per instruction, below)
             const int r = rgi + (lane / GROUP) * mv.rg;
-            if ((lane % GROUP) == 0 && r < nr && LL_OK_IDX(2, (acc0 + pr + r) * mv.ws + sw, KPART_FLOATS))
-                s.kpart[(acc0 + pr + r) * mv.ws + sw] = sum;
+            if ((lane % GROUP) == 0 && r < nr && LL_OK_IDX(2, kbase + (acc0 + pr + r) * mv.ws + sw, KPART_FLOATS))
+                s.kpart[kbase + (acc0 + pr + r) * mv.ws + sw] = sum;
             __syncwarp();
             if (lane == 0) {
                 ptrace_put(p, this_page, 2);
@@ -782,7 +806,7 @@ __device__ bool mv_instr(const KParams &p, Smem &s, uint8_t *pages, const Instr 
     }
     if (tid == 0) trace_put(p, ii, 7);
     if (consumer_any(bad)) return false;  // else every k-slice of every row is in s.kpart
-    mv_store(p, s, ins, ii, mv.ws, best, best_idx);
+    mv_store(p, s, ins, ii, mv.ws, kbase, best, best_idx);
     return true;
 }
 
@@ -854,7 +878,8 @@ __device__ bool mv_instr_bc(const KParams &p, Smem &s, uint8_t *pages, const Ins
     for (int b = 0; b < NBC; b++) {
         uint4 gv[VPL];
         load_gain<VPL>(p, s, ins, mv, gv);
-        if (!load_input<VPL, true>(p, s, ins, mv, xr[b], gv, b)) return false;
+        int kbase;  // (0: a batched input is always behind a barrier)
+        if (!load_input<VPL, true>(p, s, ins, mv, xr[b], gv, kbase, b)) return false;
     }
     if (threadIdx.x == 0) trace_put(p, ii, 1);
 
