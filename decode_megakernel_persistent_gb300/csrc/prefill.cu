@@ -534,6 +534,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 constexpr int AT_NW = 8;      // consumer warps of an attention block
 constexpr int AT_STAGES = 4;  // tiles in flight
+// The running max of a row moves only once some row of the warp has grown past
+// it by more than this (log2 units): until then probabilities are taken against
+// the held max (each at most 2^8, well inside bf16 and fp32), the output needs
+// no rescaling, and o / l is the same quotient.
+constexpr float HOLD_LOG2 = 8.f;
 
 struct PfAttnArgs {
     TensorMap kmap, vmap;  // the caches, boxes of 16 rows x 64 columns, 128-byte swizzle
@@ -605,7 +610,8 @@ __global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_co
     const int t = t_base + warp * qpw + pi;
     const int last = a.pos0 + min(t, a.n - 1);                                 // this row's last position
     const int warp_last = a.pos0 + min(t_base + warp * qpw + qpw - 1, a.n - 1);  // the warp's
-    const float scale = 1.0f / sqrtf(float(HD));
+    // scores in log2 units (q scaled by log2(e) / sqrt(hd)), probabilities by exp2
+    const float scale = 1.4426950408889634f / sqrtf(float(HD));
     // q as A fragments: k-step ks, lane (gq, tq): its row at dims 16 ks + 2tq, +1 (hi in x, lo in y) and +8, +9 (z, w)
     uint4 qa[KS];
 #pragma unroll
@@ -675,12 +681,14 @@ __global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_co
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
                 // (a row past its last position in this round keeps its state: m_new = m_run)
-                const float m_new = fmaxf(m_run, mt);
-                const float alpha = m_run == m_new ? 1.f : (m_run == -INFINITY ? 0.f : expf(m_run - m_new));
+                const float m_cand = fmaxf(m_run, mt);
+                const bool hold = __all_sync(0xffffffffu, m_cand - m_run <= HOLD_LOG2);
+                const float m_new = hold ? m_run : m_cand;
+                const float alpha = m_run == m_new ? 1.f : (m_run == -INFINITY ? 0.f : exp2f(m_run - m_new));
                 float pr[4 * TPR], ps = 0.f;
     #pragma unroll
                 for (int e = 0; e < 4 * TPR; e++) {
-                    pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
+                    pr[e] = sc[e] == -INFINITY ? 0.f : exp2f(sc[e] - m_new);
                     ps += pr[e];
                 }
                 ps += __shfl_xor_sync(0xffffffffu, ps, 1);
@@ -756,12 +764,14 @@ __global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_co
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
                 // (a row past its last position in this tile keeps its state: m_new = m_run)
-                const float m_new = fmaxf(m_run, mt);
-                const float alpha = m_run == m_new ? 1.f : (m_run == -INFINITY ? 0.f : expf(m_run - m_new));
+                const float m_cand = fmaxf(m_run, mt);
+                const bool hold = __all_sync(0xffffffffu, m_cand - m_run <= HOLD_LOG2);
+                const float m_new = hold ? m_run : m_cand;
+                const float alpha = m_run == m_new ? 1.f : (m_run == -INFINITY ? 0.f : exp2f(m_run - m_new));
                 float pr[4], ps = 0.f;
     #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    pr[e] = sc[e] == -INFINITY ? 0.f : expf(sc[e] - m_new);
+                    pr[e] = sc[e] == -INFINITY ? 0.f : exp2f(sc[e] - m_new);
                     ps += pr[e];
                 }
                 ps += __shfl_xor_sync(0xffffffffu, ps, 1);
