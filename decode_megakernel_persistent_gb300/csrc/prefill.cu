@@ -36,7 +36,7 @@
 namespace ll {
 namespace {
 
-constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 256;
+constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 320;
 constexpr int NTERMS = 3;  // bf16 terms of an activation
 constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A and B alike)
 // A pipeline stage holds one K step of every A term and every B operand (the B
@@ -130,11 +130,16 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
-// One 128 x 128 tile of C per block (EPI_GATEUP: the same tile of the gate and
-// the up products, side by side in one 128 x 256 accumulator): warp 0 lane 0
-// feeds the pipeline with TMA, warp 1 lane 0 issues the MMAs, all eight warps run
-// the epilogue (warp w reads tensor-memory lanes, i.e. tile rows,
-// 32 (w % 4) .. 32 (w % 4) + 31, and half w / 4 of the tile's columns).
+// A persistent GEMM: block b takes the output tiles b, b + gridDim.x, ... (tile
+// t: 128 rows from row tile t / tiles_n, GN columns from column tile t % tiles_n;
+// EPI_GATEUP: the same columns of the gate and the up products, side by side in
+// one 128 x 256 accumulator). Warp 0 lane 0 feeds the stages with TMA, through
+// all of the block's tiles without a break; warp 1 lane 0 issues the MMAs of a
+// tile into one of ACC_BUFS tensor-memory accumulators and commits it to
+// acc_full; warps 2..9 run the epilogue of that accumulator (warp w reads
+// tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31 and half (w - 2) / 4 of the
+// columns), then hand it back through acc_empty. With two accumulators a
+// tile's epilogue runs under the next tile's products.
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
@@ -148,31 +153,37 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     // 256..383. The epilogue adds the terms' sums. Per K step of 16: one N = 256
     // product (and one N = 128) instead of two (three) N = 128 ones.
     constexpr bool TRANS = EPI != EPI_GATEUP;
-    constexpr uint32_t TCOLS = TRANS ? (NT == 2 ? 256 : 512) : 128 * NB;
     static_assert(!TRANS || NT == 2 || NT == 3, "the transposed product takes two or three terms");
+    constexpr uint32_t ACC_COLS = TRANS ? 128 * NT : 128 * NB;  // one accumulator
+    constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
+    constexpr uint32_t TCOLS = ACC_BUFS * ACC_COLS <= 256 ? 256 : 512;  // a power of two
+    constexpr int EPI_WARPS = 8;
+    static_assert(GTHREADS == 32 * (2 + EPI_WARPS), "producer, MMA and epilogue warps");
     extern __shared__ __align__(1024) uint8_t gsm[];
     uint8_t *tiles = gsm;
     uint64_t *full = reinterpret_cast<uint64_t *>(gsm + GSTAGES * STAGE);
     uint64_t *empty = full + GSTAGES;
-    uint64_t *done = empty + GSTAGES;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
-    volatile int *err = reinterpret_cast<volatile int *>(done + 2);
+    uint64_t *acc_full = empty + GSTAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(acc_empty + 2);
+    volatile int *err = reinterpret_cast<volatile int *>(acc_empty + 3);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+    const int tiles_n = (g.N + GN - 1) / GN, ntiles = tiles_n * ((g.M + GM - 1) / GM);
     const int iters = g.K / GK;  // K steps; each stage carries every term
-    // the B matrix of this tile's columns and the tile's first row in it
-    const int bsel = NB == 2 ? 0 : (n0 >= g.bsplit2 ? 2 : n0 >= g.bsplit1 ? 1 : 0);
-    const int brow = n0 - (bsel == 2 ? g.bsplit2 : bsel == 1 ? g.bsplit1 : 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < GSTAGES; s++) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[s])) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty[s])) : "memory");
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(done)) : "memory");
+        for (int b = 0; b < 2; b++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&acc_full[b])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&acc_empty[b])), "r"(EPI_WARPS)
+                         : "memory");
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *err = 0;
     }
-    if (warp == 0) {  // fp32 columns of tensor memory: TCOLS
+    if (warp == 0) {  // fp32 columns of tensor memory: ACC_BUFS accumulators
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          saddr(const_cast<uint32_t *>(tmem_slot))),
                      "n"(TCOLS)
@@ -184,163 +195,180 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        int sent = 0;
-        for (int it = 0; it < iters; it++) {
-            const int s = it % GSTAGES;
-            if (it >= GSTAGES && !mbar_wait(&empty[s], ((it / GSTAGES) - 1) & 1, g.timeout_ns, g.status, err)) break;
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[s])), "r"(STAGE)
-                         : "memory");
-            const int kc = it * GK;
-            const uint32_t dst = saddr(tiles + size_t(s) * STAGE);
+    if (warp == 0) {
+        if (lane == 0) {
+            int sent = 0;  // stages filled, over all of this block's tiles
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int m0 = (t / tiles_n) * GM, n0 = (t % tiles_n) * GN;
+                // the B matrix of this tile's columns and the tile's first row in it
+                const int bsel = NB == 2 ? 0 : (n0 >= g.bsplit2 ? 2 : n0 >= g.bsplit1 ? 1 : 0);
+                const int brow = n0 - (bsel == 2 ? g.bsplit2 : bsel == 1 ? g.bsplit1 : 0);
+                for (int it = 0; it < iters; it++) {
+                    const int s = sent % GSTAGES;
+                    if (sent >= GSTAGES &&
+                        !mbar_wait(&empty[s], ((sent / GSTAGES) - 1) & 1, g.timeout_ns, g.status, err)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(&full[s])),
+                                 "r"(STAGE)
+                                 : "memory");
+                    const int kc = it * GK;
+                    const uint32_t dst = saddr(tiles + size_t(s) * STAGE);
 #pragma unroll
-            for (int q = 0; q < NT; q++) tma2d(dst + q * GTILE, &g.a[q], kc, m0, &full[s]);
-            if (NB == 2) {
-                tma2d(dst + NT * GTILE, &g.b[0], kc, n0, &full[s]);
-                tma2d(dst + (NT + 1) * GTILE, &g.b[1], kc, n0, &full[s]);
-            } else {
-                tma2d(dst + NT * GTILE, &g.b[bsel], kc, brow, &full[s]);
+                    for (int q = 0; q < NT; q++) tma2d(dst + q * GTILE, &g.a[q], kc, m0, &full[s]);
+                    if (NB == 2) {
+                        tma2d(dst + NT * GTILE, &g.b[0], kc, n0, &full[s]);
+                        tma2d(dst + (NT + 1) * GTILE, &g.b[1], kc, n0, &full[s]);
+                    } else {
+                        tma2d(dst + NT * GTILE, &g.b[bsel], kc, brow, &full[s]);
+                    }
+                    sent++;
+                }
             }
-            sent++;
-        }
-        // never leave with copies in flight into this block's shared memory (after
-        // an error; normally the products have consumed every stage)
-        for (int q = sent > GSTAGES ? sent - GSTAGES : 0; q < sent; q++) {
-            const uint64_t t0 = now_ns();
-            while (!mbar_try(&full[q % GSTAGES], (q / GSTAGES) & 1) && now_ns() - t0 < g.timeout_ns) {
+            // never leave with copies in flight into this block's shared memory (after
+            // an error; normally the products have consumed every stage)
+            for (int q = sent > GSTAGES ? sent - GSTAGES : 0; q < sent; q++) {
+                const uint64_t t0 = now_ns();
+                while (!mbar_try(&full[q % GSTAGES], (q / GSTAGES) & 1) && now_ns() - t0 < g.timeout_ns) {
+                }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // gate/up: the two B tiles sit one after the other in the stage, so one
-        // N = 256 product covers both (rows 128.. of the operand are the up tile)
-        constexpr uint32_t idesc = TRANS ? idesc_bf16(GN, 2 * GM) : idesc_bf16(GM, GN * NB);
-        constexpr uint32_t idesc3 = idesc_bf16(GN, GM);  // TRANS: the third term
-        for (int it = 0; it < iters; it++) {
-            const int s = it % GSTAGES;
-            if (!mbar_wait(&full[s], (it / GSTAGES) & 1, g.timeout_ns, g.status, err)) break;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // gate/up: the two B tiles sit one after the other in the stage, so one
+            // N = 256 product covers both (rows 128.. of the operand are the up tile)
+            constexpr uint32_t idesc = TRANS ? idesc_bf16(GN, 2 * GM) : idesc_bf16(GM, GN * NB);
+            constexpr uint32_t idesc3 = idesc_bf16(GN, GM);  // TRANS: the third term
+            int used = 0, tl = 0;  // stages consumed, tiles done (this block)
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, tl++) {
+                const int buf = tl % ACC_BUFS, round = tl / ACC_BUFS;
+                // the accumulator is free once the epilogue of its previous tile read it
+                if (round > 0 && !mbar_wait(&acc_empty[buf], (round - 1) & 1, g.timeout_ns, g.status, err)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t acc_base = tmem + uint32_t(buf) * ACC_COLS;
+                for (int it = 0; it < iters; it++) {
+                    const int s = used % GSTAGES;
+                    if (!mbar_wait(&full[s], (used / GSTAGES) & 1, g.timeout_ns, g.status, err)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t base = saddr(tiles + size_t(s) * STAGE);
+#pragma unroll
+                    for (int q = 0; q < (TRANS ? 1 : NT); q++) {
+                        const uint64_t ad = smem_desc_sw128(TRANS ? base + GTILE * NT : base + q * GTILE);
+                        const uint64_t bd = smem_desc_sw128(TRANS ? base : base + GTILE * NT);
+#pragma unroll
+                        for (int kk = 0; kk < GK / 16; kk++) {
+                            const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(acc_base),
+                                "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
+                                : "memory");
+                            if (TRANS && NT == 3) {
+                                const uint64_t b3 = smem_desc_sw128(base + 2 * GTILE);
+                                asm volatile(
+                                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+                                        acc_base + 2u * GM),
+                                    "l"(ad + uint64_t(2 * kk)), "l"(b3 + uint64_t(2 * kk)), "r"(idesc3), "r"(acc)
+                                    : "memory");
+                            }
+                        }
+                    }
+                    // the stage is free once these products have read it
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     saddr(&empty[s]))
+                                 : "memory");
+                    used++;
+                }
+                if (!ok) break;
+                // the accumulator is complete once every product issued so far is
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 saddr(&acc_full[buf]))
+                             : "memory");
+            }
+        }
+    } else {
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        int tl = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, tl++) {
+            const int buf = tl % ACC_BUFS, round = tl / ACC_BUFS;
+            if (!mbar_wait(&acc_full[buf], round & 1, g.timeout_ns, g.status, err) || *err) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t base = saddr(tiles + size_t(s) * STAGE);
-#pragma unroll
-            for (int q = 0; q < (TRANS ? 1 : NT); q++) {
-                const uint64_t ad = smem_desc_sw128(TRANS ? base + GTILE * NT : base + q * GTILE);
-                const uint64_t bd = smem_desc_sw128(TRANS ? base : base + GTILE * NT);
-#pragma unroll
-                for (int kk = 0; kk < GK / 16; kk++) {
-                    const uint32_t acc = (it | q | kk) != 0 ? 1u : 0u;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-                        "l"(ad + uint64_t(2 * kk)), "l"(bd + uint64_t(2 * kk)), "r"(idesc), "r"(acc)
-                        : "memory");
-                    if (TRANS && NT == 3) {
-                        const uint64_t b3 = smem_desc_sw128(base + 2 * GTILE);
-                        asm volatile(
-                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + 2u * GM),
-                            "l"(ad + uint64_t(2 * kk)), "l"(b3 + uint64_t(2 * kk)), "r"(idesc3), "r"(acc)
-                            : "memory");
-                    }
-                }
-            }
-            // the stage is free once these products have read it
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             saddr(&empty[s]))
-                         : "memory");
-        }
-        // the accumulators are complete once every product issued so far is
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(done))
-                     : "memory");
-    }
-    __syncwarp();
-    const bool ok = mbar_wait(done, 0, g.timeout_ns, g.status, err) && !*err;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = m0 + quarter * 32 + lane;
-    // (the wait is in the same statement as the load, so no use of the
-    // registers can be placed before it)
-    auto ld16 = [&](uint32_t col, uint32_t (&r)[16]) {
-        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + col;
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-            "%14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr)
-            : "memory");
-    };
-    if (ok && TRANS) {
-        // lane: output column n0 + 32 quarter + lane; columns of the accumulator:
-        // positions (term 0 at c, term 1 at 128 + c, term 2 at 256 + c), this
-        // warp's half of them
-        const int col = n0 + quarter * 32 + lane;
+            const int m0 = (t / tiles_n) * GM, n0 = (t % tiles_n) * GN;
+            const uint32_t acc_base = tmem + uint32_t(buf) * ACC_COLS;
+            // (the wait is in the same statement as the load, so no use of the
+            // registers can be placed before it)
+            auto ld16 = [&](uint32_t col, uint32_t (&r)[16]) {
+                const uint32_t taddr = acc_base + (uint32_t(quarter * 32) << 16) + col;
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                    "%13, %14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
+                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                      "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                      "=r"(r[15])
+                    : "r"(taddr)
+                    : "memory");
+            };
+            if (TRANS) {
+                // lane: output column n0 + 32 quarter + lane; columns of the accumulator:
+                // positions (term 0 at c, term 1 at 128 + c, term 2 at 256 + c), this
+                // warp's half of them
+                const int col = n0 + quarter * 32 + lane;
 #pragma unroll 1
-        for (int c0 = half * (GM / 2); c0 < (half + 1) * (GM / 2); c0 += 16) {
-            uint32_t r[16], u[16], w[16];
-            ld16(uint32_t(c0), r);
-            ld16(uint32_t(GM + c0), u);
-            if (NT == 3) ld16(uint32_t(2 * GM + c0), w);
-            if (col >= g.N) continue;
-            float *const cp = g.c + size_t(m0 + c0) * g.ldc + col;
-            float old[16];
-            if (EPI == EPI_ADD) {  // all 16 loads in flight before the first store
+                for (int c0 = half * (GM / 2); c0 < (half + 1) * (GM / 2); c0 += 16) {
+                    uint32_t r[16], u[16], w[16];
+                    ld16(uint32_t(c0), r);
+                    ld16(uint32_t(GM + c0), u);
+                    if (NT == 3) ld16(uint32_t(2 * GM + c0), w);
+                    if (col >= g.N) continue;
+                    float *const cp = g.c + size_t(m0 + c0) * g.ldc + col;
+                    float old[16];
+                    if (EPI == EPI_ADD) {  // all 16 loads in flight before the first store
 #pragma unroll
-                for (int e = 0; e < 16; e++) old[e] = m0 + c0 + e < g.M ? cp[size_t(e) * g.ldc] : 0.f;
-            }
+                        for (int e = 0; e < 16; e++) old[e] = m0 + c0 + e < g.M ? cp[size_t(e) * g.ldc] : 0.f;
+                    }
 #pragma unroll
-            for (int e = 0; e < 16; e++) {
-                float v = __uint_as_float(r[e]) + __uint_as_float(u[e]);
-                if (NT == 3) v += __uint_as_float(w[e]);
-                if (EPI == EPI_ADD) v += old[e];
-                if (m0 + c0 + e < g.M) cp[size_t(e) * g.ldc] = v;
-            }
-        }
-    } else if (ok && !TRANS) {
+                    for (int e = 0; e < 16; e++) {
+                        float v = __uint_as_float(r[e]) + __uint_as_float(u[e]);
+                        if (NT == 3) v += __uint_as_float(w[e]);
+                        if (EPI == EPI_ADD) v += old[e];
+                        if (m0 + c0 + e < g.M) cp[size_t(e) * g.ldc] = v;
+                    }
+                }
+            } else {  // EPI_GATEUP: row m0 + 32 quarter + lane, gate at c, up at 128 + c
+                const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
-        for (int c0 = half * (GN / 2); c0 < (half + 1) * (GN / 2); c0 += 16) {
-            uint32_t r[16];
-            ld16(uint32_t(c0), r);
-            uint32_t u[16];
-            if (EPI == EPI_GATEUP) ld16(uint32_t(128 + c0), u);
-            const int col0 = n0 + c0;
-            if (row >= g.M || col0 >= g.N) continue;
-            const size_t at = size_t(row) * g.ldc + col0;
-            const bool whole = col0 + 16 <= g.N;  // 16 columns at once (N is a multiple of 16 here)
-            if (EPI == EPI_STORE || EPI == EPI_ADD) {
-                float4 *cp = reinterpret_cast<float4 *>(g.c + at);
+                for (int c0 = half * (GN / 2); c0 < (half + 1) * (GN / 2); c0 += 16) {
+                    uint32_t r[16], u[16];
+                    ld16(uint32_t(c0), r);
+                    ld16(uint32_t(128 + c0), u);
+                    const int col0 = n0 + c0;
+                    if (row >= g.M || col0 + 16 > g.N) continue;  // (N is a multiple of 16 here)
+                    const size_t at = size_t(row) * g.ldc + col0;
+                    constexpr int NW = gterms(EPI_ADD);  // the down GEMM's terms
+                    uint32_t w[NW][8];
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                           __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                    if (!whole) break;
-                    if (EPI == EPI_ADD) {
-                        const float4 o = cp[q];
-                        v.x += o.x;
-                        v.y += o.y;
-                        v.z += o.z;
-                        v.w += o.w;
+                    for (int j = 0; j < 16; j += 2) {
+                        float a2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const float z = __uint_as_float(r[j + e]);
+                            a2[e] = z / (1.0f + expf(-z)) * __uint_as_float(u[j + e]);
+                        }
+#pragma unroll
+                        for (int q = 0; q < NW; q++) {
+                            const __nv_bfloat162 t2 = __floats2bfloat162_rn(a2[0], a2[1]);
+                            w[q][j / 2] = *reinterpret_cast<const uint32_t *>(&t2);
+                            a2[0] -= __low2float(t2);
+                            a2[1] -= __high2float(t2);
+                        }
                     }
-                    cp[q] = v;
-                }
-            } else {
-                constexpr int NW = gterms(EPI_ADD);  // the down GEMM's terms
-                uint32_t w[NW][8];
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    float a2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const float z = __uint_as_float(r[j + e]);
-                        a2[e] = z / (1.0f + expf(-z)) * __uint_as_float(u[j + e]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < NW; q++) {
-                        const __nv_bfloat162 t2 = __floats2bfloat162_rn(a2[0], a2[1]);
-                        w[q][j / 2] = *reinterpret_cast<const uint32_t *>(&t2);
-                        a2[0] -= __low2float(t2);
-                        a2[1] -= __high2float(t2);
-                    }
-                }
-                if (whole) {
 #pragma unroll
                     for (int q = 0; q < NW; q++) {
                         uint4 *dst = reinterpret_cast<uint4 *>(g.act[q] + at);
@@ -349,6 +377,10 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
                     }
                 }
             }
+            // this warp is done reading the accumulator: hand it back to the MMAs
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&acc_empty[buf])) : "memory");
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -907,8 +939,9 @@ int gemm(const TensorMap *a, const TensorMap *bm, int nb, int s1, int s2, int M,
             return LL_ERR_CUDA;
         attr = true;
     }
-    const dim3 grid((N + GN - 1) / GN, (M + GM - 1) / GM);
-    k_gemm<EPI><<<grid, GTHREADS, SMEM, st>>>(g);
+    // persistent: at most one block per SM, each walking its share of the tiles
+    const int ntiles = ((N + GN - 1) / GN) * ((M + GM - 1) / GM);
+    k_gemm<EPI><<<std::min(ntiles, p.nsm), GTHREADS, SMEM, st>>>(g);
     return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
