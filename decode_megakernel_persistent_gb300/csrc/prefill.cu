@@ -168,7 +168,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(acc_empty + 2);
     volatile int *err = reinterpret_cast<volatile int *>(acc_empty + 3);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_n = (g.N + GN - 1) / GN, ntiles = tiles_n * ((g.M + GM - 1) / GM);
+    const int tiles_n = (g.N + GN - 1) / GN, tiles_m = (g.M + GM - 1) / GM, ntiles = tiles_n * tiles_m;
+    // gate/up: row tiles vary fastest, so the blocks sharing a weight tile run
+    // together and read it from HBM once; the others: column tiles fastest
+    auto tile_m = [&](int t) { return EPI == EPI_GATEUP ? t % tiles_m : t / tiles_n; };
+    auto tile_n = [&](int t) { return EPI == EPI_GATEUP ? t / tiles_m : t % tiles_n; };
     const int iters = g.K / GK;  // K steps; each stage carries every term
     if (threadIdx.x == 0) {
         for (int s = 0; s < GSTAGES; s++) {
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             int sent = 0;  // stages filled, over all of this block's tiles
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int m0 = (t / tiles_n) * GM, n0 = (t % tiles_n) * GN;
+                const int m0 = tile_m(t) * GM, n0 = tile_n(t) * GN;
                 // the B matrix of this tile's columns and the tile's first row in it
                 const int bsel = NB == 2 ? 0 : (n0 >= g.bsplit2 ? 2 : n0 >= g.bsplit1 ? 1 : 0);
                 const int brow = n0 - (bsel == 2 ? g.bsplit2 : bsel == 1 ? g.bsplit1 : 0);
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             const int buf = tl % ACC_BUFS, round = tl / ACC_BUFS;
             if (!mbar_wait(&acc_full[buf], round & 1, g.timeout_ns, g.status, err) || *err) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int m0 = (t / tiles_n) * GM, n0 = (t % tiles_n) * GN;
+            const int m0 = tile_m(t) * GM, n0 = tile_n(t) * GN;
             const uint32_t acc_base = tmem + uint32_t(buf) * ACC_COLS;
             // (the wait is in the same statement as the load, so no use of the
             // registers can be placed before it)
