@@ -130,16 +130,15 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
-// A persistent GEMM: block b takes the output tiles b, b + gridDim.x, ... (tile
-// t: 128 rows from row tile t / tiles_n, GN columns from column tile t % tiles_n;
-// EPI_GATEUP: the same columns of the gate and the up products, side by side in
-// one 128 x 256 accumulator). Warp 0 lane 0 feeds the stages with TMA, through
-// all of the block's tiles without a break; warp 1 lane 0 issues the MMAs of a
-// tile into one of ACC_BUFS tensor-memory accumulators and commits it to
-// acc_full; warps 2..9 run the epilogue of that accumulator (warp w reads
-// tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31 and half (w - 2) / 4 of the
-// columns), then hand it back through acc_empty. With two accumulators a
-// tile's epilogue runs under the next tile's products.
+// A persistent GEMM: block b takes the output tiles b, b + gridDim.x, ... (a tile:
+// 128 rows by GN columns; EPI_GATEUP: the same columns of the gate and the up
+// products, side by side in one 128 x 256 accumulator). Warp 0 lane 0 feeds the
+// stages with TMA, through all of the block's tiles without a break; warp 1 lane
+// 0 issues the MMAs of a tile into one of two tensor-memory accumulators (256
+// columns each) and commits it to acc_full; warps 2..9 run the epilogue of that
+// accumulator (warp w reads tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31
+// and half (w - 2) / 4 of the columns), then hand it back through acc_empty, so
+// a tile's epilogue runs under the next tile's products.
 template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
     constexpr int NB = EPI == EPI_GATEUP ? 2 : 1;  // B operands (accumulators)
@@ -149,12 +148,12 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     // EPI_STORE and EPI_ADD run transposed: the weight tile is the MMA's A (128
     // output columns as the accumulator's lanes) and terms 0 and 1, adjacent in
     // the stage, are one 256-row B (accumulator columns: term 0's 128 positions,
-    // then term 1's); a third term is an N = 128 product of its own into columns
-    // 256..383. The epilogue adds the terms' sums. Per K step of 16: one N = 256
-    // product (and one N = 128) instead of two (three) N = 128 ones.
+    // then term 1's); a third term is an N = 128 product of its own, added into
+    // term 0's columns. The epilogue adds the two halves. Per K step of 16: one
+    // N = 256 product (and one N = 128) instead of two (three) N = 128 ones.
     constexpr bool TRANS = EPI != EPI_GATEUP;
     static_assert(!TRANS || NT == 2 || NT == 3, "the transposed product takes two or three terms");
-    constexpr uint32_t ACC_COLS = TRANS ? 128 * NT : 128 * NB;  // one accumulator
+    constexpr uint32_t ACC_COLS = TRANS ? 2 * 128 : 128 * NB;  // one accumulator
     constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
     constexpr uint32_t TCOLS = ACC_BUFS * ACC_COLS <= 256 ? 256 : 512;  // a power of two
     constexpr int EPI_WARPS = 8;
@@ -244,7 +243,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             // gate/up: the two B tiles sit one after the other in the stage, so one
             // N = 256 product covers both (rows 128.. of the operand are the up tile)
             constexpr uint32_t idesc = TRANS ? idesc_bf16(GN, 2 * GM) : idesc_bf16(GM, GN * NB);
-            constexpr uint32_t idesc3 = idesc_bf16(GN, GM);  // TRANS: the third term
+            constexpr uint32_t idesc3 = idesc_bf16(GN, GM);  // TRANS: the third term (into term 0's columns)
             int used = 0, tl = 0;  // stages consumed, tiles done (this block)
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, tl++) {
@@ -277,9 +276,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
                                 const uint64_t b3 = smem_desc_sw128(base + 2 * GTILE);
                                 asm volatile(
                                     "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-                                        acc_base + 2u * GM),
-                                    "l"(ad + uint64_t(2 * kk)), "l"(b3 + uint64_t(2 * kk)), "r"(idesc3), "r"(acc)
+                                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(acc_base),
+                                    "l"(ad + uint64_t(2 * kk)), "l"(b3 + uint64_t(2 * kk)), "r"(idesc3), "r"(1u)
                                     : "memory");
                             }
                         }
@@ -321,15 +319,14 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
             };
             if (TRANS) {
                 // lane: output column n0 + 32 quarter + lane; columns of the accumulator:
-                // positions (term 0 at c, term 1 at 128 + c, term 2 at 256 + c), this
-                // warp's half of them
+                // positions (terms 0 and 2 at c, term 1 at 128 + c), this warp's half
+                // of them
                 const int col = n0 + quarter * 32 + lane;
 #pragma unroll 1
                 for (int c0 = half * (GM / 2); c0 < (half + 1) * (GM / 2); c0 += 16) {
-                    uint32_t r[16], u[16], w[16];
+                    uint32_t r[16], u[16];
                     ld16(uint32_t(c0), r);
                     ld16(uint32_t(GM + c0), u);
-                    if (NT == 3) ld16(uint32_t(2 * GM + c0), w);
                     if (col >= g.N) continue;
                     float *const cp = g.c + size_t(m0 + c0) * g.ldc + col;
                     float old[16];
@@ -340,7 +337,6 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
 #pragma unroll
                     for (int e = 0; e < 16; e++) {
                         float v = __uint_as_float(r[e]) + __uint_as_float(u[e]);
-                        if (NT == 3) v += __uint_as_float(w[e]);
                         if (EPI == EPI_ADD) v += old[e];
                         if (m0 + c0 + e < g.M) cp[size_t(e) * g.ldc] = v;
                     }
