@@ -83,6 +83,25 @@ def test_llama1b_prefill_of_64_positions():
     pr.close()
 
 
+@pytest.mark.parametrize("shape", [
+    # 128-dim heads, four query heads per KV head: two K/V tiles per softmax round
+    synth.ModelShape("h1024hd128", 2, 1024, 8, 2, 128, 2048, 4096, True),
+    # eight query heads per KV head: one query position per warp
+    synth.ModelShape("h1024gqa8", 2, 1024, 16, 2, 64, 2048, 4096, True),
+], ids=["hd128", "gqa8"])
+def test_prefill_head_layouts(shape):
+    # 141 positions: two 128-row GEMM tiles, the second ragged, and an odd number
+    # of 16-position K/V tiles (the last two-tile round has one)
+    pr = Pair(shape, 160, gain_jitter=0.25)
+    toks = synth.make_tokens(shape.vocab, 141, seed=7)
+    got, nxt = _prefill(pr, toks, 0)
+    ref = _oracle_run(pr, toks, 0)
+    compare_logits(got, ref, f"{shape.name} prefill: last logits")
+    check_token(nxt, ref, f"{shape.name} prefill")
+    pr.kv_close(slice(0, 141))
+    pr.close()
+
+
 def test_prefill_argument_checks():
     shape = synth.TINY
     w = synth.make_weights(shape, seed=0, device="cuda")
