@@ -154,6 +154,18 @@ def test_batch_sequences_are_independent():
     np.testing.assert_array_equal(a[1][:, 0], b[1][:, 0])
 
 
+@pytest.mark.parametrize("n", [2, 4])
+@pytest.mark.parametrize("flash", ["0", "1"], ids=["block-softmax", "per-warp"])
+def test_batch_128_dim_heads(n, flash, monkeypatch):
+    # 128-dim heads (four query heads per KV head) in both attention variants:
+    # two sequences on CUDA-core pages, four on tensor-core pages
+    monkeypatch.setenv("LL_ATTN_FLASH", flash)
+    shape = synth.ModelShape("h1024hd128", 2, 1024, 8, 2, 128, 2048, 4096, True)
+    fills = [150 + 37 * b for b in range(n)]
+    orcs, first, out = run_batch(shape, n, fills, 4, jitter=0.25, expect_cc=(n == 2))
+    check_against_oracles(orcs, first, out, fills, 4, f"hd128 batch {n}")
+
+
 def test_batch_argument_checks():
     shape = SMALL
     w = synth.make_weights(shape, seed=0, device="cuda")
