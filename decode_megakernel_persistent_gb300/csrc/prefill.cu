@@ -58,6 +58,29 @@ __device__ __forceinline__ uint64_t now_ns() {
     return t;
 }
 
+// Programmatic dependent launch (the per-layer kernels of a prefill): a kernel
+// lets the next one in the stream start its blocks as soon as it runs itself
+// (their set-up then overlaps its tail), and waits, before it reads anything
+// the previous kernel wrote, until that kernel has finished and its writes are
+// visible. Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -173,6 +196,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     auto tile_m = [&](int t) { return EPI == EPI_GATEUP ? t % tiles_m : t / tiles_n; };
     auto tile_n = [&](int t) { return EPI == EPI_GATEUP ? t / tiles_m : t % tiles_n; };
     const int iters = g.K / GK;  // K steps; each stage carries every term
+    pdl_release();
     if (threadIdx.x == 0) {
         for (int s = 0; s < GSTAGES; s++) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[s])) : "memory");
@@ -197,6 +221,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // the operands (and, adding into it, C) as the previous kernel left them
 
     if (warp == 0) {
         if (lane == 0) {
@@ -447,6 +472,8 @@ __device__ __forceinline__ void norm_store8(const float (&v)[8], float r, const 
 
 __global__ void k_pf_norm_split(const float *x, const uint16_t *g, int H, float eps, Terms h) {
     __shared__ float red[32];
+    pdl_release();
+    pdl_wait();
     const int groups = H / 8, step = int(blockDim.x), j = int(threadIdx.x);
     const bool single = groups <= step;
     const float *xr = x + size_t(blockIdx.x) * H;
@@ -497,6 +524,8 @@ __device__ __forceinline__ uint2 bf16x4(float a, float b, float c, float d) {
 
 __global__ void k_pf_rope_kv(float *qkv, const float2 *rope, int pos0, int nq, int nkv, int hd, uint16_t *kc,
                              uint16_t *vc, size_t layer_base, int max_seq) {
+    pdl_release();
+    pdl_wait();
     const int t = blockIdx.x, half = hd / 2, quads = half / 4, pos = pos0 + t;
     const int qd = nq * hd, kd = nkv * hd;
     float *row = qkv + size_t(t) * (qd + 2 * kd);
@@ -597,6 +626,7 @@ __global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_co
     const int t_base = (gridDim.x - 1 - int(blockIdx.x)) * qpb;  // the longest walks first
     const int block_last = a.pos0 + min(t_base + qpb - 1, a.n - 1);
     const int ntiles = block_last / 16 + 1;
+    pdl_release();
     if (threadIdx.x == 0) {
         for (int st = 0; st < AT_STAGES; st++) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[st])) : "memory");
@@ -607,6 +637,7 @@ __global__ void __launch_bounds__((AT_NW + 1) * 32) k_pf_attn_tc(const __grid_co
     }
     if (threadIdx.x < 4) zrow[threadIdx.x] = 0u;
     __syncthreads();
+    pdl_wait();  // q (and the cache entries) as the previous kernel left them
     volatile int *errp = &err;
     if (warp == AT_NW) {  // producer
         if (lane == 0) {
@@ -867,11 +898,9 @@ int launch_attention(const KParams &p, const PrefillBufs &b, int layer, int pos0
     a.timeout_ns = p.timeout_ns;
     const int qpb = AT_NW * (p.nq / p.nkv <= 4 ? 2 : 1);
     const dim3 grid((n + qpb - 1) / qpb, p.nkv);
-    if (p.hd == 64)
-        k_pf_attn_tc<64><<<grid, (AT_NW + 1) * 32, 0, st>>>(a);
-    else
-        k_pf_attn_tc<128><<<grid, (AT_NW + 1) * 32, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+    const cudaError_t e = p.hd == 64 ? launch_pdl(k_pf_attn_tc<64>, grid, dim3((AT_NW + 1) * 32), 0, st, a)
+                                     : launch_pdl(k_pf_attn_tc<128>, grid, dim3((AT_NW + 1) * 32), 0, st, a);
+    return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -941,8 +970,9 @@ int gemm(const TensorMap *a, const TensorMap *bm, int nb, int s1, int s2, int M,
     }
     // persistent: at most one block per SM, each walking its share of the tiles
     const int ntiles = ((N + GN - 1) / GN) * ((M + GM - 1) / GM);
-    k_gemm<EPI><<<std::min(ntiles, p.nsm), GTHREADS, SMEM, st>>>(g);
-    return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+    return launch_pdl(k_gemm<EPI>, dim3(std::min(ntiles, p.nsm)), dim3(GTHREADS), size_t(SMEM), st, g) == cudaSuccess
+               ? LL_OK
+               : LL_ERR_CUDA;
 }
 
 }  // namespace
@@ -1037,22 +1067,27 @@ int launch_prefill(const KParams &p, const LayerW *host_layers, PrefillBufs &b, 
         const TensorMap *m = &b.m_w[size_t(l) * 7];
         const size_t lb = size_t(l) * per_layer;
         const int ld = qd + 2 * kd;
-        k_pf_norm_split<<<n, norm_threads, 0, st>>>(b.x, w.attn_norm, H, p.eps, th);
-        if (qd % GN == 0 && kd % GN == 0) {  // q, k and v in one GEMM over the stacked rows
+        auto ok = [](cudaError_t e) { return e == cudaSuccess ? LL_OK : LL_ERR_CUDA; };
+        // every launch of the layer's chain lets the next one start early (see pdl_wait)
+        rc = ok(launch_pdl(k_pf_norm_split, dim3(n), dim3(norm_threads), 0, st, (const float *)b.x,
+                           (const uint16_t *)w.attn_norm, H, p.eps, th));
+        if (rc == LL_OK && qd % GN == 0 && kd % GN == 0) {  // q, k and v in one GEMM over the stacked rows
             rc = gemm<EPI_STORE>(b.m_h, m, 3, qd, qd + kd, n, ld, H, b.qkv, ld, nullptr, p, st);
-        } else {
+        } else if (rc == LL_OK) {
             rc = gemm<EPI_STORE>(b.m_h, m, 1, 0, 0, n, qd, H, b.qkv, ld, nullptr, p, st);
             if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m + 1, 1, 0, 0, n, kd, H, b.qkv + qd, ld, nullptr, p, st);
             if (rc == LL_OK) rc = gemm<EPI_STORE>(b.m_h, m + 2, 1, 0, 0, n, kd, H, b.qkv + qd + kd, ld, nullptr, p, st);
         }
-        if (rc != LL_OK) break;
-        k_pf_rope_kv<<<n, 256, 0, st>>>(b.qkv, p.rope_cs, pos0, p.nq, p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq);
-        rc = launch_attention(p, b, l, pos0, n, to, st);
+        if (rc == LL_OK)
+            rc = ok(launch_pdl(k_pf_rope_kv, dim3(n), dim3(256), 0, st, b.qkv, (const float2 *)p.rope_cs, pos0, p.nq,
+                               p.nkv, p.hd, p.k_cache, p.v_cache, lb, p.max_seq));
+        if (rc == LL_OK) rc = launch_attention(p, b, l, pos0, n, to, st);
         if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_o, m + 3, 1, 0, 0, n, H, qd, b.x, H, nullptr, p, st);
-        if (rc != LL_OK) break;
-        k_pf_norm_split<<<n, norm_threads, 0, st>>>(b.x, w.mlp_norm, H, p.eps, th);
+        if (rc == LL_OK)
+            rc = ok(launch_pdl(k_pf_norm_split, dim3(n), dim3(norm_threads), 0, st, (const float *)b.x,
+                               (const uint16_t *)w.mlp_norm, H, p.eps, th));
         // gate and up in one GEMM (two accumulators), silu(gate) * up as terms
-        rc = gemm<EPI_GATEUP>(b.m_h, m + 4, 2, 0, 0, n, I, H, nullptr, I, &ta, p, st);
+        if (rc == LL_OK) rc = gemm<EPI_GATEUP>(b.m_h, m + 4, 2, 0, 0, n, I, H, nullptr, I, &ta, p, st);
         if (rc == LL_OK) rc = gemm<EPI_ADD>(b.m_a, m + 6, 1, 0, 0, n, H, I, b.x, H, nullptr, p, st);
     }
     if (rc != LL_OK) return rc;
