@@ -4,25 +4,28 @@
 // the step before it: every position of the prompt goes through every layer,
 // which turns each projection into a matrix product of (positions x width) by
 // the weight matrix, filling the KV cache for the decode steps that follow.
-// Here every projection is a tcgen05 GEMM (the fifth-generation tensor cores):
-// TMA brings 128 x 64 bf16 tiles of both operands into shared memory in the
-// 128-byte swizzle through a 3- or 4-stage mbarrier pipeline, one thread issues
-// tcgen05.mma (M = 128 positions, N = 128 outputs or 256 for gate and up
-// together, K = 16 per instruction) into a tensor-memory accumulator, and eight
-// warps read it back with tcgen05.ld for the epilogue. The decode path keeps activations in fp32; a bf16 product with
-// one term of them misses the logits' bar (and with two, bf16 roundings of the
-// K/V written to the cache flip measurably more often than in fp32), so each
-// activation matrix enters as three bf16 terms (t0 = bf16(x), t1 = bf16(x - t0),
-// t2 = bf16(x - t0 - t1): the 24 bits of an fp32 value) and all their products
-// accumulate in the same tensor-memory tile: the GEMM runs its K loop three
-// times.
+// Here every projection is a persistent tcgen05 GEMM (the fifth-generation
+// tensor cores): one block per SM walks its share of the output tiles; TMA brings
+// 128 x 64 bf16 tiles of the operands into shared memory in the 128-byte swizzle
+// through a 3- or 4-stage mbarrier pipeline that runs across tile boundaries; one
+// thread issues tcgen05.mma (K = 16 per instruction, N = 256: the positions by
+// the gate and up tiles together, or, transposed, the weight tile by two stacked
+// activation terms) into one of two tensor-memory accumulators; eight warps read
+// the other back with tcgen05.ld for the epilogue meanwhile. The decode path
+// keeps activations in fp32, and a bf16 product with one term of them misses the
+// logits' bar, so each activation matrix enters as bf16 terms (t0 = bf16(x),
+// t1 = bf16(x - t0), t2 = bf16(x - t0 - t1)): three for the Q/K/V GEMM, whose K/V
+// go to the cache (the 24 bits of an fp32 value), two for the others (16 bits);
+// a pipeline stage carries one K step of every term, so each weight tile is
+// loaded once for all of them.
 //
-// Per layer: RMSNorm into the terms; Q, K, V GEMMs; RoPE with the K/V rounded
-// to bf16 into the cache; causal attention over the cache (mma.sync tiles, one
-// warp per query position and KV head); O GEMM added into the residual;
-// RMSNorm; one GEMM for gate and up (two tensor-memory accumulators) whose
-// epilogue forms silu(gate) * up in terms; down GEMM added into the residual.
-// Then the last position's final norm, LM head and argmax.
+// Per layer: RMSNorm into the terms; Q, K, V in one GEMM; RoPE with the K/V
+// rounded to bf16 into the cache; causal attention over the cache (mma.sync
+// tiles, two query positions x the KV head's query heads per warp); O GEMM added
+// into the residual; RMSNorm; one GEMM for gate and up whose epilogue forms
+// silu(gate) * up in terms; down GEMM added into the residual. These kernels are
+// launched as programmatic dependents (see pdl_wait). Then the last position's
+// final norm, LM head and argmax.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,9 +42,10 @@ namespace {
 constexpr int GM = 128, GN = 128, GK = 64, GTHREADS = 320;
 constexpr int NTERMS = 3;  // bf16 terms of an activation
 constexpr uint32_t GTILE = GM * GK * 2;  // bytes of one 128 x 64 bf16 tile (A and B alike)
-// A pipeline stage holds one K step of every A term and every B operand (the B
-// tile is loaded once for the three terms): 64 KB with one B operand, 80 KB with
-// two; as many stages as fit the 227 KB a block may have.
+// A pipeline stage holds one K step of every A term and every B operand (each B
+// tile is loaded once for all the terms): 16 KB per tile, 64 KB for Q/K/V (three
+// terms) and gate/up (two terms, two B operands), 48 KB for O and down; as many
+// stages as fit in 192 KB of the 227 KB a block may have.
 __host__ __device__ constexpr int gstages(int tiles) { return 196608 / (tiles * int(GTILE)); }  // tiles per stage
 // The A terms a GEMM takes: three for the Q, K, V projection (its K/V are the
 // cache entries the decode steps read, rounded to bf16, so they follow the fp32
